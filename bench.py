@@ -1,0 +1,369 @@
+"""Benchmark: varlen flash attention forward + backward on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch: forward (out, lse) then backward
+(row-dot pre-pass, dK/dV, dQ), on the dense causal workload B=4 x L=4096, H=32, head_dim 128,
+bf16, packed as 4 cu_seqlens segments (inputs are synthetic, seeded, resident in HBM; each of
+q/k/v/out/dout is 134 MB, larger than the 129 MB L2, so no flush is needed between steps).
+
+Prints ONE JSON line (rank 0):
+  value        fwd+bwd TFLOP/s over unmasked pairs (whole job, all ranks), CUDA-event timed
+  fwd_tflops   forward-only TFLOP/s from the same timed region
+  e2e          same metric through the C ABI with pinned host buffers, H2D/D2H inside the timing
+  roofline     dominant kernel: algorithmic FLOPs per launch / its average event-timed duration
+  cpu_baseline the fp64 oracle (test infrastructure) on a bounded sample, host cores
+  clocks       nvidia-smi samples taken during the timed region
+
+``--impl reference`` times the fp64 CPU oracle on the same workload instead (rank 0 only).
+Multi-GPU (torchrun): every rank runs its own replica of the workload (weak scaling; the
+ranks exchange nothing in the data path; a barrier and a max-reduce of the timing only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+from variable_length_flash_gb300 import flops as F  # noqa: E402
+
+WORKLOAD = "dense4x4096_bf16_causal"
+
+
+# ------------------------------------------------------------------------------ helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples every 200 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc, self.thread = index, [], None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "", 1).isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def oracle_sample(w, x_cpu, units: int):
+    """Time the fp64 oracle on `units` (sequence, head) units of the workload, fwd + bwd.
+    Returns (seconds, pairs) -- test infrastructure, run only for the CPU baseline."""
+    import numpy as np
+
+    from oracle import attention as orc
+    cu = x_cpu["cu_seqlens_q"].tolist()
+    pairs, t0 = 0, time.perf_counter()
+    for u in range(units):
+        s, h = u % w.num_seqs, (u * 7) % w.h_q
+        a, b = cu[s], cu[s + 1]
+        g = w.h_q // w.h_kv
+        q = x_cpu["q"][a:b, h].double().numpy()
+        k = x_cpu["k"][a:b, h // g].double().numpy()
+        v = x_cpu["v"][a:b, h // g].double().numpy()
+        do = x_cpu["dout"][a:b, h].double().numpy()
+        orc.head_backward(q, k, v, do, w.softmax_scale, w.causal, w.window)
+        pairs += F.visible_pairs(b - a, b - a, w.causal, w.window)
+    del np
+    return time.perf_counter() - t0, pairs
+
+
+def cpu_inputs(w, units):
+    """Host copies of the sequences the CPU sample touches (drawn on the host generator)."""
+    return W.make_inputs(w, seed=0, device="cpu")
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = W.workload(args.workload)
+    fpp = F.flops_per_pair(w.d_qk, w.d_v)["fwd_bwd"]
+    x = cpu_inputs(w, 1)
+    for _ in range(args.warmup):
+        oracle_sample(w, x, 1)
+    times, pairs = [], 0
+    for _ in range(args.steps):
+        dt, p = oracle_sample(w, x, 1)
+        times.append(dt)
+        pairs += p
+    total = sum(times)
+    value = pairs * fpp / total / 1e12
+    cores = os.cpu_count()
+    sample = (f"{args.steps} x one (sequence, head) unit of {w.name} "
+              f"({w.lengths_q[0]} rows, fwd+bwd, fp64 numpy; BLAS threads = host cores)")
+    line = {"impl": "reference", "metric": "attention TFLOP/s fwd+bwd (unmasked pairs)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-units", type=int, default=3,
+                    help="(sequence, head) units of the workload for the CPU oracle baseline")
+    args = ap.parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import variable_length_flash_gb300 as vlf
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    w = W.workload(args.workload)
+    x = W.make_inputs(w, seed=rank, device=dev, with_dout=True)
+    fpp = F.flops_per_pair(w.d_qk, w.d_v)
+    pairs = F.workload_pairs(w)
+    dt = x["q"].dtype
+    out = torch.empty((w.total_q, w.h_q, w.d_v), dtype=dt, device=dev)
+    lse = torch.empty((w.h_q, w.total_q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    ws = torch.empty(vlf.vlf_attn_varlen_bwd_workspace_size(
+        w.total_q, w.total_kv, w.h_q, w.h_kv, w.d_qk, w.d_v, dt), dtype=torch.uint8, device=dev)
+    kw = dict(scale=w.scale, causal=w.causal, window=w.window, bias=x["bias"])
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        vlf.vlf_attn_varlen_fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_kv"],
+                                w.max_seqlen_q, w.max_seqlen_kv, out=out, lse=lse, **kw)
+        vlf.vlf_attn_varlen_bwd(x["dout"], x["q"], x["k"], x["v"], out, lse, x["cu_seqlens_q"],
+                                x["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv, dq=dq, dk=dk,
+                                dv=dv, workspace=ws, stage_events=None if ev is None else ev[1:],
+                                **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = vlf.vlf_check_error()
+    assert st == 0, vlf.vlf_status_string(st)
+
+    # events: per step [fwd start, bwd start(=fwd end), after rowdot, after dkdv, after dq]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + vlf.VLF_BWD_STAGES)]
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    n0 = vlf.vlf_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = vlf.vlf_launch_count() - n0
+    barrier(world)
+    clocks = sampler.stop()
+    st = vlf.vlf_check_error()
+    assert st == 0, vlf.vlf_status_string(st)
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ms_step = ms_total / args.steps
+    stage_names = ["fwd"] + list(vlf.BWD_STAGE_NAMES)
+    stage_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, n in enumerate(stage_names)}
+    fwd_ms = stage_ms["fwd"]
+    value = world * pairs * fpp["fwd_bwd"] / (ms_step * 1e-3) / 1e12
+    fwd_tflops = pairs * fpp["fwd"] / (fwd_ms * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (one launch per stage per step)
+    peaks = load_peaks()
+    fwd_path = vlf.vlf_fwd_path(w.h_q, w.h_kv, w.d_qk, w.d_v, dt)
+    bwd_path = vlf.vlf_bwd_path(w.h_q, w.h_kv, w.d_qk, w.d_v, dt)
+    dom = max(stage_ms, key=stage_ms.get)
+    flops_of = {"fwd": pairs * fpp["fwd"], "dkdv": pairs * fpp["dkdv"], "dq": pairs * fpp["dq"]}
+    tc = (fwd_path if dom == "fwd" else bwd_path) == 1
+    if dom == "rowdot":
+        eb = x["q"].element_size()
+        traffic_alg = 2 * w.total_q * w.h_q * w.d_v * eb + 4 * w.total_q * w.h_q
+        achieved = traffic_alg / (stage_ms[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    elif tc:
+        achieved = flops_of[dom] / (stage_ms[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        props = torch.cuda.get_device_properties(dev)
+        sm_max = (clocks or {}).get("sm_max_mhz") or 2070.0
+        alu_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12
+        achieved = flops_of[dom] / (stage_ms[dom] * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x max SM clock)"
+                                             if roof["bound"] == "alu" else "")
+
+    # end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "dout", "cu_seqlens_q",
+                                                     "cu_seqlens_kv")}
+        hout = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for k, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        dbuf = {k: torch.empty_like(x[k]) for k in host}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in hout.values())
+
+        def e2e_step():
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            vlf.vlf_attn_varlen_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["cu_seqlens_q"],
+                                    dbuf["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv,
+                                    out=out, lse=lse, **kw)
+            vlf.vlf_attn_varlen_bwd(dbuf["dout"], dbuf["q"], dbuf["k"], dbuf["v"], out, lse,
+                                    dbuf["cu_seqlens_q"], dbuf["cu_seqlens_kv"], w.max_seqlen_q,
+                                    w.max_seqlen_kv, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+            for k, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                hout[k].copy_(t, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier(world)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+        e2e = {"value": world * pairs * fpp["fwd_bwd"] / (e2e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_units > 0:
+        xc = cpu_inputs(w, args.cpu_units)
+        secs, p = oracle_sample(w, xc, args.cpu_units)
+        cpu = {"value": p * fpp["fwd_bwd"] / secs / 1e12, "unit": "TFLOP/s",
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{args.cpu_units} (sequence, head) units of {w.name}, fwd+bwd, fp64 "
+                         f"numpy, {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "attention TFLOP/s fwd+bwd (unmasked pairs)", "value": value,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": w.name, "lengths": sorted(set(w.lengths_q)),
+                       "num_seqs": w.num_seqs, "h_q": w.h_q, "h_kv": w.h_kv, "d_qk": w.d_qk,
+                       "d_v": w.d_v, "causal": w.causal, "window": w.window,
+                       "unmasked_pairs": pairs, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (q/k/v/out/dout 134 MB each), no flush",
+                       "fwd_path": "tcgen05" if fwd_path == 1 else "simt",
+                       "bwd_path": "tcgen05" if bwd_path == 1 else "simt"},
+            "fwd_tflops": fwd_tflops, "fwd_frac_of_peak": fwd_tflops / peaks["bf16_tflops"],
+            "fwd_bwd_frac_of_peak": value / world / peaks["bf16_tflops"],
+            "stage_ms": stage_ms, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": launches,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * vlf.h -- C ABI of libvlf.so: fused variable-length flash attention (forward and backward)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one the mtlattn 0.3.0 page defines for its varlen_attention call
+ * (section "Use"):
+ *   q [total_q, H_q, D_qk], k [total_kv, H_kv, D_qk], v [total_kv, H_kv, D_v], packed by
+ *   cumulative sequence lengths cu_seqlens_q / cu_seqlens_kv (int32 [num_seqs + 1]), no padding;
+ *   query head h reads kv head h / (H_q / H_kv) (GQA / MQA);
+ *   logit(i, j) = scale * (q_i . k_j) + bias[global row i, h or 0, sequence-local key j];
+ *   causal (end-aligned): row i sees key j iff j <= i + (kv_len - q_len);
+ *   window W > 0: row i sees only the last W keys up to that diagonal,
+ *                 j >= i + (kv_len - q_len) - W + 1;
+ *   out_i = softmax_j(logit(i, .)) v, accumulated in fp32 without materialising the L x L
+ *   score matrix (online softmax, mtlattn 0.3.0 header; triton-msl part 1, "What works").
+ * The asymmetric latent-attention head (D_qk = 192 = 128 "nope" ++ 64 "rope", D_v = 128) is the
+ * one of triton-msl part 2, "Latent attention".
+ *
+ * Conventions for every entry point
+ *   - All tensors are dense, row-major (C-contiguous) device buffers owned by the caller; the
+ *     library never allocates, frees or synchronises inside vlf_attn_varlen_fwd/_bwd and only
+ *     enqueues work on `stream` (mtlattn 0.3.0, "Notes": work is ordered on the caller's stream
+ *     without a per-call host sync).
+ *   - Element types: q, k, v, out, dout, dq, dk, dv share `dtype` (VLF_F16, VLF_BF16, VLF_F32);
+ *     bias, lse and the workspace are fp32.  Accumulation is fp32 for every dtype; each output is
+ *     rounded once (round-to-nearest-even) to its storage type.
+ *   - Every pointer must be 16-byte aligned.
+ *   - Correct-or-refuse (triton-msl part 1, "Correct-or-refuse"): an argument the library cannot
+ *     handle returns a negative vlf_status before anything is enqueued; nothing is silently
+ *     approximated.  Errors found on the device (bad cu_seqlens, a pipeline wait that ran out of
+ *     time) are recorded in a per-device error word and returned by vlf_check_error().  The
+ *     kernels never trap.
+ *   - Indices into q/k/v/out/bias are 64-bit: bias tensors beyond 2^32 elements are supported.
+ */
+#ifndef VLF_H
+#define VLF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *vlf_stream_t;
+
+typedef enum { VLF_F16 = 0, VLF_BF16 = 1, VLF_F32 = 2 } vlf_dtype;
+
+typedef enum {
+  VLF_OK = 0,
+  VLF_ERR_INVALID = -1,     /* null pointer, negative size, H_q % H_kv != 0, bias_heads not 1/H_q */
+  VLF_ERR_UNSUPPORTED = -2, /* a valid problem this build does not implement (e.g. head width) */
+  VLF_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+  VLF_ERR_LAUNCH = -4,      /* the CUDA runtime refused a launch or a query */
+  VLF_ERR_TIMEOUT = -5,     /* device: a pipeline wait exceeded its time limit (kernel bailed out) */
+  VLF_ERR_BAD_SEQLENS = -6, /* device: cu_seqlens not in [0, total], decreasing, or longer than max_seqlen */
+  VLF_ERR_WORKSPACE = -7    /* backward workspace missing or smaller than the size query returns */
+} vlf_status;
+
+/* Extended-call flags (vlf_attn_varlen_fwd_ex / _bwd_ex). */
+#define VLF_FLAG_NO_SKIP 1u    /* visit every KV tile, masking per element (tile-skip check) */
+#define VLF_FLAG_FORCE_SIMT 2u /* use the SIMT fp32-FMA kernels even where a tensor-core one exists */
+
+/*
+ * Forward.  mtlattn 0.3.0, section "Use" (varlen_attention with scale, causal, window, attn_bias).
+ *
+ *   q            [total_q, h_q, d_qk]      dtype
+ *   k            [total_kv, h_kv, d_qk]    dtype
+ *   v            [total_kv, h_kv, d_v]     dtype
+ *   cu_seqlens_q / cu_seqlens_kv           device int32 [num_seqs + 1], cu[0] = 0,
+ *                                          non-decreasing, cu[num_seqs] = total_q / total_kv
+ *   max_seqlen_q / max_seqlen_kv           host ints >= every sequence's q_len / kv_len
+ *                                          (size the launch grid; max_seqlen_kv is also the
+ *                                          row length of `bias`)
+ *   h_q % h_kv == 0
+ *   scale        softmax scale; <= 0 selects 1/sqrt(d_qk)
+ *   causal       0/1, end-aligned
+ *   window       <= 0: none; else the number of keys each row sees up to its diagonal
+ *   bias         NULL or fp32 [total_q, bias_heads, max_seqlen_kv], bias_heads in {1, h_q};
+ *                row = global query row, column = sequence-local key; -inf masks the pair
+ *   out          [total_q, h_q, d_v]       dtype (written)
+ *   lse          NULL or fp32 [h_q, total_q]: natural-log log-sum-exp of each row's logits,
+ *                -inf for a row that sees no key (its out row is 0).  Required by the backward.
+ * Supported: dtype F16/BF16 with any 1 <= d_qk, d_v <= 256 (tensor-core kernels for
+ * (d_qk, d_v) in {(64,64), (128,128), (192,128)}); dtype F32 with d_qk, d_v <= 256 (fp32 FMA).
+ */
+int vlf_attn_varlen_fwd(const void *q, const void *k, const void *v,
+                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                        int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
+                        int h_q, int h_kv, int d_qk, int d_v, int dtype,
+                        float scale, int causal, int window,
+                        const float *bias, int bias_heads,
+                        void *out, float *lse, vlf_stream_t stream);
+
+int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
+                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                           int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
+                           int h_q, int h_kv, int d_qk, int d_v, int dtype,
+                           float scale, int causal, int window,
+                           const float *bias, int bias_heads,
+                           void *out, float *lse, vlf_stream_t stream, unsigned flags);
+
+/*
+ * Bytes of fp32 workspace vlf_attn_varlen_bwd needs (row dot products dO.O, fp32 dQ
+ * accumulator).  Pure host arithmetic; never fails (returns 0 for invalid sizes).
+ */
+size_t vlf_attn_varlen_bwd_workspace_size(int total_q, int total_kv, int h_q, int h_kv,
+                                          int d_qk, int d_v, int dtype);
+
+/*
+ * Backward.  The gradients of sum(out * dout) with respect to q, k, v, the bias held constant
+ * (mtlattn 0.3.0, "Use": the bias is treated as constant; triton-msl part 2, "Beyond softmax":
+ * a tiled FlashAttention-2 backward).  Same shapes and conventions as the forward, plus
+ *   out, lse     the forward's outputs for the same inputs
+ *   dout         [total_q, h_q, d_v]       dtype
+ *   dq           [total_q, h_q, d_qk]      dtype (written)
+ *   dk, dv       [total_kv, h_kv, d_qk], [total_kv, h_kv, d_v] dtype (written; each kv head
+ *                sums the contributions of its h_q / h_kv query heads)
+ *   workspace    device buffer of at least vlf_attn_varlen_bwd_workspace_size(...) bytes,
+ *                owned by the caller, contents need not be initialised; clobbered.
+ */
+int vlf_attn_varlen_bwd(const void *q, const void *k, const void *v, const void *out,
+                        const float *lse, const void *dout,
+                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                        int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
+                        int h_q, int h_kv, int d_qk, int d_v, int dtype,
+                        float scale, int causal, int window,
+                        const float *bias, int bias_heads,
+                        void *dq, void *dk, void *dv,
+                        void *workspace, size_t workspace_bytes, vlf_stream_t stream);
+
+/*
+ * As vlf_attn_varlen_bwd, plus `flags` and optional per-stage timing events.  When
+ * stage_events is not NULL it holds n_stage_events >= VLF_BWD_STAGES + 1 cudaEvent_t handles
+ * (created by the caller); event 0 is recorded on `stream` before the first kernel and event
+ * s+1 after stage s, stages being, in order: 0 the dO.O row-dot pre-pass, 1 the dK/dV kernel,
+ * 2 the dQ kernel.  Recording adds no synchronisation.
+ */
+#define VLF_BWD_STAGES 3
+int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *out,
+                           const float *lse, const void *dout,
+                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                           int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
+                           int h_q, int h_kv, int d_qk, int d_v, int dtype,
+                           float scale, int causal, int window,
+                           const float *bias, int bias_heads,
+                           void *dq, void *dk, void *dv,
+                           void *workspace, size_t workspace_bytes, vlf_stream_t stream,
+                           unsigned flags, void *const *stage_events, int n_stage_events);
+
+/*
+ * Number of kernels this library has launched in this process (all devices, all streams),
+ * counted on the host at each successful launch.  For benchmarks that report their launches.
+ */
+uint64_t vlf_launch_count(void);
+
+/*
+ * Which kernel family the forward / backward would use for this problem: 1 tensor-core
+ * (tcgen05), 0 SIMT fp32 FMA, negative status if the problem is refused.  Host only.
+ */
+int vlf_fwd_path(int h_q, int h_kv, int d_qk, int d_v, int dtype, int bias_heads, unsigned flags);
+int vlf_bwd_path(int h_q, int h_kv, int d_qk, int d_v, int dtype, int bias_heads, unsigned flags);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error word (VLF_OK,
+ * VLF_ERR_TIMEOUT or VLF_ERR_BAD_SEQLENS), or VLF_ERR_LAUNCH if the CUDA runtime reports an
+ * error.  The only entry point that blocks the host.
+ */
+int vlf_check_error(vlf_stream_t stream);
+
+/* Static description of a status code. */
+const char *vlf_status_string(int status);
+
+/*
+ * Tile scheduler (host-callable, no GPU needed).  For sequence-local query rows [r0, r1) of a
+ * sequence with q_len queries and kv_len keys, the key range [*lo, *hi) that holds every key
+ * any of those rows may see under the causal/window rules above; keys outside it are skipped
+ * whole (mtlattn 0.3.0, "Use": fully masked KV tiles are skipped, window jumps to its band).
+ * Returns VLF_OK or VLF_ERR_INVALID.
+ */
+int vlf_sched_kv_band(int r0, int r1, int q_len, int kv_len, int causal, int window,
+                      int *lo, int *hi);
+
+/* The query rows [*lo, *hi) that may see any key of [j0, j1) (the backward's dK/dV band). */
+int vlf_sched_q_band(int j0, int j1, int q_len, int kv_len, int causal, int window,
+                     int *lo, int *hi);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int vlf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VLF_H */

@@ -1,0 +1,176 @@
+"""GPU vs fp64 oracle, every element, on small varlen problems that still span several tiles
+and ragged tails: dtypes x {self, cross} x {causal, window, GQA/MQA, bias dim1 in {1, H}} x head
+widths {64, 128, 192/128, odd}, lengths including 0, 1, 15-17, 127-129 and thousands of tiny
+windows.  Also: tile skipping is exact (skip on/off give identical bits), bad cu_seqlens are
+reported through the device error word, and the SIMT and tensor-core paths both pass."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.parity import assert_within, compare, gpu_run, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+ODD = [1, 15, 16, 17, 127, 128, 129, 0, 300]
+
+CASES = {
+    "varlen64_fp16_full": W.workload("varlen64_fp16_full"),
+    "varlen64_fp16_causal": W.workload("varlen64_fp16_causal"),
+    "bf16_d128_gqa_causal_odd": W.custom(ODD, dtype="bf16", h_q=4, h_kv=2, d_qk=128, causal=True),
+    "fp16_d128_full_odd": W.custom(ODD, dtype="fp16", h_q=2, d_qk=128),
+    "bf16_latent_192_128": W.custom([129, 64, 1, 300], dtype="bf16", h_q=2, d_qk=192, d_v=128,
+                                    causal=True, scale=1 / 192 ** 0.5),
+    "fp16_d128_window16": W.custom([200, 33, 257], dtype="fp16", h_q=2, d_qk=128, causal=True,
+                                   window=16),
+    "bf16_d64_window1_tiny": W.custom([3, 1, 2, 5] * 6, dtype="bf16", h_q=2, d_qk=64, causal=True,
+                                      window=1),
+    "fp16_cross_causal": W.custom([5, 100, 64, 130], [70, 30, 64, 129], dtype="fp16", h_q=2,
+                                  d_qk=64, causal=True),
+    "bf16_cross_full": W.custom([5, 100], [70, 300], dtype="bf16", h_q=2, d_qk=128),
+    "bf16_mqa_d128": W.custom([150, 77], dtype="bf16", h_q=8, h_kv=1, d_qk=128, causal=True),
+    "fp32_d64_causal": W.custom([17, 64, 100], dtype="fp32", h_q=2, d_qk=64, causal=True),
+    "fp32_d40_window": W.custom([50, 90], dtype="fp32", h_q=2, h_kv=1, d_qk=40, d_v=24,
+                                causal=True, window=7),
+    "fp16_d96": W.custom([70, 129], dtype="fp16", h_q=2, d_qk=96, causal=True),
+    "bf16_empty_seqs": W.custom([0, 5, 0, 130], [3, 5, 0, 130], dtype="bf16", h_q=2, d_qk=64,
+                                causal=False),
+}
+
+
+def _bias_case(dtype, heads, causal, d, window=0):
+    w = W.custom([70, 1, 140], dtype=dtype, h_q=4, h_kv=2, d_qk=d, causal=causal, window=window)
+    x = W.make_inputs(w, seed=11, with_dout=True)
+    g = torch.Generator("cpu").manual_seed(12)
+    b = torch.randn((w.total_q, heads, w.max_seqlen_kv), generator=g)
+    b[torch.rand(b.shape, generator=g) < 0.1] = float("-inf")
+    b[75, :, :] = float("-inf")          # a row that the bias masks completely
+    x["bias"] = b.contiguous()
+    return w, x
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_parity_case(name):
+    w = CASES[name]
+    x = W.make_inputs(w, seed=5, with_dout=True)
+    gpu = gpu_run(w, x)
+    ref = oracle_run(w, x)
+    assert_within(compare(w, gpu, ref), name)
+
+
+@pytest.mark.parametrize("dtype,heads,causal,d,window", [
+    ("fp16", 4, False, 64, 0), ("bf16", 1, True, 128, 0), ("fp16", 4, True, 128, 33),
+    ("bf16", 4, False, 192, 0), ("fp32", 1, True, 64, 0)])
+def test_parity_bias(dtype, heads, causal, d, window):
+    w, x = _bias_case(dtype, heads, causal, d, window)
+    if d == 192:
+        w.d_v = 128
+        x["v"] = x["v"][:, :, :128].contiguous()
+        x["dout"] = x["dout"][:, :, :128].contiguous()
+    gpu = gpu_run(w, x)
+    ref = oracle_run(w, x)
+    assert_within(compare(w, gpu, ref), f"bias {dtype} {heads} {causal} {d}")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_outlier_channels(dtype):
+    """Transformer activations spike to 1e2-1e3 in a few channels: fp32 accumulation and the
+    max subtraction must keep the result finite and accurate."""
+    w = W.custom([200, 57], dtype=dtype, h_q=2, d_qk=128, causal=True)
+    x = W.make_inputs(w, seed=21, with_dout=True)
+    for t in ("q", "k"):
+        y = x[t].float()
+        y[..., 3] *= 300.0
+        y[..., 77] *= -900.0
+        x[t] = y.to(x[t].dtype)
+    gpu = gpu_run(w, x)
+    for k in ("out", "lse", "dq", "dk", "dv"):
+        assert torch.isfinite(gpu[k]).all(), k
+    ref = oracle_run(w, x)
+    errs = compare(w, gpu, ref, keys=["out", "lse"])
+    assert_within(errs, f"outliers {dtype}")
+
+
+@pytest.mark.parametrize("name", ["bf16_d128_gqa_causal_odd", "fp16_d128_window16",
+                                  "varlen64_fp16_causal", "bf16_latent_192_128"])
+@pytest.mark.parametrize("simt", [False, True])
+def test_tile_skipping_is_exact(name, simt):
+    """Skipping fully masked KV tiles changes no bit of any output."""
+    import variable_length_flash_gb300 as vlf
+    w = CASES[name]
+    x = W.make_inputs(w, seed=9, with_dout=True)
+    base = vlf.VLF_FLAG_FORCE_SIMT if simt else 0
+    a = gpu_run(w, x, flags=base)
+    b = gpu_run(w, x, flags=base | vlf.VLF_FLAG_NO_SKIP)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("name", ["bf16_d128_gqa_causal_odd", "bf16_latent_192_128",
+                                  "varlen64_fp16_full"])
+def test_simt_path_parity(name):
+    """The SIMT fp32-FMA kernels on 16-bit data (the tensor-core kernels' independent twin)."""
+    import variable_length_flash_gb300 as vlf
+    w = CASES[name]
+    x = W.make_inputs(w, seed=6, with_dout=True)
+    gpu = gpu_run(w, x, flags=vlf.VLF_FLAG_FORCE_SIMT)
+    ref = oracle_run(w, x)
+    assert_within(compare(w, gpu, ref), name + " simt")
+
+
+def test_bad_cu_seqlens_reported_and_device_stays_usable():
+    import variable_length_flash_gb300 as vlf
+    w = W.custom([10, 20], dtype="bf16", h_q=2, d_qk=64)
+    x = W.make_inputs(w, seed=1)
+    dev = {k: (t.cuda() if isinstance(t, torch.Tensor) else t) for k, t in x.items()}
+    for bad in ([0, 25, 20], [0, 10, 31], [1, 10, 30], [0, 10, 29]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        vlf.vlf_attn_varlen_fwd(dev["q"], dev["k"], dev["v"], cu, cu, 30, 30)
+        assert vlf.vlf_check_error() == vlf.VLF_ERR_BAD_SEQLENS, bad
+    # a sequence longer than max_seqlen_q is refused too (it would not be covered by the grid)
+    vlf.vlf_attn_varlen_fwd(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"],
+                            dev["cu_seqlens_kv"], 12, 20)
+    assert vlf.vlf_check_error() == vlf.VLF_ERR_BAD_SEQLENS
+    # and the next good call works
+    gpu = gpu_run(w, x, backward=False)
+    ref = oracle_run(w, x, backward=False)
+    assert_within(compare(w, gpu, ref), "after error")
+
+
+def test_refuses_grad_requiring_bias():
+    import variable_length_flash_gb300 as vlf
+    w = W.custom([8], dtype="bf16", h_q=2, d_qk=64)
+    x = W.make_inputs(w, seed=1)
+    dev = {k: (t.cuda() if isinstance(t, torch.Tensor) else t) for k, t in x.items()}
+    b = torch.zeros((8, 1, 8), device="cuda", requires_grad=True)
+    with pytest.raises(vlf.VlfError):
+        vlf.vlf_attn_varlen_fwd(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"],
+                                dev["cu_seqlens_kv"], 8, 8, bias=b)
+
+
+def test_fuzz_correct_or_refuse():
+    """Random shapes and flags: every call either matches the oracle or is refused loudly."""
+    import variable_length_flash_gb300 as vlf
+    rng = np.random.default_rng(1234)
+    for trial in range(12):
+        n = int(rng.integers(1, 5))
+        lq = [int(x) for x in rng.integers(0, 200, n)]
+        cross = rng.random() < 0.3
+        lk = [int(x) for x in rng.integers(0, 200, n)] if cross else lq
+        if sum(lq) == 0 or sum(lk) == 0:
+            continue
+        hkv = int(rng.choice([1, 2]))
+        hq = hkv * int(rng.choice([1, 2, 4]))
+        d, dv = [(64, 64), (128, 128), (192, 128), (32, 32), (80, 48)][int(rng.integers(0, 5))]
+        dtype = str(rng.choice(["fp16", "bf16", "fp32"]))
+        causal = bool(rng.random() < 0.6)
+        window = int(rng.choice([0, 0, 1, 7, 64]))
+        w = W.custom(lq, lk, dtype=dtype, h_q=hq, h_kv=hkv, d_qk=d, d_v=dv, causal=causal,
+                     window=window)
+        x = W.make_inputs(w, seed=100 + trial, with_dout=True)
+        try:
+            gpu = gpu_run(w, x)
+        except vlf.VlfError:
+            continue
+        ref = oracle_run(w, x)
+        assert_within(compare(w, gpu, ref), f"fuzz {trial} {w}")

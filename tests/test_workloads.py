@@ -52,3 +52,30 @@ def test_sample_rows_include_sequence_tails():
     rows = W.sample_rows(w, 4, seed=0, tail=2)
     for r in (3, 4, 12, 13, 15, 16):
         assert r in rows
+
+
+def test_pair_counts_match_brute_force_masks():
+    """The closed-form pair counter used for TFLOP/s equals counting the oracle's masks."""
+    import numpy as np
+
+    from oracle import attention as orc
+    from variable_length_flash_gb300 import flops
+    for q_len, kv_len in ((1, 1), (17, 17), (100, 255), (255, 100), (64, 64)):
+        for causal, window in ((False, 0), (True, 0), (True, 1), (True, 7), (False, 5)):
+            want = int(orc.visible(q_len, kv_len, causal, window).sum())
+            assert flops.visible_pairs(q_len, kv_len, causal, window) == want
+    # the forward-only varlen workload: sums of L^2 and L(L+1)/2 over {17, 64, 100, 255}, 4 heads
+    assert flops.workload_pairs(W.workload("varlen64_fp16_full")) == 317_640
+    assert flops.workload_pairs(W.workload("varlen64_fp16_causal")) == 159_692
+    assert flops.workload_pairs(W.workload("dense4x4096_bf16_causal")) == 4 * 32 * 4096 * 4097 // 2
+    # prefix-LM pairs: key <= 8191 or key <= query, counted from the generated bias
+    w = W.workload("long49152_fp16_bias_prefix")
+    rows = torch.arange(0, 49152, 997)
+    b = W.bias_block(w, rows, [0])
+    got = int(torch.isfinite(b).sum())
+    want = int(sum(min(49152, max(8192, int(r) + 1)) for r in rows))
+    assert got == want
+    assert flops.workload_pairs(w) == 16 * sum(min(49152, max(8192, i + 1)) for i in range(49152))
+    assert flops.flops_per_pair(128, 128) == {"fwd": 512, "bwd": 1280, "fwd_bwd": 1792,
+                                              "dkdv": 1024, "dq": 768}
+    assert flops.flops_per_pair(192, 128)["fwd_bwd"] == 2304

@@ -1,0 +1,263 @@
+"""Python binding of libvlf.so: fused variable-length flash attention for GB300 (sm_103a).
+
+Argument marshalling only.  Every step of the computation runs in the library's CUDA kernels;
+PyTorch supplies device memory and the current stream.  There is no CPU fallback: importing
+this package raises if the compiled library is missing.
+
+The functions carry the names of the C entry points in ``include/vlf.h``:
+
+* ``vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, ...)`` -> (out, lse)
+* ``vlf_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, ...)``
+  -> (dq, dk, dv)
+* ``vlf_attn_varlen_bwd_workspace_size``, ``vlf_check_error``, ``vlf_status_string``,
+  ``vlf_sched_kv_band``, ``vlf_sched_q_band``, ``vlf_version``.
+
+The operation is the varlen attention of the mtlattn 0.3.0 page (section "Use"): packed
+q/k/v [tokens, heads, head_dim] with int32 cu_seqlens, end-aligned causal, sliding window,
+GQA/MQA, additive fp32 bias [total_q, H or 1, max_kv] (held constant in the backward; a bias
+that requires grad is refused).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvlf.so")
+
+VLF_F16, VLF_BF16, VLF_F32 = 0, 1, 2
+VLF_OK = 0
+VLF_ERR_INVALID, VLF_ERR_UNSUPPORTED, VLF_ERR_ALIGN, VLF_ERR_LAUNCH = -1, -2, -3, -4
+VLF_ERR_TIMEOUT, VLF_ERR_BAD_SEQLENS, VLF_ERR_WORKSPACE = -5, -6, -7
+VLF_FLAG_NO_SKIP = 1
+VLF_FLAG_FORCE_SIMT = 2
+
+_DTYPE = {torch.float16: VLF_F16, torch.bfloat16: VLF_BF16, torch.float32: VLF_F32}
+
+EXPORTS = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_fwd_ex", "vlf_attn_varlen_bwd",
+           "vlf_attn_varlen_bwd_ex", "vlf_attn_varlen_bwd_workspace_size", "vlf_check_error",
+           "vlf_status_string", "vlf_sched_kv_band", "vlf_sched_q_band", "vlf_version",
+           "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path"]
+VLF_BWD_STAGES = 3
+BWD_STAGE_NAMES = ["rowdot", "dkdv", "dq"]
+
+
+class VlfError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"vlf status {status}: {vlf_status_string(status)}{': ' + what if what else ''}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; "
+                          "g.build()'` (needs nvcc for sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, Z, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint
+    fwd = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, I, P, I, P, P, P]
+    lib.vlf_attn_varlen_fwd.argtypes = fwd
+    lib.vlf_attn_varlen_fwd_ex.argtypes = fwd + [U]
+    bwd = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, I, P, I, P, P, P, P, Z, P]
+    lib.vlf_attn_varlen_bwd.argtypes = bwd
+    lib.vlf_attn_varlen_bwd_ex.argtypes = bwd + [U, P, I]
+    for name in ("vlf_attn_varlen_fwd", "vlf_attn_varlen_fwd_ex", "vlf_attn_varlen_bwd",
+                 "vlf_attn_varlen_bwd_ex"):
+        getattr(lib, name).restype = I
+    lib.vlf_attn_varlen_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.vlf_attn_varlen_bwd_workspace_size.restype = Z
+    lib.vlf_check_error.argtypes = [P]
+    lib.vlf_check_error.restype = I
+    lib.vlf_status_string.argtypes = [I]
+    lib.vlf_status_string.restype = ctypes.c_char_p
+    IP = ctypes.POINTER(ctypes.c_int)
+    lib.vlf_sched_kv_band.argtypes = [I, I, I, I, I, I, IP, IP]
+    lib.vlf_sched_kv_band.restype = I
+    lib.vlf_sched_q_band.argtypes = [I, I, I, I, I, I, IP, IP]
+    lib.vlf_sched_q_band.restype = I
+    lib.vlf_version.argtypes = []
+    lib.vlf_version.restype = I
+    lib.vlf_launch_count.argtypes = []
+    lib.vlf_launch_count.restype = ctypes.c_uint64
+    for name in ("vlf_fwd_path", "vlf_bwd_path"):
+        getattr(lib, name).argtypes = [I, I, I, I, I, I, U]
+        getattr(lib, name).restype = I
+    return lib
+
+
+_lib = _load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, what: str = ""):
+    if status != VLF_OK:
+        raise VlfError(status, what)
+
+
+def vlf_status_string(status: int) -> str:
+    return _lib.vlf_status_string(int(status)).decode()
+
+
+def vlf_version() -> int:
+    return _lib.vlf_version()
+
+
+def vlf_launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(_lib.vlf_launch_count())
+
+
+def vlf_fwd_path(h_q, h_kv, d_qk, d_v, dtype, bias_heads=0, flags=0) -> int:
+    """1: tensor-core forward, 0: SIMT fp32-FMA forward, negative: refused."""
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return _lib.vlf_fwd_path(h_q, h_kv, d_qk, d_v, dt, bias_heads, flags)
+
+
+def vlf_bwd_path(h_q, h_kv, d_qk, d_v, dtype, bias_heads=0, flags=0) -> int:
+    """1: tensor-core backward, 0: SIMT fp32-FMA backward, negative: refused."""
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return _lib.vlf_bwd_path(h_q, h_kv, d_qk, d_v, dt, bias_heads, flags)
+
+
+def vlf_check_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    return _lib.vlf_check_error(_stream(stream))
+
+
+def vlf_sched_kv_band(r0, r1, q_len, kv_len, causal, window):
+    lo, hi = ctypes.c_int(), ctypes.c_int()
+    _check(_lib.vlf_sched_kv_band(r0, r1, q_len, kv_len, int(causal), int(window),
+                                  ctypes.byref(lo), ctypes.byref(hi)), "kv band")
+    return lo.value, hi.value
+
+
+def vlf_sched_q_band(j0, j1, q_len, kv_len, causal, window):
+    lo, hi = ctypes.c_int(), ctypes.c_int()
+    _check(_lib.vlf_sched_q_band(j0, j1, q_len, kv_len, int(causal), int(window),
+                                 ctypes.byref(lo), ctypes.byref(hi)), "q band")
+    return lo.value, hi.value
+
+
+def vlf_attn_varlen_bwd_workspace_size(total_q, total_kv, h_q, h_kv, d_qk, d_v, dtype) -> int:
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(_lib.vlf_attn_varlen_bwd_workspace_size(total_q, total_kv, h_q, h_kv, d_qk, d_v, dt))
+
+
+def _events(evs):
+    if evs is None:
+        return None, 0
+    arr = (ctypes.c_void_p * len(evs))(*[ctypes.c_void_p(e.cuda_event) for e in evs])
+    _events.keep = arr  # keep alive for the duration of the call
+    return ctypes.cast(arr, ctypes.c_void_p), len(evs)
+
+
+def _max_len(cu):
+    return int((cu[1:] - cu[:-1]).max().item()) if cu.numel() > 1 else 0
+
+
+def _req(t, name, dtype=None):
+    if t is None:
+        raise VlfError(VLF_ERR_INVALID, f"{name} is None")
+    if not t.is_cuda:
+        raise VlfError(VLF_ERR_INVALID, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise VlfError(VLF_ERR_INVALID, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise VlfError(VLF_ERR_INVALID, f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _bias_args(bias, total_q, h_q):
+    if bias is None:
+        return None, 0
+    if bias.requires_grad:
+        raise VlfError(VLF_ERR_UNSUPPORTED, "the bias is treated as a constant; a bias that "
+                       "requires grad is refused")
+    _req(bias, "bias", torch.float32)
+    if bias.dim() != 3 or bias.shape[0] != total_q or bias.shape[1] not in (1, h_q):
+        raise VlfError(VLF_ERR_INVALID, "bias must be [total_q, 1 or H_q, max_seqlen_kv]")
+    return bias, int(bias.shape[1])
+
+
+def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_seqlen_kv=None,
+                        scale=None, causal=False, window=0, bias=None, out=None, lse=None,
+                        stream=None, flags=0):
+    """Forward.  q [Tq,Hq,Dqk], k [Tkv,Hkv,Dqk], v [Tkv,Hkv,Dv] (fp16/bf16/fp32, CUDA,
+    contiguous), cu_seqlens int32 [n+1].  Returns out [Tq,Hq,Dv] and lse fp32 [Hq,Tq].
+    ``max_seqlen_kv=None`` reads it from cu_seqlens_kv (a host sync); the bias's last dim
+    must equal max_seqlen_kv when a bias is given."""
+    _req(q, "q"), _req(k, "k", q.dtype), _req(v, "v", q.dtype)
+    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise VlfError(VLF_ERR_INVALID, "q, k, v must be [tokens, heads, head_dim]")
+    tq, hq, dqk = q.shape
+    tk, hkv, dv = v.shape
+    if k.shape[0] != tk or k.shape[1] != hkv or k.shape[2] != dqk:
+        raise VlfError(VLF_ERR_INVALID, "k shape")
+    if max_seqlen_kv is None:
+        max_seqlen_kv = int(bias.shape[2]) if bias is not None else _max_len(cu_seqlens_kv)
+    if bias is not None and bias.shape[2] != max_seqlen_kv:
+        raise VlfError(VLF_ERR_INVALID, "bias last dim must be max_seqlen_kv")
+    bias, bh = _bias_args(bias, tq, hq)
+    if out is None:
+        out = torch.empty((tq, hq, dv), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((hq, tq), dtype=torch.float32, device=q.device)
+    _req(out, "out", q.dtype), _req(lse, "lse", torch.float32)
+    st = _lib.vlf_attn_varlen_fwd_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+        cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv,
+        _DTYPE[q.dtype], float(scale) if scale else 0.0, int(bool(causal)), int(window or 0),
+        _ptr(bias), bh, _ptr(out), _ptr(lse), _stream(stream), int(flags))
+    _check(st, "vlf_attn_varlen_fwd")
+    return out, lse
+
+
+def vlf_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q,
+                        max_seqlen_kv=None, scale=None, causal=False, window=0, bias=None,
+                        dq=None, dk=None, dv=None, workspace=None, stream=None, flags=0,
+                        stage_events=None):
+    """Backward: gradients of sum(out * dout) w.r.t. q, k, v (bias constant).
+    Returns dq, dk, dv in the input dtype.  ``workspace`` (uint8 CUDA tensor of at least
+    vlf_attn_varlen_bwd_workspace_size bytes) is allocated with torch when not given.
+    ``stage_events``: optional list of VLF_BWD_STAGES + 1 ``torch.cuda.Event`` (timing) recorded
+    before the first and after each backward kernel on the same stream."""
+    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _req(t, n, q.dtype)
+    _req(lse, "lse", torch.float32)
+    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
+    tq, hq, dqk = q.shape
+    tk, hkv, dvv = v.shape
+    if max_seqlen_kv is None:
+        max_seqlen_kv = int(bias.shape[2]) if bias is not None else _max_len(cu_seqlens_kv)
+    bias, bh = _bias_args(bias, tq, hq)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = vlf_attn_varlen_bwd_workspace_size(tq, tk, hq, hkv, dqk, dvv, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = _lib.vlf_attn_varlen_bwd_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_kv), cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q),
+        int(max_seqlen_kv), hq, hkv, dqk, dvv, _DTYPE[q.dtype], float(scale) if scale else 0.0,
+        int(bool(causal)), int(window or 0), _ptr(bias), bh, _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(workspace), workspace.numel(), _stream(stream), int(flags), *_events(stage_events))
+    _check(st, "vlf_attn_varlen_bwd")
+    return dq, dk, dv
+
+
+__all__ = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_bwd", "vlf_attn_varlen_bwd_workspace_size",
+           "vlf_check_error", "vlf_status_string", "vlf_sched_kv_band", "vlf_sched_q_band",
+           "vlf_version", "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path", "VlfError",
+           "LIB_PATH", "EXPORTS"]

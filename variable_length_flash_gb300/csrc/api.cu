@@ -1,0 +1,268 @@
+// C ABI of libvlf.so (declared in include/vlf.h): argument checks, dispatch to the kernels,
+// and the per-device error word that the kernels write instead of trapping.
+#include <math.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+// One error word per device (module-scope __device__ variable; each device that loads the
+// library holds its own copy).  Kernels get its address through Params::err.
+__device__ int g_vlf_error_word = 0;
+
+namespace vlf {
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace vlf
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_err_ptr[kMaxDevices] = {nullptr};
+
+int *error_word_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_vlf_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int *>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared argument checks of the forward and backward.  Returns VLF_OK or a negative status.
+int check_common(const void *q, const void *k, const void *v, const int32_t *cu_q,
+                 const int32_t *cu_kv, int num_seqs, int total_q, int total_kv, int max_q,
+                 int max_kv, int h_q, int h_kv, int d_qk, int d_v, int dtype, const float *bias,
+                 int bias_heads) {
+  if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_q < 0 || max_kv < 0) return VLF_ERR_INVALID;
+  if (h_q < 1 || h_kv < 1 || h_q % h_kv != 0) return VLF_ERR_INVALID;
+  if (d_qk < 1 || d_v < 1) return VLF_ERR_INVALID;
+  if (dtype != VLF_F16 && dtype != VLF_BF16 && dtype != VLF_F32) return VLF_ERR_INVALID;
+  if (num_seqs == 0 && (total_q != 0 || total_kv != 0)) return VLF_ERR_INVALID;
+  if (num_seqs > 0 && (!cu_q || !cu_kv)) return VLF_ERR_INVALID;
+  if ((total_q > 0 || total_kv > 0) && (!q || !k || !v)) return VLF_ERR_INVALID;
+  if (bias && bias_heads != 1 && bias_heads != h_q) return VLF_ERR_INVALID;
+  if (d_qk > 256 || d_v > 256) return VLF_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || h_q > 65535) return VLF_ERR_UNSUPPORTED;
+  // row strides of 16-bit data must keep 16-byte alignment for vector / TMA access
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cu_q) || !aligned16(cu_kv) ||
+      !aligned16(bias))
+    return VLF_ERR_ALIGN;
+  return VLF_OK;
+}
+
+void fill_common(vlf::Params &p, const void *q, const void *k, const void *v, const int32_t *cu_q,
+                 const int32_t *cu_kv, int num_seqs, int total_q, int total_kv, int max_q,
+                 int max_kv, int h_q, int h_kv, int d_qk, int d_v, int dtype, float scale,
+                 int causal, int window, const float *bias, int bias_heads, unsigned flags) {
+  p = vlf::Params{};
+  p.q = q; p.k = k; p.v = v; p.cu_q = cu_q; p.cu_kv = cu_kv;
+  p.num_seqs = num_seqs; p.total_q = total_q; p.total_kv = total_kv;
+  p.max_q = max_q; p.max_kv = max_kv;
+  p.h_q = h_q; p.h_kv = h_kv; p.d_qk = d_qk; p.d_v = d_v; p.group = h_q / h_kv;
+  p.dtype = dtype;
+  p.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)d_qk));
+  p.scale_log2 = (float)((double)p.scale * 1.4426950408889634);
+  p.causal = causal ? 1 : 0;
+  p.window = window > 0 ? window : 0;
+  p.bias = bias; p.bias_heads = bias ? bias_heads : 0;
+  p.flags = flags;
+}
+
+size_t workspace_bytes_for(int total_q, int h_q, int d_qk, int dtype) {
+  if (total_q < 0 || h_q < 1 || d_qk < 1) return 0;
+  size_t rowdot = (size_t)h_q * (size_t)total_q * sizeof(float);
+  rowdot = (rowdot + 255) & ~(size_t)255;
+  if (dtype == VLF_F32) return rowdot;
+  return rowdot + vlf::tc_backward_workspace(total_q, h_q, d_qk);
+}
+
+}  // namespace
+
+extern "C" {
+
+int vlf_version(void) { return 100; }
+
+uint64_t vlf_launch_count(void) { return vlf::g_launches.load(std::memory_order_relaxed); }
+
+static vlf::Params shape_params(int h_q, int h_kv, int d_qk, int d_v, int dtype, int bias_heads,
+                                unsigned flags) {
+  vlf::Params p{};
+  p.h_q = h_q; p.h_kv = h_kv; p.d_qk = d_qk; p.d_v = d_v; p.dtype = dtype;
+  p.group = h_kv > 0 ? h_q / h_kv : 0;
+  p.bias_heads = bias_heads;
+  p.flags = flags;
+  return p;
+}
+
+int vlf_fwd_path(int h_q, int h_kv, int d_qk, int d_v, int dtype, int bias_heads, unsigned flags) {
+  if (h_q < 1 || h_kv < 1 || h_q % h_kv || d_qk < 1 || d_v < 1 || dtype < 0 || dtype > 2)
+    return VLF_ERR_INVALID;
+  if (d_qk > 256 || d_v > 256) return VLF_ERR_UNSUPPORTED;
+  vlf::Params p = shape_params(h_q, h_kv, d_qk, d_v, dtype, bias_heads, flags);
+  return (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_forward_supported(p)) ? 1 : 0;
+}
+
+int vlf_bwd_path(int h_q, int h_kv, int d_qk, int d_v, int dtype, int bias_heads, unsigned flags) {
+  if (h_q < 1 || h_kv < 1 || h_q % h_kv || d_qk < 1 || d_v < 1 || dtype < 0 || dtype > 2)
+    return VLF_ERR_INVALID;
+  if (d_qk > 256 || d_v > 256) return VLF_ERR_UNSUPPORTED;
+  vlf::Params p = shape_params(h_q, h_kv, d_qk, d_v, dtype, bias_heads, flags);
+  return (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_backward_supported(p)) ? 1 : 0;
+}
+
+const char *vlf_status_string(int status) {
+  switch (status) {
+    case VLF_OK: return "ok";
+    case VLF_ERR_INVALID: return "invalid argument";
+    case VLF_ERR_UNSUPPORTED: return "unsupported problem (dtype / head width / size)";
+    case VLF_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case VLF_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case VLF_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case VLF_ERR_BAD_SEQLENS: return "bad cu_seqlens (out of range, decreasing, or longer than max_seqlen)";
+    case VLF_ERR_WORKSPACE: return "backward workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int vlf_sched_kv_band(int r0, int r1, int q_len, int kv_len, int causal, int window, int *lo,
+                      int *hi) {
+  if (!lo || !hi || q_len < 0 || kv_len < 0 || r0 < 0 || r1 <= r0 || r1 > q_len) return VLF_ERR_INVALID;
+  vlf::kv_band(r0, r1, q_len, kv_len, causal, window, *lo, *hi);
+  return VLF_OK;
+}
+
+int vlf_sched_q_band(int j0, int j1, int q_len, int kv_len, int causal, int window, int *lo,
+                     int *hi) {
+  if (!lo || !hi || q_len < 0 || kv_len < 0 || j0 < 0 || j1 <= j0 || j1 > kv_len) return VLF_ERR_INVALID;
+  vlf::q_band(j0, j1, q_len, kv_len, causal, window, *lo, *hi);
+  return VLF_OK;
+}
+
+int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
+                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                           int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
+                           int h_q, int h_kv, int d_qk, int d_v, int dtype, float scale,
+                           int causal, int window, const float *bias, int bias_heads, void *out,
+                           float *lse, vlf_stream_t stream, unsigned flags) {
+  int st = check_common(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+                        max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, bias, bias_heads);
+  if (st != VLF_OK) return st;
+  if (total_q > 0 && !out) return VLF_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(lse)) return VLF_ERR_ALIGN;
+  if (num_seqs == 0 || max_seqlen_q == 0) return VLF_OK;
+  vlf::Params p;
+  fill_common(p, q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, max_seqlen_q,
+              max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, scale, causal, window, bias, bias_heads,
+              flags);
+  p.out = out;
+  p.lse = lse;
+  p.err = error_word_ptr();
+  if (!p.err) return VLF_ERR_LAUNCH;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_forward_supported(p))
+    e = vlf::tc_forward(p, cs);
+  else
+    e = vlf::simt_forward(p, cs);
+  return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
+}
+
+int vlf_attn_varlen_fwd(const void *q, const void *k, const void *v, const int32_t *cu_seqlens_q,
+                        const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int total_kv,
+                        int max_seqlen_q, int max_seqlen_kv, int h_q, int h_kv, int d_qk, int d_v,
+                        int dtype, float scale, int causal, int window, const float *bias,
+                        int bias_heads, void *out, float *lse, vlf_stream_t stream) {
+  return vlf_attn_varlen_fwd_ex(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+                                max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, scale,
+                                causal, window, bias, bias_heads, out, lse, stream, 0u);
+}
+
+size_t vlf_attn_varlen_bwd_workspace_size(int total_q, int total_kv, int h_q, int h_kv, int d_qk,
+                                          int d_v, int dtype) {
+  (void)total_kv; (void)h_kv; (void)d_v;
+  return workspace_bytes_for(total_q, h_q, d_qk, dtype);
+}
+
+int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *out,
+                           const float *lse, const void *dout, const int32_t *cu_seqlens_q,
+                           const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int total_kv,
+                           int max_seqlen_q, int max_seqlen_kv, int h_q, int h_kv, int d_qk,
+                           int d_v, int dtype, float scale, int causal, int window,
+                           const float *bias, int bias_heads, void *dq, void *dk, void *dv,
+                           void *workspace, size_t workspace_bytes, vlf_stream_t stream,
+                           unsigned flags, void *const *stage_events, int n_stage_events) {
+  if (stage_events && n_stage_events < VLF_BWD_STAGES + 1) return VLF_ERR_INVALID;
+  int st = check_common(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+                        max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, bias, bias_heads);
+  if (st != VLF_OK) return st;
+  if (total_q > 0 && (!out || !lse || !dout || !dq)) return VLF_ERR_INVALID;
+  if (total_kv > 0 && (!dk || !dv)) return VLF_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv) || !aligned16(workspace))
+    return VLF_ERR_ALIGN;
+  const size_t need = workspace_bytes_for(total_q, h_q, d_qk, dtype);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return VLF_ERR_WORKSPACE;
+  if (num_seqs == 0) return VLF_OK;
+  vlf::Params p;
+  fill_common(p, q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, max_seqlen_q,
+              max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, scale, causal, window, bias, bias_heads,
+              flags);
+  const cudaEvent_t *ev = reinterpret_cast<const cudaEvent_t *>(stage_events);
+  p.out = const_cast<void *>(out);
+  p.lse = const_cast<float *>(lse);
+  p.dout = dout;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  size_t rowdot = (size_t)h_q * (size_t)total_q * sizeof(float);
+  rowdot = (rowdot + 255) & ~(size_t)255;
+  p.rowdot = static_cast<float *>(workspace);
+  p.dq_acc = dtype == VLF_F32 ? nullptr
+                              : reinterpret_cast<float *>(static_cast<char *>(workspace) + rowdot);
+  p.err = error_word_ptr();
+  if (!p.err) return VLF_ERR_LAUNCH;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_backward_supported(p))
+    e = vlf::tc_backward(p, cs, ev);
+  else
+    e = vlf::simt_backward(p, cs, ev);
+  return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
+}
+
+int vlf_attn_varlen_bwd(const void *q, const void *k, const void *v, const void *out,
+                        const float *lse, const void *dout, const int32_t *cu_seqlens_q,
+                        const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int total_kv,
+                        int max_seqlen_q, int max_seqlen_kv, int h_q, int h_kv, int d_qk, int d_v,
+                        int dtype, float scale, int causal, int window, const float *bias,
+                        int bias_heads, void *dq, void *dk, void *dv, void *workspace,
+                        size_t workspace_bytes, vlf_stream_t stream) {
+  return vlf_attn_varlen_bwd_ex(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, num_seqs,
+                                total_q, total_kv, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk,
+                                d_v, dtype, scale, causal, window, bias, bias_heads, dq, dk, dv,
+                                workspace, workspace_bytes, stream, 0u, nullptr, 0);
+}
+
+int vlf_check_error(vlf_stream_t stream) {
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return VLF_ERR_LAUNCH;
+  int *ptr = error_word_ptr();
+  if (!ptr) return VLF_ERR_LAUNCH;
+  int word = 0;
+  if (cudaMemcpy(&word, ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return VLF_ERR_LAUNCH;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return VLF_ERR_LAUNCH;
+  }
+  if (cudaGetLastError() != cudaSuccess) return VLF_ERR_LAUNCH;
+  return word;
+}
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// Host-side entry points of the kernel translation units (internal to libvlf.so).
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace vlf {
+
+struct Params;
+
+// SIMT fp32-FMA kernels (simt.cu): every dtype and head width up to 256.
+cudaError_t simt_forward(const Params &p, cudaStream_t st);
+// ev: NULL or VLF_BWD_STAGES + 1 events recorded before the first and after each stage.
+cudaError_t simt_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev);
+
+// Tensor-core kernels (tc_fwd.cu / tc_bwd.cu).  `supported` says whether the shape has one.
+bool tc_forward_supported(const Params &p);
+cudaError_t tc_forward(const Params &p, cudaStream_t st);
+bool tc_backward_supported(const Params &p);
+cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev);
+size_t tc_backward_workspace(int total_q, int h_q, int d_qk);
+
+// Host-side count of successful kernel launches (api.cu).
+void count_launch(int n = 1);
+
+// Records ev[i] on st when ev is not NULL.
+inline cudaError_t mark(const cudaEvent_t *ev, int i, cudaStream_t st) {
+  return ev ? cudaEventRecord(ev[i], st) : cudaSuccess;
+}
+
+}  // namespace vlf
