@@ -238,6 +238,9 @@ def main():
     # events: per step [fwd start, bwd start(=fwd end), after rowdot, after dkdv, after dq]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + vlf.VLF_BWD_STAGES)]
            for _ in range(args.steps)]
+    for row in evs:  # torch creates the CUDA event at its first record()
+        for e in row:
+            e.record(stream)
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()

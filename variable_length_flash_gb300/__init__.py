@@ -156,7 +156,11 @@ def vlf_attn_varlen_bwd_workspace_size(total_q, total_kv, h_q, h_kv, d_qk, d_v, 
 def _events(evs):
     if evs is None:
         return None, 0
-    arr = (ctypes.c_void_p * len(evs))(*[ctypes.c_void_p(e.cuda_event) for e in evs])
+    handles = [e.cuda_event for e in evs]
+    if not all(handles):
+        raise VlfError(VLF_ERR_INVALID, "stage events must exist (torch creates them at their "
+                       "first record())")
+    arr = (ctypes.c_void_p * len(evs))(*[ctypes.c_void_p(h) for h in handles])
     _events.keep = arr  # keep alive for the duration of the call
     return ctypes.cast(arr, ctypes.c_void_p), len(evs)
 
