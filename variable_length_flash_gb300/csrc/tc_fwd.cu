@@ -1,8 +1,507 @@
-// Tensor-core (tcgen05 / TMEM / TMA) forward: not yet present in this build.
+// Tensor-core forward (sm_103a): tcgen05 MMAs accumulating in TMEM, TMA-staged Q/K/V tiles.
+//
+// The loop is the FlashAttention-2 one that triton-msl part 1 ("What works") describes -- Q
+// staged once, then for each K/V tile: S = Q K^T, online softmax (running max and sum with a
+// rescale), O += P V -- re-laid out for Blackwell:
+//
+//  * A CTA owns two 128-row query tiles of one sequence: consecutive row blocks of one head, or,
+//    when a kv head serves an even number of query heads (GQA), the same rows of two query
+//    heads that share K/V.  Each K/V tile brought into shared memory feeds both.
+//  * Warp roles (320 threads): warp 0 issues TMA loads (Q once, then K and V tiles into rings);
+//    warp 1 allocates TMEM and issues the MMAs from one thread; warps 2-5 run the softmax of
+//    query tile 0 and warps 6-9 that of tile 1, one thread per query row (TMEM lane = row).
+//  * TMEM (512 columns): S_t at column 128 t, O_t at 256 + 128 t.  P_t (16-bit) is written over
+//    the first half of S_t and fed to the P.V MMA straight from TMEM.
+//  * Tile scheduler (mtlattn 0.3.0, "Use"): each query tile visits only the KV tiles of its
+//    causal / window band; the per-element mask is applied only in the tiles the band cuts.
+//    Tiles start at multiples of 128 keys, so skipping changes no bit of the result.
+//  * Online softmax in base 2 with the scale folded into one FMA; the running max used for the
+//    exponent is only moved (and O rescaled) when the row max grows by more than 8 (P <= 256),
+//    which leaves the result mathematically unchanged.
+//  * Every wait is bounded (see tc_common.cuh); a timeout records VLF_ERR_TIMEOUT and the CTA
+//    drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+#include <math.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace vlf {
-bool tc_forward_supported(const Params &) { return false; }
-cudaError_t tc_forward(const Params &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace tc;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+
+template <int DQK, int DV, int NK, int NV>
+struct FwdCfg {
+  static constexpr int KBQ = DQK / 64, KBV = DV / 64;  // 64-column (128-byte) swizzle blocks
+  static constexpr int BLK = 128 * 128;                // bytes of one 128-row x 64-col block
+  static constexpr int Q_BYTES = KBQ * BLK, K_BYTES = KBQ * BLK, V_BYTES = KBV * BLK;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NV * V_BYTES;
+  // barriers: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2],
+  // o_done[2], drain
+  static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NK, B_VF = B_KE + NK, B_VE = B_VF + NV;
+  static constexpr int B_S = B_VE + NV, B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr int THREADS = 320;
+  static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "tile shapes");
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+// Time-bounded wait that ignores the abort flag (used to drain in-flight work at teardown).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 200000000ull) break;
+  }
+}
+
+struct TileInfo {
+  int row0[2], head[2];
+  int jlo[2], jhi[2];  // KV tile range of each query tile (empty: jlo == jhi)
+  int lo, hi;          // union
+};
+
+__device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx, int by,
+                                          bool pair_heads, TileInfo &ti) {
+  for (int t = 0; t < 2; ++t) {
+    ti.row0[t] = pair_heads ? bx * 128 : bx * 256 + 128 * t;
+    ti.head[t] = pair_heads ? 2 * by + t : by;
+    int jl = 0, jh = 0;
+    if (ti.row0[t] < sq.q_len && sq.kv_len > 0) {
+      int klo, khi;
+      kv_band(ti.row0[t], min(ti.row0[t] + 128, sq.q_len), sq.q_len, sq.kv_len, p.causal,
+              p.window, klo, khi);
+      if (p.flags & VLF_FLAG_NO_SKIP) { klo = 0; khi = sq.kv_len; }
+      if (khi > klo) { jl = klo / 128; jh = (khi + 127) / 128; }
+    }
+    ti.jlo[t] = jl;
+    ti.jhi[t] = jh;
+  }
+  const bool e0 = ti.jhi[0] <= ti.jlo[0], e1 = ti.jhi[1] <= ti.jlo[1];
+  if (e0 && e1) { ti.lo = ti.hi = 0; }
+  else if (e0) { ti.lo = ti.jlo[1]; ti.hi = ti.jhi[1]; }
+  else if (e1) { ti.lo = ti.jlo[0]; ti.hi = ti.jhi[0]; }
+  else { ti.lo = min(ti.jlo[0], ti.jlo[1]); ti.hi = max(ti.jhi[0], ti.jhi[1]); }
+}
+
+template <int DQK, int DV, int NK, int NV>
+__global__ void __launch_bounds__(320, 1)
+tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
+  using C = FwdCfg<DQK, DV, NK, NV>;
+  extern __shared__ uint8_t smem_raw[];
+  const bool pair_heads = (p.group % 2 == 0);
+  const int s = blockIdx.z;
+  Seq sq;
+  if (!load_seq(p, s, sq)) return;
+  if (s == 0 && (__ldg(p.cu_q) != 0 || __ldg(p.cu_kv) != 0)) set_error(p.err, VLF_ERR_BAD_SEQLENS);
+  if (s == p.num_seqs - 1 && (sq.q0 + sq.q_len != p.total_q || sq.k0 + sq.kv_len != p.total_kv))
+    set_error(p.err, VLF_ERR_BAD_SEQLENS);
+  // heavy (late, long-band) row blocks first under causal masking
+  const int bx = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  TileInfo ti;
+  tile_info(p, sq, bx, blockIdx.y, pair_heads, ti);
+  if (ti.row0[0] >= sq.q_len) return;  // whole CTA beyond this sequence
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t bar0 = base + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_Q), 1);
+    for (int i = 0; i < NK; ++i) { mbar_init(bar(C::B_KF + i), 1); mbar_init(bar(C::B_KE + i), 1); }
+    for (int i = 0; i < NV; ++i) { mbar_init(bar(C::B_VF + i), 1); mbar_init(bar(C::B_VE + i), 1); }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::B_S + t), 1);
+      mbar_init(bar(C::B_P + t), 128);
+      mbar_init(bar(C::B_O + t), 1);
+    }
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int hk = ti.head[0] / p.group;  // both query tiles read the same kv head
+  const int is_bf16 = p.dtype == VLF_BF16;
+  const int lo = ti.lo, hi = ti.hi;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && hi > lo) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      int nq = 0;
+      for (int t = 0; t < 2; ++t) nq += ti.row0[t] < sq.q_len ? 1 : 0;
+      mbar_expect_tx(bar(C::B_Q), nq * C::Q_BYTES);
+      for (int t = 0; t < 2; ++t) {
+        if (ti.row0[t] >= sq.q_len) continue;
+        for (int c = 0; c < C::KBQ; ++c)
+          tma_load_2d(sQ + t * C::Q_BYTES + c * C::BLK, &maps.q, ti.head[t] * DQK + 64 * c,
+                      sq.q0 + ti.row0[t], bar(C::B_Q));
+      }
+      int k_issued[NK] = {0}, v_issued[NV] = {0};
+      bool ok = true;
+      for (int j = lo; j < hi && ok; ++j) {
+        const int it = j - lo;
+        const int ks = it % NK, vs = it % NV;
+        if (it >= NK) ok = mbar_wait(bar(C::B_KE + ks), ((it / NK) - 1) & 1, abort_flag, p.err);
+        if (!ok) break;
+        mbar_expect_tx(bar(C::B_KF + ks), C::K_BYTES);
+        for (int c = 0; c < C::KBQ; ++c)
+          tma_load_2d(sK + ks * C::K_BYTES + c * C::BLK, &maps.k, hk * DQK + 64 * c,
+                      sq.k0 + j * 128, bar(C::B_KF + ks));
+        ++k_issued[ks];
+        if (it >= NV) ok = mbar_wait(bar(C::B_VE + vs), ((it / NV) - 1) & 1, abort_flag, p.err);
+        if (!ok) break;
+        mbar_expect_tx(bar(C::B_VF + vs), C::V_BYTES);
+        for (int c = 0; c < C::KBV; ++c)
+          tma_load_2d(sV + vs * C::V_BYTES + c * C::BLK, &maps.v, hk * DV + 64 * c,
+                      sq.k0 + j * 128, bar(C::B_VF + vs));
+        ++v_issued[vs];
+      }
+      // make sure no copy is still landing in shared memory when the CTA leaves
+      drain_wait(bar(C::B_Q), 0);
+      for (int i = 0; i < NK; ++i)
+        if (k_issued[i]) drain_wait(bar(C::B_KF + i), (k_issued[i] - 1) & 1);
+      for (int i = 0; i < NV; ++i)
+        if (v_issued[i]) drain_wait(bar(C::B_VF + i), (v_issued[i] - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && hi > lo) {
+      const uint32_t id_s = idesc_f16(is_bf16, 128, 128, 0, 0);  // S = Q K^T, both K-major
+      const uint32_t id_o = idesc_f16(is_bf16, 128, DV, 0, 1);   // O += P V, V MN-major
+      int pv_count[2] = {0, 0}, p_count[2] = {0, 0};
+      auto part = [&](int t, int j) { return j >= ti.jlo[t] && j < ti.jhi[t]; };
+      auto issue_s = [&](int t, int j) {
+        const uint32_t ks = (uint32_t)((j - lo) % NK);
+        const uint32_t qa = sQ + t * C::Q_BYTES, ka = sK + ks * C::K_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
+          mma_ss(tmem + 128 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 id_s, kk > 0);
+        }
+        mma_commit(bar(C::B_S + t));
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vs = (uint32_t)((j - lo) % NV);
+        const uint32_t va = sV + vs * C::V_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk)
+          mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8,
+                 sdesc_sw128(va + kk * 2048, C::BLK, 1024), id_o, (j > ti.jlo[t] || kk > 0) ? 1u : 0u);
+        mma_commit(bar(C::B_O + t));
+        ++pv_count[t];
+      };
+      bool ok = mbar_wait(bar(C::B_Q), 0, abort_flag, p.err) &&
+                mbar_wait(bar(C::B_KF + 0), 0, abort_flag, p.err);
+      if (ok) {
+        fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (part(t, lo)) issue_s(t, lo);
+        mma_commit(bar(C::B_KE + 0));
+      }
+      for (int j = lo; j < hi && ok; ++j) {
+        const int it = j - lo;
+        ok = mbar_wait(bar(C::B_VF + it % NV), (it / NV) & 1, abort_flag, p.err);
+        if (!ok) break;
+        fence_after();
+        bool k_next = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (part(t, j)) {
+            ok = mbar_wait(bar(C::B_P + t), p_count[t] & 1, abort_flag, p.err);
+            if (!ok) break;
+            ++p_count[t];
+            fence_after();
+            issue_pv(t, j);
+          }
+          if (j + 1 < hi && part(t, j + 1)) {
+            if (!k_next) {
+              ok = mbar_wait(bar(C::B_KF + (it + 1) % NK), ((it + 1) / NK) & 1, abort_flag, p.err);
+              if (!ok) break;
+              k_next = true;
+            }
+            // S_t(j+1) overwrites the TMEM columns P_t(j) was read from: wait for that P.V
+            if (part(t, j)) ok = mbar_wait(bar(C::B_O + t), (pv_count[t] - 1) & 1, abort_flag, p.err);
+            if (!ok) break;
+            fence_after();
+            issue_s(t, j + 1);
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(C::B_VE + it % NV));
+        if (j + 1 < hi) mma_commit(bar(C::B_KE + (it + 1) % NK));
+      }
+      // drain: every MMA this thread issued has completed before TMEM is released
+      mma_commit(bar(C::B_DRAIN));
+      drain_wait(bar(C::B_DRAIN), 0);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax / epilogue
+    const int t = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;
+    const int i = ti.row0[t] + r;  // sequence-local query row
+    const bool row_ok = i < sq.q_len;
+    const int off = sq.kv_len - sq.q_len;
+    const int head = ti.head[t];
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    const uint32_t s_addr = lane_addr + 128 * t, o_addr = lane_addr + 256 + 128 * t;
+    const float sl2 = p.scale_log2;
+    const float *brow = nullptr;
+    if (p.bias && row_ok) {
+      const int bh = p.bias_heads == 1 ? 0 : head;
+      brow = p.bias + ((size_t)(sq.q0 + i) * (size_t)p.bias_heads + (size_t)bh) * (size_t)p.max_kv;
+    }
+    float m_ref = -INFINITY, l = 0.f;
+    const int jlo = ti.jlo[t], jhi = ti.jhi[t];
+    bool ok = true;
+    for (int j = jlo; j < jhi; ++j) {
+      const int n = j - jlo;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_S + t), n & 1, abort_flag, p.err));
+      if (!ok) break;
+      fence_after();
+      const int kb = j * 128;
+      const bool full = row_ok && (kb + 127 < sq.kv_len) && (!p.causal || kb + 127 <= i + off) &&
+                        (p.window <= 0 || kb >= i + off - p.window + 1);
+      const bool plain = full && brow == nullptr;
+      // pass 1: row max of the base-2 logits
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(s_addr + ch * 32, v);
+        tmem_ld_wait();
+        if (plain) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int kj = kb + ch * 32 + e;
+            float x = -INFINITY;
+            if (row_ok && pair_visible(i, kj, off, sq.kv_len, p.causal, p.window)) {
+              x = __uint_as_float(v[e]) * sl2;
+              if (brow) x = fmaf(__ldg(brow + kj), kLog2e, x);
+            }
+            mx = fmaxf(mx, x);
+          }
+        }
+      }
+      if (plain) mx *= sl2;
+      // move the reference max only when it grows by more than the threshold
+      const float m_new = fmaxf(m_ref, mx);
+      float alpha = 1.f;
+      bool move = false;
+      if (m_new != -INFINITY && m_new > m_ref + kRescaleThreshold) {
+        alpha = ex2(m_ref - m_new);  // m_ref == -inf -> 0
+        move = true;
+      }
+      // O_t holds earlier tiles' P.V (complete: S_t(j) was issued after it); rescale rows whose
+      // reference moved and that have accumulated something
+      const bool need = move && n > 0 && l > 0.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float a = need ? alpha : 1.f;
+#pragma unroll 1
+        for (int ch = 0; ch < DV / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(o_addr + ch * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+          tmem_st32(o_addr + ch * 32, v);
+        }
+      }
+      if (move) {
+        l *= alpha;
+        m_ref = m_new;
+      }
+      // pass 2: P = 2^(logit2 - m_ref), row sum, 16-bit P over the first half of S_t
+      const bool dead = (m_ref == -INFINITY);
+      const float neg_m = -m_ref;
+      float sum = 0.f;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(s_addr + ch * 32, v);
+        tmem_ld_wait();
+        float pr[32];
+        if (dead) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pr[e] = 0.f;
+        } else if (plain) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pr[e] = ex2(fmaf(__uint_as_float(v[e]), sl2, neg_m));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int kj = kb + ch * 32 + e;
+            float x = -INFINITY;
+            if (row_ok && pair_visible(i, kj, off, sq.kv_len, p.causal, p.window)) {
+              x = __uint_as_float(v[e]) * sl2;
+              if (brow) x = fmaf(__ldg(brow + kj), kLog2e, x);
+            }
+            pr[e] = ex2(x + neg_m);
+          }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          sum += pr[2 * e] + pr[2 * e + 1];
+          pk[e] = pack2(pr[2 * e], pr[2 * e + 1], is_bf16);
+        }
+        __syncwarp();
+        tmem_st16(s_addr + ch * 16, pk);
+      }
+      l += sum;
+      __syncwarp();
+      tmem_st_wait();
+      fence_before();
+      mbar_arrive(bar(C::B_P + t));
+    }
+    // epilogue: O / l in the output dtype, LSE in natural log
+    const int nt = jhi - jlo;
+    if (ok && nt > 0) ok = mbar_wait(bar(C::B_O + t), (nt - 1) & 1, abort_flag, p.err);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t grow = (size_t)sq.q0 + (size_t)(row_ok ? i : 0);
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
+                                             ((grow * p.h_q + head) * DV) * 2);
+#pragma unroll 1
+      for (int ch = 0; ch < DV / 32; ++ch) {
+        uint32_t v[32];
+        if (nt > 0) {
+          __syncwarp();
+          tmem_ld32(o_addr + ch * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv, is_bf16);
+        if (row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[ch * 4 + q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
+      }
+      if (row_ok && p.lse)
+        p.lse[(size_t)head * p.total_q + grow] = l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+// 2-D map over a [rows, cols] row-major 16-bit matrix with row pitch `pitch_elems`; box of 64
+// columns x box_rows rows, 128-byte swizzle (the layout the MMA descriptors above expect).
+bool make_tmap_16bit(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+                     uint64_t pitch_elems, uint32_t box_rows, int is_bf16) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   2, const_cast<void *>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool tc_forward_supported(const Params &p) {
+  if (p.dtype != VLF_F16 && p.dtype != VLF_BF16) return false;
+  const bool shape = (p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 128 && p.d_v == 128) ||
+                     (p.d_qk == 192 && p.d_v == 128);
+  return shape;
+}
+
+namespace {
+template <int DQK, int DV, int NK, int NV>
+cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
+  using C = FwdCfg<DQK, DV, NK, NV>;
+  FwdMaps maps;
+  const int bf = p.dtype == VLF_BF16;
+  if (p.total_q == 0 || p.total_kv == 0) return simt_forward(p, st);  // nothing to stage
+  if (!make_tmap_16bit(&maps.q, p.q, p.total_q, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, 128, bf) ||
+      !make_tmap_16bit(&maps.k, p.k, p.total_kv, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, 128, bf) ||
+      !make_tmap_16bit(&maps.v, p.v, p.total_kv, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, 128, bf))
+    return cudaErrorInvalidValue;
+  const bool pair_heads = (p.group % 2 == 0);
+  const int rows_per_cta = pair_heads ? 128 : 256;
+  const dim3 grid((p.max_q + rows_per_cta - 1) / rows_per_cta, pair_heads ? p.h_q / 2 : p.h_q,
+                  p.num_seqs);
+  if (grid.x == 0) return cudaSuccess;
+  auto kern = tc_fwd_kernel<DQK, DV, NK, NV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(maps, p);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+}  // namespace
+
+cudaError_t tc_forward(const Params &p, cudaStream_t st) {
+  if (p.d_qk == 64) return launch_fwd<64, 64, 3, 3>(p, st);
+  if (p.d_qk == 128) return launch_fwd<128, 128, 2, 2>(p, st);
+  return launch_fwd<192, 128, 2, 1>(p, st);
+}
+
 }  // namespace vlf
