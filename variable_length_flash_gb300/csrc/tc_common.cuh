@@ -210,6 +210,12 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// The two 16-bit values of a packed pair, back in fp32 (exact).
+__device__ __forceinline__ float2 unpack2(uint32_t v, int is_bf16) {
+  if (is_bf16) return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  return __half22float2(*reinterpret_cast<__half2 *>(&v));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -17,7 +17,8 @@
 //    Tiles start at multiples of 128 keys, so skipping changes no bit of the result.
 //  * Online softmax in base 2 with the scale folded into one FMA; the running max used for the
 //    exponent is only moved (and O rescaled) when the row max grows by more than 8 (P <= 256),
-//    which leaves the result mathematically unchanged.
+//    which leaves the result mathematically unchanged.  The row sum adds the 16-bit P values
+//    the MMA actually multiplies, so the output weights are normalised exactly.
 //  * Every wait is bounded (see tc_common.cuh); a timeout records VLF_ERR_TIMEOUT and the CTA
 //    drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -374,11 +375,14 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
             pr[e] = ex2(x + neg_m);
           }
         }
+        // the row sum is taken over the rounded P the MMA consumes, so the weights that
+        // multiply V are normalised exactly (a one-hot row returns its V row unchanged)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          sum += pr[2 * e] + pr[2 * e + 1];
           pk[e] = pack2(pr[2 * e], pr[2 * e + 1], is_bf16);
+          const float2 r2 = unpack2(pk[e], is_bf16);
+          sum += r2.x + r2.y;
         }
         __syncwarp();
         tmem_st16(s_addr + ch * 16, pk);
