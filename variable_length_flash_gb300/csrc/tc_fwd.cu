@@ -17,8 +17,9 @@
 //    Tiles start at multiples of 128 keys, so skipping changes no bit of the result.
 //  * Online softmax in base 2 with the scale folded into one FMA; the running max used for the
 //    exponent is only moved (and O rescaled) when the row max grows by more than 8 (P <= 256),
-//    which leaves the result mathematically unchanged.  The row sum adds the 16-bit P values
-//    the MMA actually multiplies, so the output weights are normalised exactly.
+//    which leaves the result mathematically unchanged.  O is normalised by the sum of the
+//    16-bit P values the MMA actually multiplies (a one-hot row returns its V row unchanged);
+//    LSE uses the fp32 sum.
 //  * Every wait is bounded (see tc_common.cuh); a timeout records VLF_ERR_TIMEOUT and the CTA
 //    drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -282,7 +283,8 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       const int bh = p.bias_heads == 1 ? 0 : head;
       brow = p.bias + ((size_t)(sq.q0 + i) * (size_t)p.bias_heads + (size_t)bh) * (size_t)p.max_kv;
     }
-    float m_ref = -INFINITY, l = 0.f;
+    // l: sum of the rounded P the MMA multiplies (normalises O); lf: the fp32 sum (for LSE)
+    float m_ref = -INFINITY, l = 0.f, lf = 0.f;
     const int jlo = ti.jlo[t], jhi = ti.jhi[t];
     bool ok = true;
     for (int j = jlo; j < jhi; ++j) {
@@ -344,12 +346,13 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       }
       if (move) {
         l *= alpha;
+        lf *= alpha;
         m_ref = m_new;
       }
       // pass 2: P = 2^(logit2 - m_ref), row sum, 16-bit P over the first half of S_t
       const bool dead = (m_ref == -INFINITY);
       const float neg_m = -m_ref;
-      float sum = 0.f;
+      float sum = 0.f, sumf = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
@@ -383,11 +386,13 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           pk[e] = pack2(pr[2 * e], pr[2 * e + 1], is_bf16);
           const float2 r2 = unpack2(pk[e], is_bf16);
           sum += r2.x + r2.y;
+          sumf += pr[2 * e] + pr[2 * e + 1];
         }
         __syncwarp();
         tmem_st16(s_addr + ch * 16, pk);
       }
       l += sum;
+      lf += sumf;
       __syncwarp();
       tmem_st_wait();
       fence_before();
@@ -425,7 +430,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         }
       }
       if (row_ok && p.lse)
-        p.lse[(size_t)head * p.total_q + grow] = l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+        p.lse[(size_t)head * p.total_q + grow] = lf > 0.f ? (m_ref + lg2(lf)) * kLn2 : -INFINITY;
     }
   }
 
