@@ -103,8 +103,9 @@ int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
                            void *out, float *lse, vlf_stream_t stream, unsigned flags);
 
 /*
- * Bytes of fp32 workspace vlf_attn_varlen_bwd needs (row dot products dO.O, fp32 dQ
- * accumulator).  Pure host arithmetic; never fails (returns 0 for invalid sizes).
+ * Bytes of fp32 workspace vlf_attn_varlen_bwd needs: the row dot products D = rowsum(dO o O),
+ * [h_q, total_q] fp32 (rounded up to 256 bytes).  Pure host arithmetic; never fails (returns 0
+ * for invalid sizes).
  */
 size_t vlf_attn_varlen_bwd_workspace_size(int total_q, int total_kv, int h_q, int h_kv,
                                           int d_qk, int d_v, int dtype);

@@ -221,11 +221,8 @@ int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   p.lse = const_cast<float *>(lse);
   p.dout = dout;
   p.dq = dq; p.dk = dk; p.dv = dv;
-  size_t rowdot = (size_t)h_q * (size_t)total_q * sizeof(float);
-  rowdot = (rowdot + 255) & ~(size_t)255;
   p.rowdot = static_cast<float *>(workspace);
-  p.dq_acc = dtype == VLF_F32 ? nullptr
-                              : reinterpret_cast<float *>(static_cast<char *>(workspace) + rowdot);
+  p.dq_acc = nullptr;
   p.err = error_word_ptr();
   if (!p.err) return VLF_ERR_LAUNCH;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

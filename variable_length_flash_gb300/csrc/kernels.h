@@ -9,6 +9,8 @@ struct Params;
 
 // SIMT fp32-FMA kernels (simt.cu): every dtype and head width up to 256.
 cudaError_t simt_forward(const Params &p, cudaStream_t st);
+// Backward pre-pass: rowdot[h, row] = sum_c dO[row, h, c] * O[row, h, c] (simt.cu).
+cudaError_t rowdot_forward(const Params &p, cudaStream_t st);
 // ev: NULL or VLF_BWD_STAGES + 1 events recorded before the first and after each stage.
 cudaError_t simt_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev);
 

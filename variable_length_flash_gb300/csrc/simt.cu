@@ -421,6 +421,20 @@ cudaError_t simt_forward(const Params &p, cudaStream_t st) {
   }
 }
 
+cudaError_t rowdot_forward(const Params &p, cudaStream_t st) {
+  if (p.total_q == 0) return cudaSuccess;
+  const long long pairs = (long long)p.total_q * p.h_q;
+  const unsigned blocks = (unsigned)((pairs + 7) / 8);
+  switch (p.dtype) {
+    case VLF_F16: rowdot_kernel<__half><<<blocks, 256, 0, st>>>(p); break;
+    case VLF_BF16: rowdot_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(p); break;
+    default: rowdot_kernel<float><<<blocks, 256, 0, st>>>(p); break;
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
 cudaError_t simt_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   switch (p.dtype) {
     case VLF_F16: return bwd_t<__half>(p, st, ev);
