@@ -67,7 +67,7 @@ def test_host_refusals_before_any_launch(kw, status):
 
 def test_workspace_size_query():
     n = vlf.vlf_attn_varlen_bwd_workspace_size(1000, 1000, 8, 2, 128, 128, vlf.VLF_BF16)
-    assert n >= 1000 * 8 * 4 + 1000 * 8 * 128 * 4
+    assert n >= 1000 * 8 * 4 and n % 256 == 0          # D = rowsum(dO o O), [H_q, total_q] fp32
     assert vlf.vlf_attn_varlen_bwd_workspace_size(-1, 0, 8, 2, 128, 128, vlf.VLF_BF16) == 0
 
 

@@ -53,7 +53,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with parity `parity` of barrier `bar` to complete.  Bounded: gives up after
 // kTimeoutNs (recording VLF_ERR_TIMEOUT) or as soon as another role of the CTA has given up.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                        int *err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
