@@ -188,6 +188,35 @@ int vlf_sched_kv_band(int r0, int r1, int q_len, int kv_len, int causal, int win
 int vlf_sched_q_band(int j0, int j1, int q_len, int kv_len, int causal, int window,
                      int *lo, int *hi);
 
+/*
+ * Backward that allocates nothing.  The pages have no counterpart to this entry point; it exists
+ * for callers that cannot allocate device memory at call time -- a plugin whose enqueue hook may
+ * not allocate, a service that reserves its memory budget up front, or code that must not
+ * trigger the device-wide synchronisation cudaMalloc / cudaFree can cause.  Same arguments and
+ * results as vlf_attn_varlen_bwd without the workspace: the row dot products live in a
+ * fixed-size array inside the library's own device memory instead.
+ *   - Size limit: h_q * total_q <= 8,388,608 (vlf_noalloc_scratch_bytes() bytes of fp32);
+ *     larger problems return VLF_ERR_UNSUPPORTED before anything is enqueued.
+ *   - Every GPU that loads the library holds that array (32 MiB) until the process exits.
+ *   - Calls on one device share the array and it keeps the last call's contents (nothing in it
+ *     needs to start at zero).  Calls whose work overlaps on the GPU race on it: order them on
+ *     one stream, or with events.
+ *   - The first call on each device looks up the array's device address; make that first call
+ *     before any stream capture begins.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+int vlf_attn_varlen_bwd_noalloc(const void *q, const void *k, const void *v, const void *out,
+                                const float *lse, const void *dout,
+                                const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv,
+                                int num_seqs, int total_q, int total_kv, int max_seqlen_q,
+                                int max_seqlen_kv, int h_q, int h_kv, int d_qk, int d_v, int dtype,
+                                float scale, int causal, int window,
+                                const float *bias, int bias_heads,
+                                void *dq, void *dk, void *dv, vlf_stream_t stream);
+
+/* Bytes of the fixed array vlf_attn_varlen_bwd_noalloc uses as its workspace. */
+size_t vlf_noalloc_scratch_bytes(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int vlf_version(void);
 

@@ -39,7 +39,8 @@ _DTYPE = {torch.float16: VLF_F16, torch.bfloat16: VLF_BF16, torch.float32: VLF_F
 EXPORTS = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_fwd_ex", "vlf_attn_varlen_bwd",
            "vlf_attn_varlen_bwd_ex", "vlf_attn_varlen_bwd_workspace_size", "vlf_check_error",
            "vlf_status_string", "vlf_sched_kv_band", "vlf_sched_q_band", "vlf_version",
-           "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path"]
+           "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path", "vlf_attn_varlen_bwd_noalloc",
+           "vlf_noalloc_scratch_bytes"]
 VLF_BWD_STAGES = 3
 BWD_STAGE_NAMES = ["rowdot", "dkdv", "dq"]
 
@@ -78,6 +79,10 @@ def _load():
     lib.vlf_sched_q_band.restype = I
     lib.vlf_version.argtypes = []
     lib.vlf_version.restype = I
+    lib.vlf_attn_varlen_bwd_noalloc.argtypes = bwd[:23] + [P, P, P, P]  # ... bias_heads, dq, dk, dv, stream
+    lib.vlf_attn_varlen_bwd_noalloc.restype = I
+    lib.vlf_noalloc_scratch_bytes.argtypes = []
+    lib.vlf_noalloc_scratch_bytes.restype = Z
     lib.vlf_launch_count.argtypes = []
     lib.vlf_launch_count.restype = ctypes.c_uint64
     for name in ("vlf_fwd_path", "vlf_bwd_path"):
@@ -261,7 +266,42 @@ def vlf_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, ma
     return dq, dk, dv
 
 
+def vlf_noalloc_scratch_bytes() -> int:
+    return int(_lib.vlf_noalloc_scratch_bytes())
+
+
+def vlf_attn_varlen_bwd_noalloc(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv,
+                                max_seqlen_q, max_seqlen_kv=None, scale=None, causal=False,
+                                window=0, bias=None, dq=None, dk=None, dv=None, stream=None):
+    """Backward through the entry point that allocates nothing on the device: the library keeps
+    the row-dot workspace in a fixed array of its own (vlf_noalloc_scratch_bytes() bytes per
+    GPU), for callers that cannot allocate device memory when they call.  Calls that overlap on
+    the GPU share that array and race; problems with h_q * total_q above the array's size are
+    refused.  The gradient outputs are allocated here with torch only when not passed in."""
+    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _req(t, n, q.dtype)
+    _req(lse, "lse", torch.float32)
+    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
+    tq, hq, dqk = q.shape
+    tk, hkv, dvv = v.shape
+    if max_seqlen_kv is None:
+        max_seqlen_kv = int(bias.shape[2]) if bias is not None else _max_len(cu_seqlens_kv)
+    bias, bh = _bias_args(bias, tq, hq)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = _lib.vlf_attn_varlen_bwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_kv), cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q),
+        int(max_seqlen_kv), hq, hkv, dqk, dvv, _DTYPE[q.dtype], float(scale) if scale else 0.0,
+        int(bool(causal)), int(window or 0), _ptr(bias), bh, _ptr(dq), _ptr(dk), _ptr(dv),
+        _stream(stream))
+    _check(st, "vlf_attn_varlen_bwd_noalloc")
+    return dq, dk, dv
+
+
 __all__ = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_bwd", "vlf_attn_varlen_bwd_workspace_size",
            "vlf_check_error", "vlf_status_string", "vlf_sched_kv_band", "vlf_sched_q_band",
-           "vlf_version", "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path", "VlfError",
+           "vlf_version", "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path",
+           "vlf_attn_varlen_bwd_noalloc", "vlf_noalloc_scratch_bytes", "VlfError",
            "LIB_PATH", "EXPORTS"]
