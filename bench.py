@@ -194,7 +194,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-units", type=int, default=3,
+    ap.add_argument("--cpu-units", type=int, default=20,
                     help="(sequence, head) units of the workload for the CPU oracle baseline")
     args = ap.parse_args()
     rank, world, local = dist_setup()

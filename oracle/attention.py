@@ -183,6 +183,23 @@ def head_backward(q, k, v, dout, scale, causal=False, window=0, bias=None,
     return {"O": O, "LSE": LSE, "dq": dq, "dk": dk, "dv": dv}
 
 
+def head_backward_rows(q_rows, rows, k, v, dout_rows, q_len, scale, causal=False, window=0,
+                       bias_rows=None):
+    """dQ of the sequence-local ``rows`` of one query head (plus their O and LSE).
+
+    Every quantity dQ_i needs -- the row's softmax P_i, D_i = dO_i . O_i, dP_i = dO_i V^T and
+    dS_i = P_i o (dP_i - D_i) -- belongs to row i alone, so this is the definition in
+    head_backward restricted to the given rows.  q_rows [n, D_qk], dout_rows [n, D_v],
+    bias_rows [n, kv_len] or None.  Returns O [n, D_v], LSE [n], dq [n, D_qk].
+    """
+    ok = visible(q_len, k.shape[0], causal, window, rows)
+    P, lse = softmax(logits(q_rows, k, scale, ok, bias_rows))
+    O = P @ v
+    Di = (dout_rows * O).sum(axis=1)
+    dS = P * (dout_rows @ v.T - Di[:, None])
+    return O, lse, scale * (dS @ k)
+
+
 def backward(q, k, v, dout, cu_q, cu_kv, scale=None, causal=False, window=0, bias=None):
     """Whole packed backward (small problems).  Returns dq, dk, dv (float64, input layouts).
 

@@ -394,7 +394,13 @@ def check_subset_and_chunks(orc):
     part = orc.head_backward(q, k, v, do, 0.5, True, 4, lambda idx: bias[idx], rows, cols, chunk=3)
     ok = (_close(part["dq"], full["dq"][rows], 1e-12) and _close(part["dk"], full["dk"][cols], 1e-12)
           and _close(part["dv"], full["dv"][cols], 1e-12) and _close(part["O"], full["O"], 1e-12))
-    return (ok, "" if ok else "subset/chunked backward differs")
+    if not ok:
+        return False, "subset/chunked backward differs"
+    # the row-local form used for sampled rows of large inputs
+    O, L, dq = orc.head_backward_rows(q[rows], rows, k, v, do[rows], L, 0.5, True, 4, bias[rows])
+    ok = (_close(O, full["O"][rows], 1e-12) and _close(L, full["LSE"][rows], 1e-12)
+          and _close(dq, full["dq"][rows], 1e-12))
+    return (ok, "" if ok else "row-local backward differs")
 
 
 ALL_CHECKS = [check_worked_examples, check_masks, check_single_key_and_identical_keys,

@@ -1,0 +1,122 @@
+"""GPU vs fp64 oracle at the benchmark workloads' full sizes, in the launch configuration bench.py
+times (default flags, tensor-core path):
+
+* O, LSE and dQ on seeded random query rows plus the last 4 rows of every sequence (the rows a
+  32-bit index overflow would corrupt first), for a sample of query heads that includes the
+  first and the last;
+* dK and dV on whole (sequence, kv head) units -- every key of the unit, summed over the GQA
+  group -- including the last sequence and the last kv head.  For the 49,152-token sequence the
+  unit's keys are a seeded sample plus the prefix boundary and the last key (the oracle still
+  takes every query row into each key's sum).
+
+Inputs are drawn on the device with the seeded generators; the oracle receives host copies of
+the input tensors and recomputes the bias rows on the host from the same fp64 formula.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as orc
+from tests.parity import LSE_TOL, TOL, gpu_run, max_err
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+LARGE = ["dense4x4096_bf16_causal", "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
+         "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix"]
+
+
+def _np(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _head_sample(w, rng):
+    heads = {0, w.h_q - 1}
+    while len(heads) < min(4, w.h_q):
+        heads.add(int(rng.integers(0, w.h_q)))
+    return sorted(heads)
+
+
+def _bias_rows(w, grows, head):
+    """fp64 bias rows (global query rows `grows`) for query head `head`, from the generator."""
+    hb = 0 if w.bias_heads == 1 else head
+    b = W.bias_block(w, torch.as_tensor(np.asarray(grows), dtype=torch.int64), [hb])
+    return b[:, 0, :].double().numpy()
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_full_size_workload(name):
+    torch.cuda.empty_cache()
+    w = W.workload(name)
+    x = W.make_inputs(w, seed=0, device="cuda", with_dout=True)
+    res = gpu_run(w, x)
+    tol = TOL[w.dtype]
+    rng = np.random.default_rng(2024)
+    cu = [0]
+    for L in w.lengths_q:
+        cu.append(cu[-1] + L)
+    g = w.h_q // w.h_kv
+    scale = w.softmax_scale
+
+    # ---------------------------------------------------------------- sampled rows: O, LSE, dQ
+    rows = W.sample_rows(w, n_random=256, seed=3, tail=4)
+    heads = _head_sample(w, rng)
+    rows_t = torch.as_tensor(rows, dtype=torch.int64, device="cuda")
+    q_rows = _np(x["q"][rows_t])
+    do_rows = _np(x["dout"][rows_t])
+    out_rows, dq_rows = _np(res["out"][rows_t]), _np(res["dq"][rows_t])
+    lse_all = res["lse"]
+    seq_of = np.searchsorted(np.asarray(cu), np.asarray(rows), side="right") - 1
+    errs = {"out": 0.0, "lse": 0.0, "dq": 0.0}
+    for s in sorted(set(seq_of.tolist())):
+        sel = np.nonzero(seq_of == s)[0]
+        local = np.asarray(rows)[sel] - cu[s]
+        k0, k1 = cu[s], cu[s + 1]
+        for h in heads:
+            hk = h // g
+            k = _np(x["k"][k0:k1, hk])
+            v = _np(x["v"][k0:k1, hk])
+            b = _bias_rows(w, np.asarray(rows)[sel], h) if w.bias else None
+            O, L, dq = orc.head_backward_rows(q_rows[sel, h], local, k, v, do_rows[sel, h],
+                                              k1 - k0, scale, w.causal, w.window, b)
+            lse_gpu = lse_all[h, torch.as_tensor(np.asarray(rows)[sel], device="cuda")]
+            errs["out"] = max(errs["out"], max_err(out_rows[sel, h], O))
+            errs["lse"] = max(errs["lse"], max_err(_np(lse_gpu), L))
+            errs["dq"] = max(errs["dq"], max_err(dq_rows[sel, h], dq))
+    assert errs["out"] <= tol and errs["lse"] <= LSE_TOL[w.dtype] and errs["dq"] <= 3 * tol, errs
+
+    # ---------------------------------------------------------------- dK / dV units
+    n = w.num_seqs
+    long_seq = max(w.lengths_q) > 20000
+    units = {(n - 1, w.h_kv - 1)}
+    if (n > 1 or w.h_kv > 1) and not long_seq:  # a 49k-token unit costs a minute of fp64 CPU
+        units.add((int(rng.integers(0, n)), int(rng.integers(0, w.h_kv))))
+    for s, hk in sorted(units):
+        q0, q1 = cu[s], cu[s + 1]
+        L = q1 - q0
+        if long_seq:
+            cols = set(rng.choice(L, 96, replace=False).tolist())
+            cols |= {0, 8190, 8191, 8192, 8193, L - 2, L - 1}
+            cols = sorted(c for c in cols if 0 <= c < L)
+        else:
+            cols = None
+        k = _np(x["k"][q0:q1, hk])
+        v = _np(x["v"][q0:q1, hk])
+        dk = 0.0
+        dv = 0.0
+        for gh in range(g):
+            h = hk * g + gh
+            q = _np(x["q"][q0:q1, h])
+            do = _np(x["dout"][q0:q1, h])
+            bias = (lambda idx, h=h: _bias_rows(w, q0 + idx, h)) if w.bias else None
+            r = orc.head_backward(q, k, v, do, scale, w.causal, w.window, bias, rows=[],
+                                  cols=cols, chunk=2048 if long_seq else None)
+            dk = dk + r["dk"]
+            dv = dv + r["dv"]
+        ck = slice(None) if cols is None else torch.as_tensor(cols, device="cuda")
+        gdk = _np(res["dk"][q0:q1, hk][ck])
+        gdv = _np(res["dv"][q0:q1, hk][ck])
+        e_dk, e_dv = max_err(gdk, dk), max_err(gdv, dv)
+        assert e_dk <= 3 * tol and e_dv <= 3 * tol, (name, s, hk, e_dk, e_dv)
+    del x, res
+    torch.cuda.empty_cache()
