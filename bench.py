@@ -80,6 +80,26 @@ def load_peaks():
             "source": "fallback"}
 
 
+def ncu_traffic(role: str, workload: str):
+    """DRAM bytes per launch (read + write) that one ncu capture measured for this kernel on
+    this workload, or None if there is no capture or the kernel's sources changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    k = rec.get("kernels", {}).get(role)
+    if k is None or rec.get("workload") != workload:
+        return None
+    h = hashlib.sha256()
+    for f in k["source_files"]:
+        fp = os.path.join(ROOT, "variable_length_flash_gb300", "csrc", f)
+        if not os.path.exists(fp):
+            return None
+        h.update(open(fp, "rb").read())
+    return k["dram_bytes_per_launch"] if h.hexdigest() == k["source_sha256"] else None
+
+
 class ClockSampler:
     """nvidia-smi SM clock / throttle-reason samples every 200 ms while running."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -291,7 +311,7 @@ def main():
         achieved = flops_of[dom] / (stage_ms[dom] * 1e-3) / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = ncu_traffic(dom, w.name) if tc or dom == "rowdot" else None
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x max SM clock)"
                                              if roof["bound"] == "alu" else "")
