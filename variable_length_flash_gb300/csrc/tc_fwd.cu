@@ -296,31 +296,41 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       const bool full = row_ok && (kb + 127 < sq.kv_len) && (!p.causal || kb + 127 <= i + off) &&
                         (p.window <= 0 || kb >= i + off - p.window + 1);
       const bool plain = full && brow == nullptr;
-      // pass 1: row max of the base-2 logits
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld32(s_addr + ch * 32, v);
-        tmem_ld_wait();
-        if (plain) {
+      // the whole S row (128 fp32) in registers: four TMEM loads, one wait
+      uint32_t v[128];
+      __syncwarp();
+      tmem_ld32_at(s_addr + 0, v, 0);
+      tmem_ld32_at(s_addr + 32, v, 32);
+      tmem_ld32_at(s_addr + 64, v, 64);
+      tmem_ld32_at(s_addr + 96, v, 96);
+      tmem_ld_wait();
+      // row max of the base-2 logits.  plain rows keep raw q.k in v (the scale goes into the
+      // exponent FMA); other rows get v = scale*log2e*q.k + log2e*bias, or -inf where masked.
+      float mx;
+      if (plain) {
+        float m8[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-        } else {
+        for (int q = 0; q < 16; ++q) {
+          const float *f = reinterpret_cast<const float *>(v) + 8 * q;
+          m8[q] = fmax3(fmax3(f[0], f[1], f[2]), fmax3(f[3], f[4], f[5]), fmaxf(f[6], f[7]));
+        }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int kj = kb + ch * 32 + e;
-            float x = -INFINITY;
-            if (row_ok && pair_visible(i, kj, off, sq.kv_len, p.causal, p.window)) {
-              x = __uint_as_float(v[e]) * sl2;
-              if (brow) x = fmaf(__ldg(brow + kj), kLog2e, x);
-            }
-            mx = fmaxf(mx, x);
+        for (int q = 0; q < 5; ++q) m8[q] = fmax3(m8[q], m8[q + 5], m8[q + 10]);
+        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), m8[3], fmaxf(m8[4], m8[15])) * sl2;
+      } else {
+        mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 128; ++e) {
+          const int kj = kb + e;
+          float x = -INFINITY;
+          if (row_ok && pair_visible(i, kj, off, sq.kv_len, p.causal, p.window)) {
+            x = __uint_as_float(v[e]) * sl2;
+            if (brow) x = fmaf(__ldg(brow + kj), kLog2e, x);
           }
+          v[e] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
         }
       }
-      if (plain) mx *= sl2;
       // move the reference max only when it grows by more than the threshold
       const float m_new = fmaxf(m_ref, mx);
       float alpha = 1.f;
@@ -336,12 +346,12 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         const float a = need ? alpha : 1.f;
 #pragma unroll 1
         for (int ch = 0; ch < DV / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(o_addr + ch * 32, v);
+          uint32_t o[32];
+          tmem_ld32(o_addr + ch * 32, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
-          tmem_st32(o_addr + ch * 32, v);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+          tmem_st32(o_addr + ch * 32, o);
         }
       }
       if (move) {
@@ -349,50 +359,35 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         lf *= alpha;
         m_ref = m_new;
       }
-      // pass 2: P = 2^(logit2 - m_ref), row sum, 16-bit P over the first half of S_t
-      const bool dead = (m_ref == -INFINITY);
-      const float neg_m = -m_ref;
-      float sum = 0.f, sumf = 0.f;
-#pragma unroll 1
+      // P = 2^(logit2 - m_ref) two at a time (packed FMA), written in 16-bit over the first half
+      // of S_t.  A row still without any visible key has every logit at -inf: its exponent
+      // offset is taken as 0 so that P = 0.
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+      const uint64_t scale2 = f2pack(plain ? sl2 : 1.f, plain ? sl2 : 1.f);
+      const uint64_t negm2 = f2pack(neg_m, neg_m);
+      uint64_t sumf2 = f2pack(0.f, 0.f);
+      float sumr = 0.f;
+#pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld32(s_addr + ch * 32, v);
-        tmem_ld_wait();
-        float pr[32];
-        if (dead) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pr[e] = 0.f;
-        } else if (plain) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pr[e] = ex2(fmaf(__uint_as_float(v[e]), sl2, neg_m));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int kj = kb + ch * 32 + e;
-            float x = -INFINITY;
-            if (row_ok && pair_visible(i, kj, off, sq.kv_len, p.causal, p.window)) {
-              x = __uint_as_float(v[e]) * sl2;
-              if (brow) x = fmaf(__ldg(brow + kj), kLog2e, x);
-            }
-            pr[e] = ex2(x + neg_m);
-          }
-        }
-        // the row sum is taken over the rounded P the MMA consumes, so the weights that
-        // multiply V are normalised exactly (a one-hot row returns its V row unchanged)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          pk[e] = pack2(pr[2 * e], pr[2 * e + 1], is_bf16);
-          const float2 r2 = unpack2(pk[e], is_bf16);
-          sum += r2.x + r2.y;
-          sumf += pr[2 * e] + pr[2 * e + 1];
+          const int c = ch * 32 + 2 * e;
+          const float2 x = f2unpack(fma2(f2pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                         scale2, negm2));
+          const float pa = ex2(x.x), pb = ex2(x.y);
+          sumf2 = add2(sumf2, f2pack(pa, pb));
+          pk[e] = pack2(pa, pb, is_bf16);
+          // the row sum adds the rounded P the MMA consumes, so the weights that multiply V are
+          // normalised exactly (a one-hot row returns its V row unchanged)
+          sumr = add_halves(sumr, pk[e], is_bf16);
         }
         __syncwarp();
         tmem_st16(s_addr + ch * 16, pk);
       }
-      l += sum;
-      lf += sumf;
+      const float2 sf = f2unpack(sumf2);
+      l += sumr;
+      lf += sf.x + sf.y;
       __syncwarp();
       tmem_st_wait();
       fence_before();
