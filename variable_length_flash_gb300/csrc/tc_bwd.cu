@@ -12,10 +12,13 @@
 //          their A operand from TMEM.  LSE and D of the 64 query columns come through smem.
 //   dQ:    a CTA owns 128 query rows of one head (Q, dO stay in shared memory) and walks the
 //          64-key K / V tiles of its band: S = Q K^T, dP = dO V^T, dS in TMEM, dQ += dS K.
-// Warp roles (192 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps 2-5 compute
-// (one thread per TMEM lane).  S/dP buffers are double-buffered in TMEM where columns allow so
-// the next tile's products overlap this tile's elementwise pass.  Tiles outside the causal /
-// window band are skipped (they contribute exact zeros).  Every wait is bounded.
+// Warp roles (320 threads): warp 0 stages tiles with TMA and, with all its lanes, the item's LSE
+// and D columns into the same shared-memory stage; warp 1 allocates TMEM and issues the MMAs;
+// warps 2-9 are two compute warpgroups, each owning 32 of the item's 64 columns (one thread per
+// TMEM lane, so every row has two threads).  Each warpgroup writes its 16-bit P / dS over its own
+// S / dP columns.  S/dP buffers are double-buffered in TMEM where columns allow so the next
+// tile's products overlap this tile's elementwise pass.  Tiles outside the causal / window band
+// are skipped (they contribute exact zeros).  Every wait is bounded.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -49,8 +52,9 @@ struct BwdCfg {
   static constexpr int I0_BYTES = KB0 * IBLK, I1_BYTES = KB1 * IBLK;
   static constexpr int STAGE_BYTES = I0_BYTES + I1_BYTES;
   static constexpr int OFF_O0 = 0, OFF_O1 = O0_BYTES, OFF_IN = O0_BYTES + O1_BYTES;
-  static constexpr int OFF_LD = OFF_IN + NSTAGE * STAGE_BYTES;  // per-warp LSE / D columns
-  static constexpr int OFF_BAR = OFF_LD + 4 * 128 * 4;
+  // per stage: the item's 64 columns as 32 pairs {-LSE2_c, -LSE2_c+1, -D_c, -D_c+1} (dK/dV)
+  static constexpr int OFF_LD = OFF_IN + NSTAGE * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_LD + NSTAGE * 128 * 4;
   // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE], s_full[NBUF], p_ready[NBUF],
   // item_done[NBUF], drain
   static constexpr int B_OUT = 0, B_IF = 1, B_IE = B_IF + NSTAGE, B_S = B_IE + NSTAGE;
@@ -75,7 +79,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 template <int MODE, int DQK, int DV, int NBUF, int NSTAGE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   using C = BwdCfg<MODE, DQK, DV, NBUF, NSTAGE>;
   extern __shared__ uint8_t smem_raw[];
@@ -117,7 +121,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
   const uint32_t sO0 = base + C::OFF_O0, sO1 = base + C::OFF_O1, sIn = base + C::OFF_IN;
-  float *ldbuf = reinterpret_cast<float *>(gbase + C::OFF_LD);  // [warp][LSE 64 | D 64]
+  float4 *ldbuf = reinterpret_cast<float4 *>(gbase + C::OFF_LD);  // [stage][32 column pairs]
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
@@ -125,10 +129,12 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_OUT), 1);
-    for (int i = 0; i < NSTAGE; ++i) { mbar_init(bar(C::B_IF + i), 1); mbar_init(bar(C::B_IE + i), 1); }
+    // in_full: the TMA bytes plus 33 arrivals (lane 0's expect_tx and every producer lane after
+    // writing its LSE / D pair); p_ready: all 256 compute threads
+    for (int i = 0; i < NSTAGE; ++i) { mbar_init(bar(C::B_IF + i), 33); mbar_init(bar(C::B_IE + i), 1); }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(bar(C::B_S + b), 1);
-      mbar_init(bar(C::B_P + b), 128);
+      mbar_init(bar(C::B_P + b), 256);
       mbar_init(bar(C::B_D + b), 1);
     }
     mbar_init(bar(C::B_DRAIN), 1);
@@ -150,39 +156,67 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   auto item_row = [&](int n) { return MODE == kDkdv ? lo64 + (n % nq_tiles) * 64 : lo64 + n * 64; };
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_items > 0) {
-      tma_prefetch_desc(&maps.outer0);
-      tma_prefetch_desc(&maps.outer1);
-      tma_prefetch_desc(&maps.inner0);
-      tma_prefetch_desc(&maps.inner1);
-      const int orow = (MODE == kDkdv ? sq.k0 : sq.q0) + tile0;
-      const int oh = MODE == kDkdv ? hk : head_outer;  // head index inside the outer tensors
-      mbar_expect_tx(bar(C::B_OUT), C::O0_BYTES + C::O1_BYTES);
-      for (int c = 0; c < C::KB0; ++c)
-        tma_load_2d(sO0 + c * C::OBLK, &maps.outer0, oh * DQK + 64 * c, orow, bar(C::B_OUT));
-      for (int c = 0; c < C::KB1; ++c)
-        tma_load_2d(sO1 + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
-      int issued[NSTAGE] = {0};
-      bool ok = true;
-      for (int n = 0; n < n_items && ok; ++n) {
-        const int st = n % NSTAGE;
-        if (n >= NSTAGE) ok = mbar_wait(bar(C::B_IE + st), ((n / NSTAGE) - 1) & 1, abort_flag, p.err);
-        if (!ok) break;
-        const int ih = MODE == kDkdv ? item_head(n) : hk;  // head inside the inner tensors
-        const int irow = (MODE == kDkdv ? sq.q0 : sq.k0) + item_row(n);
-        const uint32_t dst = sIn + st * C::STAGE_BYTES;
-        mbar_expect_tx(bar(C::B_IF + st), C::STAGE_BYTES);
+    // ------------------------------------------------------------------ producer
+    if (n_items > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&maps.outer0);
+        tma_prefetch_desc(&maps.outer1);
+        tma_prefetch_desc(&maps.inner0);
+        tma_prefetch_desc(&maps.inner1);
+        const int orow = (MODE == kDkdv ? sq.k0 : sq.q0) + tile0;
+        const int oh = MODE == kDkdv ? hk : head_outer;  // head index inside the outer tensors
+        mbar_expect_tx(bar(C::B_OUT), C::O0_BYTES + C::O1_BYTES);
         for (int c = 0; c < C::KB0; ++c)
-          tma_load_2d(dst + c * C::IBLK, &maps.inner0, ih * DQK + 64 * c, irow, bar(C::B_IF + st));
+          tma_load_2d(sO0 + c * C::OBLK, &maps.outer0, oh * DQK + 64 * c, orow, bar(C::B_OUT));
         for (int c = 0; c < C::KB1; ++c)
-          tma_load_2d(dst + C::I0_BYTES + c * C::IBLK, &maps.inner1, ih * DV + 64 * c, irow,
-                      bar(C::B_IF + st));
-        ++issued[st];
+          tma_load_2d(sO1 + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
       }
-      drain_wait(bar(C::B_OUT), 0);
-      for (int i = 0; i < NSTAGE; ++i)
-        if (issued[i]) drain_wait(bar(C::B_IF + i), (issued[i] - 1) & 1);
+      int issued[NSTAGE] = {0};
+      for (int n = 0; n < n_items; ++n) {
+        const int st = n % NSTAGE;
+        if (n >= NSTAGE) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(bar(C::B_IE + st), ((n / NSTAGE) - 1) & 1, abort_flag, p.err);
+          if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
+        }
+        if (MODE == kDkdv) {
+          // -LSE (base 2; -inf for rows that see nothing or lie past the sequence, so P = 0) and
+          // -D of the item's columns 2 lane and 2 lane + 1
+          const int h = item_head(n), i0 = item_row(n);
+          float nl[2], nd[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qi = i0 + 2 * lane + u;
+            nl[u] = -INFINITY;
+            nd[u] = 0.f;
+            if (qi < sq.q_len) {
+              const size_t gi = (size_t)h * p.total_q + sq.q0 + qi;
+              const float L = p.lse[gi];
+              nl[u] = L == -INFINITY ? -INFINITY : -L * kLog2e;
+              nd[u] = -p.rowdot[gi];
+            }
+          }
+          ldbuf[st * 32 + lane] = make_float4(nl[0], nl[1], nd[0], nd[1]);
+        }
+        if (lane == 0) {
+          const int ih = MODE == kDkdv ? item_head(n) : hk;  // head inside the inner tensors
+          const int irow = (MODE == kDkdv ? sq.q0 : sq.k0) + item_row(n);
+          const uint32_t dst = sIn + st * C::STAGE_BYTES;
+          mbar_expect_tx(bar(C::B_IF + st), C::STAGE_BYTES);
+          for (int c = 0; c < C::KB0; ++c)
+            tma_load_2d(dst + c * C::IBLK, &maps.inner0, ih * DQK + 64 * c, irow, bar(C::B_IF + st));
+          for (int c = 0; c < C::KB1; ++c)
+            tma_load_2d(dst + C::I0_BYTES + c * C::IBLK, &maps.inner1, ih * DV + 64 * c, irow,
+                        bar(C::B_IF + st));
+          ++issued[st];
+        }
+        mbar_arrive(bar(C::B_IF + st));
+      }
+      if (lane == 0) {
+        drain_wait(bar(C::B_OUT), 0);
+        for (int i = 0; i < NSTAGE; ++i)
+          if (issued[i]) drain_wait(bar(C::B_IF + i), (issued[i] - 1) & 1);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -192,42 +226,50 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // accumulations: A from TMEM (K = 64 inner rows), B = inner tile MN-major
       const uint32_t id_a0 = idesc_f16(is_bf16, 128, MODE == kDkdv ? DV : DQK, 0, 1);
       const uint32_t id_a1 = idesc_f16(is_bf16, 128, DQK, 0, 1);
+      // descriptors are built once; a K step adds its byte offset / 16 to the start-address
+      // field (shared addresses stay far below the field's 2^18-byte range, so nothing carries)
+      const uint64_t d_o0 = sdesc_sw128(sO0, 16, 1024), d_o1 = sdesc_sw128(sO1, 16, 1024);
       auto issue_sp = [&](int n) {
         const int b = n % NBUF, st = n % NSTAGE;
         const uint32_t in0 = sIn + st * C::STAGE_BYTES, in1 = in0 + C::I0_BYTES;
+        const uint64_t d_i0 = sdesc_sw128(in0, 16, 1024), d_i1 = sdesc_sw128(in1, 16, 1024);
         const uint32_t s_col = tmem + C::BUF + 128 * b, dp_col = s_col + 64;
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss(s_col, sdesc_sw128(sO0 + oa, 16, 1024), sdesc_sw128(in0 + ia, 16, 1024), id_sp, kk > 0);
+          mma_ss(s_col, d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss(dp_col, sdesc_sw128(sO1 + oa, 16, 1024), sdesc_sw128(in1 + ia, 16, 1024), id_sp, kk > 0);
+          mma_ss(dp_col, d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
         }
         mma_commit(bar(C::B_S + b));
       };
+      // the 16-bit A operand of K step kk (16 inner rows): warpgroup kk / 2 wrote it over the first
+      // half of its own 32 columns
+      auto a_col = [](int kk) { return (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1)); };
       auto issue_acc = [&](int n) {
         const int b = n % NBUF, st = n % NSTAGE;
         const uint32_t in0 = sIn + st * C::STAGE_BYTES, in1 = in0 + C::I0_BYTES;
         const uint32_t s_col = tmem + C::BUF + 128 * b, dp_col = s_col + 64;
+        const uint64_t d_i0 = sdesc_sw128(in0, C::IBLK, 1024), d_i1 = sdesc_sw128(in1, C::IBLK, 1024);
         if (MODE == kDkdv) {
-          // dV += P^T dO   (P^T over the first half of S^T; dO MN-major, 64-column blocks 8 KB apart)
+          // dV += P^T dO   (dO MN-major: 64-column blocks 8 KB apart, 16 rows per K step)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::ACC0, s_col + kk * 8, sdesc_sw128(in1 + kk * 2048, C::IBLK, 1024), id_a0,
+            mma_ts(tmem + C::ACC0, s_col + a_col(kk), d_i1 + (uint64_t)((kk * 2048) >> 4), id_a0,
                    (n > 0 || kk > 0) ? 1u : 0u);
           // dK += dS^T Q
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::ACC1, dp_col + kk * 8, sdesc_sw128(in0 + kk * 2048, C::IBLK, 1024), id_a1,
+            mma_ts(tmem + C::ACC1, dp_col + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id_a1,
                    (n > 0 || kk > 0) ? 1u : 0u);
         } else {
           // dQ += dS K   (K tile MN-major)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::ACC0, dp_col + kk * 8, sdesc_sw128(in0 + kk * 2048, C::IBLK, 1024), id_a0,
+            mma_ts(tmem + C::ACC0, dp_col + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id_a0,
                    (n > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(C::B_D + b));
@@ -261,20 +303,22 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     }
   } else {
     // ------------------------------------------------------------------ elementwise + epilogue
+    const int half = (warp - 2) >> 2;  // which 32 of the item's 64 columns
+    const int col0 = 32 * half;
     const int quarter = warp & 3;
     const int r = 32 * quarter + lane;  // TMEM lane = outer row (key for dK/dV, query for dQ)
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     const float sl2 = p.scale_log2;
-    // this thread's outer row
-    const int orow = tile0 + r;
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
+    const int orow = tile0 + r;  // this thread's outer row
     const bool orow_ok = MODE == kDkdv ? orow < sq.kv_len : orow < sq.q_len;
-    float row_lse2 = INFINITY, row_d = 0.f;  // dQ: this row's LSE (base 2) and D
+    float row_nl = -INFINITY, row_nd = 0.f;  // dQ: this row's -LSE (base 2) and -D
     const float *brow_dq = nullptr;
     if (MODE == kDq && orow_ok) {
       const size_t gi = (size_t)head_outer * p.total_q + sq.q0 + orow;
       const float L = p.lse[gi];
-      row_lse2 = L == -INFINITY ? INFINITY : L * kLog2e;
-      row_d = p.rowdot[gi];
+      row_nl = L == -INFINITY ? -INFINITY : -L * kLog2e;
+      row_nd = -p.rowdot[gi];
       if (p.bias) {
         const int bh = p.bias_heads == 1 ? 0 : head_outer;
         brow_dq = p.bias + ((size_t)(sq.q0 + orow) * p.bias_heads + bh) * (size_t)p.max_kv;
@@ -282,73 +326,65 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     }
     bool ok = true;
     for (int n = 0; n < n_items; ++n) {
-      const int b = n % NBUF;
+      const int b = n % NBUF, st = n % NSTAGE;
       const int h = item_head(n);
-      const int i0 = item_row(n);  // first inner row of the item
-      float *lsb = ldbuf + quarter * 128;
-      if (MODE == kDkdv) {
-        // LSE (base 2; +inf for rows that see nothing or lie past the sequence) and D of the
-        // item's 64 query columns; each warp keeps its own copy (warp-local sync only)
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int qi = i0 + lane + 32 * u;
-          float L2 = INFINITY, Dv = 0.f;
-          if (qi < sq.q_len) {
-            const size_t gi = (size_t)h * p.total_q + sq.q0 + qi;
-            const float L = p.lse[gi];
-            L2 = L == -INFINITY ? INFINITY : L * kLog2e;
-            Dv = p.rowdot[gi];
-          }
-          lsb[lane + 32 * u] = L2;
-          lsb[64 + lane + 32 * u] = Dv;
-        }
-        __syncwarp();
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_S + b), (n / NBUF) & 1, abort_flag, p.err));
+      const int i0 = item_row(n) + col0;  // first inner row of this thread's 32 columns
+      bool w = mbar_wait(bar(C::B_S + b), (n / NBUF) & 1, abort_flag, p.err);
+      // the LSE / D pairs were written by the producer lanes before their arrive on in_full:
+      // acquire that barrier too before reading them
+      if (MODE == kDkdv && w) w = mbar_wait(bar(C::B_IF + st), (n / NSTAGE) & 1, abort_flag, p.err);
+      ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       fence_after();
-      const uint32_t s_addr = lane_addr + C::BUF + 128 * b, dp_addr = s_addr + 64;
+      const uint32_t s_addr = lane_addr + C::BUF + 128 * b + col0, dp_addr = s_addr + 64;
+      uint32_t sv[32], dv[32];
+      __syncwarp();
+      tmem_ld32(s_addr, sv);
+      tmem_ld32(dp_addr, dv);
       const float *brow = brow_dq;
       if (MODE == kDkdv && p.bias && orow_ok) {
         const int bh = p.bias_heads == 1 ? 0 : h;
         brow = p.bias + (size_t)bh * p.max_kv + orow;  // + (q0 + i) * bias_heads * max_kv per column
       }
-      // is every element of this thread's row of the item visible (no per-element mask)?
+      // is every element of this thread's 32 columns visible (no per-element mask)?
       bool plain;
       if (MODE == kDkdv) {
-        const int j = orow, ilast = i0 + 63;
+        const int j = orow, ilast = i0 + 31;
         plain = orow_ok && ilast < sq.q_len && (!p.causal || j <= i0 + off) &&
                 (p.window <= 0 || j >= ilast + off - p.window + 1);
       } else {
-        const int i = orow, jlast = i0 + 63;
+        const int i = orow, jlast = i0 + 31;
         plain = orow_ok && jlast < sq.kv_len && (!p.causal || jlast <= i + off) &&
                 (p.window <= 0 || i0 >= i + off - p.window + 1);
       }
       plain = plain && p.bias == nullptr;
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sv[32], dv[32];
-        __syncwarp();
-        tmem_ld32(s_addr + ch * 32, sv);
-        tmem_ld32(dp_addr + ch * 32, dv);
-        tmem_ld_wait();
-        float pr[32], ds[32];
+      const float4 *lp = ldbuf + st * 32 + 16 * half;  // this half's 16 column pairs (dK/dV)
+      tmem_ld_wait();
+      uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = ch * 32 + e;
-          float lse2, dcol;
-          if (MODE == kDkdv) { lse2 = lsb[col]; dcol = lsb[64 + col]; }
-          else { lse2 = row_lse2; dcol = row_d; }
-          float x;
-          if (plain) {
-            x = __uint_as_float(sv[e]) * sl2;
-          } else {
-            const int i = MODE == kDkdv ? i0 + col : orow;
-            const int j = MODE == kDkdv ? orow : i0 + col;
-            x = -INFINITY;
+      for (int e = 0; e < 16; ++e) {
+        const int c = 2 * e;
+        uint64_t nl2, nd2;
+        if (MODE == kDkdv) {
+          const float4 q4 = lp[e];
+          nl2 = f2pack(q4.x, q4.y);
+          nd2 = f2pack(q4.z, q4.w);
+        } else {
+          nl2 = f2pack(row_nl, row_nl);
+          nd2 = f2pack(row_nd, row_nd);
+        }
+        uint64_t x2;
+        if (plain) {
+          x2 = fma2(f2pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nl2);
+        } else {
+          float xs[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int i = MODE == kDkdv ? i0 + c + u : orow;
+            const int j = MODE == kDkdv ? orow : i0 + c + u;
+            float x = -INFINITY;
             if (orow_ok && i < sq.q_len && pair_visible(i, j, off, sq.kv_len, p.causal, p.window)) {
-              x = __uint_as_float(sv[e]) * sl2;
+              x = __uint_as_float(sv[c + u]) * sl2;
               if (brow) {
                 const float bv = MODE == kDkdv
                                      ? __ldg(brow + (size_t)(sq.q0 + i) * p.bias_heads * (size_t)p.max_kv)
@@ -356,65 +392,68 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
                 x = fmaf(bv, kLog2e, x);
               }
             }
+            xs[u] = x;
           }
-          pr[e] = ex2(x - lse2);  // masked (-inf) or dead row (lse2 = +inf) -> 0
-          ds[e] = pr[e] * (__uint_as_float(dv[e]) - dcol);
+          x2 = add2(f2pack(xs[0], xs[1]), nl2);
         }
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          pk[e] = pack2(pr[2 * e], pr[2 * e + 1], is_bf16);
-          dk[e] = pack2(ds[2 * e], ds[2 * e + 1], is_bf16);
-        }
-        __syncwarp();
-        if (MODE == kDkdv) tmem_st16(s_addr + ch * 16, pk);
-        tmem_st16(dp_addr + ch * 16, dk);
+        // P = 2^(logit2 - LSE2): masked logits (-inf) and rows without keys (-LSE2 = -inf) give 0
+        const float2 x = f2unpack(x2);
+        const float pa = ex2(x.x), pb = ex2(x.y);
+        const uint64_t p2 = f2pack(pa, pb);
+        const uint64_t t2 = add2(f2pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), nd2);
+        const float2 ds = f2unpack(mul2(p2, t2));  // dS = P o (dP - D)
+        pk[e] = pack2(pa, pb, is_bf16);
+        dk[e] = pack2(ds.x, ds.y, is_bf16);
       }
       __syncwarp();
+      if (MODE == kDkdv) tmem_st16(s_addr, pk);
+      tmem_st16(dp_addr, dk);
       tmem_st_wait();
       fence_before();
       mbar_arrive(bar(C::B_P + b));
     }
-    // epilogue
+    // epilogue: the last item's accumulations complete every MMA of the CTA
     if (ok && n_items > 0)
       ok = mbar_wait(bar(C::B_D + (n_items - 1) % NBUF), ((n_items - 1) / NBUF) & 1, abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       fence_after();
-      auto store_acc = [&](uint32_t col, int width, void *dst_base, int heads, int head, float mul) {
+      // columns [c0, c0 + ncols) of an accumulator (row width `width` in the output) -> dtype
+      auto store_acc = [&](uint32_t tcol, int c0, int ncols, int width, void *dst_base, int heads,
+                           int head, float mul) {
         uint4 *dst = nullptr;
         if (orow_ok) {
           const size_t g = (size_t)((MODE == kDkdv ? sq.k0 : sq.q0) + orow);
           dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(dst_base) +
-                                          ((g * heads + head) * (size_t)width) * 2);
+                                          ((g * heads + head) * (size_t)width + c0) * 2);
         }
 #pragma unroll 1
-        for (int ch = 0; ch < width / 32; ++ch) {
+        for (int ch = 0; ch < ncols / 32; ++ch) {
           uint32_t v[32];
           if (n_items > 0) {
             __syncwarp();
-            tmem_ld32(lane_addr + col + ch * 32, v);
+            tmem_ld32(lane_addr + tcol + c0 + ch * 32, v);
             tmem_ld_wait();
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = 0u;
           }
-          uint32_t pk[16];
+          uint32_t o16[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul, is_bf16);
+            o16[e] = pack2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul, is_bf16);
           if (dst) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
-              dst[ch * 4 + q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+              dst[ch * 4 + q4] = make_uint4(o16[4 * q4], o16[4 * q4 + 1], o16[4 * q4 + 2], o16[4 * q4 + 3]);
           }
         }
       };
       if (MODE == kDkdv) {
-        store_acc(C::ACC0, DV, p.dv, p.h_kv, hk, 1.f);
-        store_acc(C::ACC1, DQK, p.dk, p.h_kv, hk, p.scale);
+        if (half == 0) store_acc(C::ACC0, 0, DV, DV, p.dv, p.h_kv, hk, 1.f);
+        else store_acc(C::ACC1, 0, DQK, DQK, p.dk, p.h_kv, hk, p.scale);
       } else {
-        store_acc(C::ACC0, DQK, p.dq, p.h_q, head_outer, p.scale);
+        store_acc(C::ACC0, half * (DQK / 2), DQK / 2, DQK, p.dq, p.h_q, head_outer, p.scale);
       }
     }
   }
@@ -452,7 +491,7 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   auto kern = tc_bwd_kernel<MODE, DQK, DV, NBUF, NSTAGE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 192, C::SMEM, st>>>(m, p);
+  kern<<<grid, 320, C::SMEM, st>>>(m, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
