@@ -220,7 +220,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_items > 0) {
+    // the whole warp runs the issue loop (uniform operands); elect.sync picks the issuing lane
+    if (n_items > 0) {
       // S / dP: M = 128 outer rows, N = 64 inner rows, both operands K-major
       const uint32_t id_sp = idesc_f16(is_bf16, 128, 64, 0, 0);
       // accumulations: A from TMEM (K = 64 inner rows), B = inner tile MN-major
@@ -237,14 +238,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss(s_col, d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
+          mma_ss_w(s_col, d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss(dp_col, d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
+          mma_ss_w(dp_col, d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
         }
-        mma_commit(bar(C::B_S + b));
+        mma_commit_w(bar(C::B_S + b));
       };
       // the 16-bit A operand of K step kk (16 inner rows): warpgroup kk / 2 wrote it over the first
       // half of its own 32 columns
@@ -258,47 +259,47 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           // dV += P^T dO   (dO MN-major: 64-column blocks 8 KB apart, 16 rows per K step)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::ACC0, s_col + a_col(kk), d_i1 + (uint64_t)((kk * 2048) >> 4), id_a0,
+            mma_ts_w(tmem + C::ACC0, s_col + a_col(kk), d_i1 + (uint64_t)((kk * 2048) >> 4), id_a0,
                    (n > 0 || kk > 0) ? 1u : 0u);
           // dK += dS^T Q
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::ACC1, dp_col + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id_a1,
+            mma_ts_w(tmem + C::ACC1, dp_col + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id_a1,
                    (n > 0 || kk > 0) ? 1u : 0u);
         } else {
           // dQ += dS K   (K tile MN-major)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::ACC0, dp_col + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id_a0,
+            mma_ts_w(tmem + C::ACC0, dp_col + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id_a0,
                    (n > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(C::B_D + b));
-        mma_commit(bar(C::B_IE + st));
+        mma_commit_w(bar(C::B_D + b));
+        mma_commit_w(bar(C::B_IE + st));
       };
-      bool ok = mbar_wait(bar(C::B_OUT), 0, abort_flag, p.err);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_OUT), 0, abort_flag, p.err));
       for (int n = 0; n < NBUF && n < n_items && ok; ++n) {
-        ok = mbar_wait(bar(C::B_IF + n % NSTAGE), (n / NSTAGE) & 1, abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_IF + n % NSTAGE), (n / NSTAGE) & 1, abort_flag, p.err));
         if (!ok) break;
         fence_after();
         issue_sp(n);
       }
       for (int n = 0; n < n_items && ok; ++n) {
         const int b = n % NBUF;
-        ok = mbar_wait(bar(C::B_P + b), (n / NBUF) & 1, abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_P + b), (n / NBUF) & 1, abort_flag, p.err));
         if (!ok) break;
         fence_after();
         issue_acc(n);
         const int m = n + NBUF;
         if (m < n_items) {
           // the products of item m reuse buffer b: wait until item n's accumulations read it
-          ok = mbar_wait(bar(C::B_D + b), (n / NBUF) & 1, abort_flag, p.err) &&
-               mbar_wait(bar(C::B_IF + m % NSTAGE), (m / NSTAGE) & 1, abort_flag, p.err);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_D + b), (n / NBUF) & 1, abort_flag, p.err) &&
+               mbar_wait(bar(C::B_IF + m % NSTAGE), (m / NSTAGE) & 1, abort_flag, p.err));
           if (!ok) break;
           fence_after();
           issue_sp(m);
         }
       }
-      mma_commit(bar(C::B_DRAIN));
+      mma_commit_w(bar(C::B_DRAIN));
       drain_wait(bar(C::B_DRAIN), 0);
     }
   } else {

@@ -197,49 +197,51 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && hi > lo) {
+    // the whole warp runs the issue loop (uniform operands); elect.sync picks the issuing lane
+    if (hi > lo) {
       const uint32_t id_s = idesc_f16(is_bf16, 128, 128, 0, 0);  // S = Q K^T, both K-major
       const uint32_t id_o = idesc_f16(is_bf16, 128, DV, 0, 1);   // O += P V, V MN-major
       int pv_count[2] = {0, 0}, p_count[2] = {0, 0};
       auto part = [&](int t, int j) { return j >= ti.jlo[t] && j < ti.jhi[t]; };
       auto issue_s = [&](int t, int j) {
         const uint32_t ks = (uint32_t)((j - lo) % NK);
-        const uint32_t qa = sQ + t * C::Q_BYTES, ka = sK + ks * C::K_BYTES;
+        const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
+        const uint64_t dk = sdesc_sw128(sK + ks * C::K_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
-          mma_ss(tmem + 128 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 id_s, kk > 0);
+          // a K step adds its byte offset / 16 to the descriptor's start-address field
+          const uint64_t off = (uint64_t)(((kk >> 2) * C::BLK + (kk & 3) * 32) >> 4);
+          mma_ss_w(tmem + 128 * t, dq + off, dk + off, id_s, kk > 0);
         }
-        mma_commit(bar(C::B_S + t));
+        mma_commit_w(bar(C::B_S + t));
       };
       auto issue_pv = [&](int t, int j) {
         const uint32_t vs = (uint32_t)((j - lo) % NV);
-        const uint32_t va = sV + vs * C::V_BYTES;
+        const uint64_t dv = sdesc_sw128(sV + vs * C::V_BYTES, C::BLK, 1024);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)
-          mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8,
-                 sdesc_sw128(va + kk * 2048, C::BLK, 1024), id_o, (j > ti.jlo[t] || kk > 0) ? 1u : 0u);
-        mma_commit(bar(C::B_O + t));
+          mma_ts_w(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, dv + (uint64_t)((kk * 2048) >> 4),
+                   id_o, (j > ti.jlo[t] || kk > 0) ? 1u : 0u);
+        mma_commit_w(bar(C::B_O + t));
         ++pv_count[t];
       };
-      bool ok = mbar_wait(bar(C::B_Q), 0, abort_flag, p.err) &&
-                mbar_wait(bar(C::B_KF + 0), 0, abort_flag, p.err);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_Q), 0, abort_flag, p.err) &&
+                mbar_wait(bar(C::B_KF + 0), 0, abort_flag, p.err));
       if (ok) {
         fence_after();
         for (int t = 0; t < 2; ++t)
           if (part(t, lo)) issue_s(t, lo);
-        mma_commit(bar(C::B_KE + 0));
+        mma_commit_w(bar(C::B_KE + 0));
       }
       for (int j = lo; j < hi && ok; ++j) {
         const int it = j - lo;
-        ok = mbar_wait(bar(C::B_VF + it % NV), (it / NV) & 1, abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_VF + it % NV), (it / NV) & 1, abort_flag, p.err));
         if (!ok) break;
         fence_after();
         bool k_next = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (part(t, j)) {
-            ok = mbar_wait(bar(C::B_P + t), p_count[t] & 1, abort_flag, p.err);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_P + t), p_count[t] & 1, abort_flag, p.err));
             if (!ok) break;
             ++p_count[t];
             fence_after();
@@ -247,23 +249,23 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           }
           if (j + 1 < hi && part(t, j + 1)) {
             if (!k_next) {
-              ok = mbar_wait(bar(C::B_KF + (it + 1) % NK), ((it + 1) / NK) & 1, abort_flag, p.err);
+              ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KF + (it + 1) % NK), ((it + 1) / NK) & 1, abort_flag, p.err));
               if (!ok) break;
               k_next = true;
             }
             // S_t(j+1) overwrites the TMEM columns P_t(j) was read from: wait for that P.V
-            if (part(t, j)) ok = mbar_wait(bar(C::B_O + t), (pv_count[t] - 1) & 1, abort_flag, p.err);
+            if (part(t, j)) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_O + t), (pv_count[t] - 1) & 1, abort_flag, p.err));
             if (!ok) break;
             fence_after();
             issue_s(t, j + 1);
           }
         }
         if (!ok) break;
-        mma_commit(bar(C::B_VE + it % NV));
-        if (j + 1 < hi) mma_commit(bar(C::B_KE + (it + 1) % NK));
+        mma_commit_w(bar(C::B_VE + it % NV));
+        if (j + 1 < hi) mma_commit_w(bar(C::B_KE + (it + 1) % NK));
       }
       // drain: every MMA this thread issued has completed before TMEM is released
-      mma_commit(bar(C::B_DRAIN));
+      mma_commit_w(bar(C::B_DRAIN));
       drain_wait(bar(C::B_DRAIN), 0);
     }
   } else {
