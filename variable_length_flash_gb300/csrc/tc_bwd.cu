@@ -310,7 +310,6 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     const int r = 32 * quarter + lane;  // TMEM lane = outer row (key for dK/dV, query for dQ)
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     const float sl2 = p.scale_log2;
-    const uint64_t sl2x2 = f2pack(sl2, sl2);
     const int orow = tile0 + r;  // this thread's outer row
     const bool orow_ok = MODE == kDkdv ? orow < sq.kv_len : orow < sq.q_len;
     float row_nl = -INFINITY, row_nd = 0.f;  // dQ: this row's -LSE (base 2) and -D
@@ -362,22 +361,27 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       const float4 *lp = ldbuf + st * 32 + 16 * half;  // this half's 16 column pairs (dK/dV)
       tmem_ld_wait();
       uint32_t pk[16], dk[16];
+      if (plain) {
+        // every pair visible, no bias: P = 2^(S log2e scale - LSE2), dS = P (dP - D)
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int c = 2 * e;
-        uint64_t nl2, nd2;
-        if (MODE == kDkdv) {
-          const float4 q4 = lp[e];
-          nl2 = f2pack(q4.x, q4.y);
-          nd2 = f2pack(q4.z, q4.w);
-        } else {
-          nl2 = f2pack(row_nl, row_nl);
-          nd2 = f2pack(row_nd, row_nd);
+        for (int e = 0; e < 16; ++e) {
+          const int c = 2 * e;
+          float4 q4;
+          if (MODE == kDkdv) q4 = lp[e];
+          else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
+          const float pa = ex2(fmaf(__uint_as_float(sv[c]), sl2, q4.x));
+          const float pb = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, q4.y));
+          const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
+          pk[e] = pack2(pa, pb, is_bf16);
+          dk[e] = pack2(pa * ta, pb * tb, is_bf16);
         }
-        uint64_t x2;
-        if (plain) {
-          x2 = fma2(f2pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nl2);
-        } else {
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = 2 * e;
+          float4 q4;
+          if (MODE == kDkdv) q4 = lp[e];
+          else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
           float xs[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
@@ -395,16 +399,12 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             }
             xs[u] = x;
           }
-          x2 = add2(f2pack(xs[0], xs[1]), nl2);
+          // masked logits (-inf) and rows without keys (-LSE2 = -inf) give P = 0
+          const float pa = ex2(xs[0] + q4.x), pb = ex2(xs[1] + q4.y);
+          const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
+          pk[e] = pack2(pa, pb, is_bf16);
+          dk[e] = pack2(pa * ta, pb * tb, is_bf16);
         }
-        // P = 2^(logit2 - LSE2): masked logits (-inf) and rows without keys (-LSE2 = -inf) give 0
-        const float2 x = f2unpack(x2);
-        const float pa = ex2(x.x), pb = ex2(x.y);
-        const uint64_t p2 = f2pack(pa, pb);
-        const uint64_t t2 = add2(f2pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), nd2);
-        const float2 ds = f2unpack(mul2(p2, t2));  // dS = P o (dP - D)
-        pk[e] = pack2(pa, pb, is_bf16);
-        dk[e] = pack2(ds.x, ds.y, is_bf16);
       }
       __syncwarp();
       if (MODE == kDkdv) tmem_st16(s_addr, pk);

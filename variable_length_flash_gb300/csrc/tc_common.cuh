@@ -51,11 +51,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with parity `parity` of barrier `bar` to complete.  Bounded: gives up after
-// kTimeoutNs (recording VLF_ERR_TIMEOUT) or as soon as another role of the CTA has given up.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       int *err) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait (out of line: most waits find the phase already complete).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int *abort_flag, int *err) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -68,6 +66,14 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
       }
     }
   }
+}
+
+// Wait for the phase with parity `parity` of barrier `bar` to complete.  Bounded: gives up after
+// kTimeoutNs (recording VLF_ERR_TIMEOUT) or as soon as another role of the CTA has given up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err);
 }
 
 // ---------------------------------------------------------------- TMA
