@@ -6,19 +6,29 @@
 //
 // One kernel body serves both (MODE):
 //   dK/dV: a CTA owns 128 keys of one kv head (K, V tiles stay in shared memory) and walks the
-//          64-row Q / dO tiles of every query head of its GQA group that can see those keys.
-//          S^T = K Q^T and dP^T = V dO^T land in TMEM (lanes = keys); the compute warpgroup
-//          turns them into 16-bit P^T and dS^T in TMEM; dV += P^T dO and dK += dS^T Q take
-//          their A operand from TMEM.  LSE and D of the 64 query columns come through smem.
+//          IR-row Q / dO tiles ("items") of every query head of its GQA group that can see those
+//          keys.  S^T = K Q^T and dP^T = V dO^T land in TMEM (lanes = keys); the compute warps
+//          turn them into 16-bit P^T and dS^T in TMEM; dV += P^T dO and dK += dS^T Q take their A
+//          operand from TMEM.  LSE and D of the item's query columns come through smem.
 //   dQ:    a CTA owns 128 query rows of one head (Q, dO stay in shared memory) and walks the
-//          64-key K / V tiles of its band: S = Q K^T, dP = dO V^T, dS in TMEM, dQ += dS K.
+//          IR-key K / V items of its band: S = Q K^T, dP = dO V^T, dS in TMEM, dQ += dS K.
+// Item width IR: an MMA of 128 x N x 16 with both operands in shared memory runs at full rate
+// only for N >= 128 (at N = 64 it is limited by shared-memory bandwidth), but 128-row items
+// leave TMEM room for one S/dP buffer only.  The dQ kernel (three products per item) uses
+// 128-row items for head widths 64 and 128; the dK/dV kernel (four products) keeps 64-row items
+// with two S/dP buffers so the next item's products overlap this item's elementwise pass; the
+// latent head (QK width 192) uses 64-row items in both.
 // Warp roles (320 threads): warp 0 stages tiles with TMA and, with all its lanes, the item's LSE
-// and D columns into the same shared-memory stage; warp 1 allocates TMEM and issues the MMAs;
-// warps 2-9 are two compute warpgroups, each owning 32 of the item's 64 columns (one thread per
-// TMEM lane, so every row has two threads).  Each warpgroup writes its 16-bit P / dS over its own
-// S / dP columns.  S/dP buffers are double-buffered in TMEM where columns allow so the next
-// tile's products overlap this tile's elementwise pass.  Tiles outside the causal / window band
-// are skipped (they contribute exact zeros).  Every wait is bounded.
+// and D columns into the same shared-memory stage; warp 1 allocates TMEM and issues the MMAs
+// from the whole converged warp (elect.sync picks the issuing lane); warps 2-9 are two compute
+// warpgroups, each owning half of the item's columns (one thread per TMEM lane).  Each warpgroup
+// writes its 16-bit P / dS over its own S / dP columns.
+// MMA order with one S/dP buffer: after item n's P / dS are ready the accumulations of n are
+// queued; S(n+1) is issued as soon as the accumulation that reads the S columns has completed
+// (it then queues behind the other accumulation), dP(n+1) once the dP columns are released.
+// With two buffers item n+2's products follow the completion of item n's accumulations.
+// Tiles outside the causal / window band are skipped (they contribute exact zeros).  Every wait
+// is bounded.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -43,32 +53,38 @@ struct BwdMaps {
 };
 
 // outer0/outer1: K, V (dK/dV) or Q, dO (dQ), 128 rows.  inner0/inner1: Q, dO (dK/dV) or K, V
-// (dQ), 64 rows per item.
-template <int MODE, int DQK, int DV, int NBUF, int NSTAGE>
+// (dQ), IR rows per item.
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE>
 struct BwdCfg {
   static constexpr int KB0 = DQK / 64, KB1 = DV / 64;  // 64-col blocks of tensors 0 / 1
-  static constexpr int OBLK = 128 * 128, IBLK = 64 * 128;  // bytes per 64-col block
+  static constexpr int OBLK = 128 * 128, IBLK = IR * 128;  // bytes per 64-col block
   static constexpr int O0_BYTES = KB0 * OBLK, O1_BYTES = KB1 * OBLK;
   static constexpr int I0_BYTES = KB0 * IBLK, I1_BYTES = KB1 * IBLK;
   static constexpr int STAGE_BYTES = I0_BYTES + I1_BYTES;
   static constexpr int OFF_O0 = 0, OFF_O1 = O0_BYTES, OFF_IN = O0_BYTES + O1_BYTES;
-  // per stage: the item's 64 columns as 32 pairs {-LSE2_c, -LSE2_c+1, -D_c, -D_c+1} (dK/dV)
+  // per stage: the item's IR columns as IR/2 pairs {-LSE2_c, -LSE2_c+1, -D_c, -D_c+1} (dK/dV)
+  static constexpr int PAIRS = IR / 2;
   static constexpr int OFF_LD = OFF_IN + NSTAGE * STAGE_BYTES;
-  static constexpr int OFF_BAR = OFF_LD + NSTAGE * 128 * 4;
+  static constexpr int OFF_BAR = OFF_LD + NSTAGE * PAIRS * 16;
   // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE], s_full[NBUF], p_ready[NBUF],
-  // item_done[NBUF], drain
+  // acc0_done (dV; single buffer only), acc_done[NBUF] (dK or dQ: the item's last accumulation),
+  // drain
   static constexpr int B_OUT = 0, B_IF = 1, B_IE = B_IF + NSTAGE, B_S = B_IE + NSTAGE;
-  static constexpr int B_P = B_S + NBUF, B_D = B_P + NBUF, B_DRAIN = B_D + NBUF;
+  static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + 1, B_DRAIN = B_D + NBUF;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
-  // TMEM: accumulators first, then NBUF x (S 64 cols, dP 64 cols)
-  static constexpr uint32_t ACC0 = 0;                           // dV (dK/dV) or dQ (dQ)
-  static constexpr uint32_t ACC1 = 128;                         // dK (dK/dV)
+  // TMEM: accumulators first, then NBUF x (S IR cols, dP IR cols)
+  static constexpr uint32_t ACC0 = 0;    // dV (dK/dV) or dQ (dQ)
+  static constexpr uint32_t ACC1 = 128;  // dK (dK/dV)
   static constexpr uint32_t BUF = MODE == kDkdv ? 128 + DQK : 256;
-  static_assert(BUF + NBUF * 128 <= 512, "TMEM columns");
+  static constexpr int HALF = IR / 2;      // columns per compute warpgroup
+  static constexpr int CHUNKS = HALF / 32;  // 32-column chunks per compute thread
+  static_assert(BUF + NBUF * 2 * IR <= 512, "TMEM columns");
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(DV <= 128 && DQK <= 256 && DQK % 64 == 0 && DV % 64 == 0, "head widths");
+  static_assert(IR == 64 || IR == 128, "item rows");
+  static_assert(NBUF == 1 || IR == 64, "double buffering only with 64-row items");
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -78,17 +94,17 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int MODE, int DQK, int DV, int NBUF, int NSTAGE>
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE>
 __global__ void __launch_bounds__(320, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
-  using C = BwdCfg<MODE, DQK, DV, NBUF, NSTAGE>;
+  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE>;
   extern __shared__ uint8_t smem_raw[];
   const int s = blockIdx.z;
   Seq sq;
   if (!load_seq(p, s, sq)) return;
   const int off = sq.kv_len - sq.q_len;
-  // the CTA's outer tile and its item range
-  int tile0, head_outer, hk, n_items, lo64 = 0, nq_tiles = 0;
+  // the CTA's outer tile and its item range (items start at multiples of IR)
+  int tile0, head_outer, hk, n_items, lo = 0, nq_tiles = 0;
   if (MODE == kDkdv) {
     tile0 = blockIdx.x * 128;  // first key
     hk = blockIdx.y;
@@ -99,8 +115,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       q_band(tile0, min(tile0 + 128, sq.kv_len), sq.q_len, sq.kv_len, p.causal, p.window, qlo, qhi);
       if (p.flags & VLF_FLAG_NO_SKIP) { qlo = 0; qhi = sq.q_len; }
     }
-    lo64 = (qlo / 64) * 64;
-    nq_tiles = qhi > qlo ? (qhi - lo64 + 63) / 64 : 0;
+    lo = (qlo / IR) * IR;
+    nq_tiles = qhi > qlo ? (qhi - lo + IR - 1) / IR : 0;
     n_items = nq_tiles * p.group;
   } else {
     const int bx = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
@@ -113,15 +129,15 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       kv_band(tile0, min(tile0 + 128, sq.q_len), sq.q_len, sq.kv_len, p.causal, p.window, klo, khi);
       if (p.flags & VLF_FLAG_NO_SKIP) { klo = 0; khi = sq.kv_len; }
     }
-    lo64 = (klo / 64) * 64;
-    n_items = khi > klo ? (khi - lo64 + 63) / 64 : 0;
+    lo = (klo / IR) * IR;
+    n_items = khi > klo ? (khi - lo + IR - 1) / IR : 0;
   }
 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
   const uint32_t sO0 = base + C::OFF_O0, sO1 = base + C::OFF_O1, sIn = base + C::OFF_IN;
-  float4 *ldbuf = reinterpret_cast<float4 *>(gbase + C::OFF_LD);  // [stage][32 column pairs]
+  float4 *ldbuf = reinterpret_cast<float4 *>(gbase + C::OFF_LD);  // [stage][IR/2 column pairs]
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
@@ -130,13 +146,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_OUT), 1);
     // in_full: the TMA bytes plus 33 arrivals (lane 0's expect_tx and every producer lane after
-    // writing its LSE / D pair); p_ready: all 256 compute threads
+    // writing its LSE / D pairs); p_ready: all 256 compute threads
     for (int i = 0; i < NSTAGE; ++i) { mbar_init(bar(C::B_IF + i), 33); mbar_init(bar(C::B_IE + i), 1); }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(bar(C::B_S + b), 1);
       mbar_init(bar(C::B_P + b), 256);
       mbar_init(bar(C::B_D + b), 1);
     }
+    mbar_init(bar(C::B_D0), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     mbar_init_fence();
@@ -153,7 +170,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 
   // item n -> (query head, first inner row) ; inner rows are queries (dK/dV) or keys (dQ)
   auto item_head = [&](int n) { return MODE == kDkdv ? hk * p.group + n / nq_tiles : head_outer; };
-  auto item_row = [&](int n) { return MODE == kDkdv ? lo64 + (n % nq_tiles) * 64 : lo64 + n * 64; };
+  auto item_row = [&](int n) { return MODE == kDkdv ? lo + (n % nq_tiles) * IR : lo + n * IR; };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -181,22 +198,25 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         }
         if (MODE == kDkdv) {
           // -LSE (base 2; -inf for rows that see nothing or lie past the sequence, so P = 0) and
-          // -D of the item's columns 2 lane and 2 lane + 1
+          // -D of the item's column pairs lane, lane + 32, ...
           const int h = item_head(n), i0 = item_row(n);
-          float nl[2], nd[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qi = i0 + 2 * lane + u;
-            nl[u] = -INFINITY;
-            nd[u] = 0.f;
-            if (qi < sq.q_len) {
-              const size_t gi = (size_t)h * p.total_q + sq.q0 + qi;
-              const float L = p.lse[gi];
-              nl[u] = L == -INFINITY ? -INFINITY : -L * kLog2e;
-              nd[u] = -p.rowdot[gi];
+          for (int pp = 0; pp < C::PAIRS / 32; ++pp) {
+            float nl[2], nd[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int qi = i0 + 2 * (lane + 32 * pp) + u;
+              nl[u] = -INFINITY;
+              nd[u] = 0.f;
+              if (qi < sq.q_len) {
+                const size_t gi = (size_t)h * p.total_q + sq.q0 + qi;
+                const float L = p.lse[gi];
+                nl[u] = L == -INFINITY ? -INFINITY : -L * kLog2e;
+                nd[u] = -p.rowdot[gi];
+              }
             }
+            ldbuf[st * C::PAIRS + lane + 32 * pp] = make_float4(nl[0], nl[1], nd[0], nd[1]);
           }
-          ldbuf[st * 32 + lane] = make_float4(nl[0], nl[1], nd[0], nd[1]);
         }
         if (lane == 0) {
           const int ih = MODE == kDkdv ? item_head(n) : hk;  // head inside the inner tensors
@@ -220,92 +240,108 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // the whole warp runs the issue loop (uniform operands); elect.sync picks the issuing lane
     if (n_items > 0) {
-      // S / dP: M = 128 outer rows, N = 64 inner rows, both operands K-major
-      const uint32_t id_sp = idesc_f16(is_bf16, 128, 64, 0, 0);
-      // accumulations: A from TMEM (K = 64 inner rows), B = inner tile MN-major
+      // S / dP: M = 128 outer rows, N = IR inner rows, both operands K-major
+      const uint32_t id_sp = idesc_f16(is_bf16, 128, IR, 0, 0);
+      // accumulations: A from TMEM (K = IR inner rows), B = inner tile MN-major
       const uint32_t id_a0 = idesc_f16(is_bf16, 128, MODE == kDkdv ? DV : DQK, 0, 1);
       const uint32_t id_a1 = idesc_f16(is_bf16, 128, DQK, 0, 1);
       // descriptors are built once; a K step adds its byte offset / 16 to the start-address
       // field (shared addresses stay far below the field's 2^18-byte range, so nothing carries)
       const uint64_t d_o0 = sdesc_sw128(sO0, 16, 1024), d_o1 = sdesc_sw128(sO1, 16, 1024);
-      auto issue_sp = [&](int n) {
-        const int b = n % NBUF, st = n % NSTAGE;
-        const uint32_t in0 = sIn + st * C::STAGE_BYTES, in1 = in0 + C::I0_BYTES;
-        const uint64_t d_i0 = sdesc_sw128(in0, 16, 1024), d_i1 = sdesc_sw128(in1, 16, 1024);
-        const uint32_t s_col = tmem + C::BUF + 128 * b, dp_col = s_col + 64;
+      auto s_cols = [&](int n) { return tmem + C::BUF + 2 * IR * (n % NBUF); };
+      auto issue_s = [&](int n) {  // S (dK/dV: S^T) of item n
+        const uint64_t d_i0 = sdesc_sw128(sIn + (n % NSTAGE) * C::STAGE_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss_w(s_col, d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
+          mma_ss_w(s_cols(n), d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
         }
+      };
+      auto issue_dp = [&](int n) {  // dP (dK/dV: dP^T) of item n
+        const uint64_t d_i1 = sdesc_sw128(sIn + (n % NSTAGE) * C::STAGE_BYTES + C::I0_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss_w(dp_col, d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
+          mma_ss_w(s_cols(n) + IR, d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
         }
-        mma_commit_w(bar(C::B_S + b));
       };
-      // the 16-bit A operand of K step kk (16 inner rows): warpgroup kk / 2 wrote it over the first
-      // half of its own 32 columns
+      // the 16-bit A operand of K step kk (16 inner rows) sits in the first half of the 32-column
+      // chunk its compute thread loaded: column 32 * (kk / 2) + 8 * (kk % 2)
       auto a_col = [](int kk) { return (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1)); };
-      auto issue_acc = [&](int n) {
-        const int b = n % NBUF, st = n % NSTAGE;
-        const uint32_t in0 = sIn + st * C::STAGE_BYTES, in1 = in0 + C::I0_BYTES;
-        const uint32_t s_col = tmem + C::BUF + 128 * b, dp_col = s_col + 64;
-        const uint64_t d_i0 = sdesc_sw128(in0, C::IBLK, 1024), d_i1 = sdesc_sw128(in1, C::IBLK, 1024);
-        if (MODE == kDkdv) {
-          // dV += P^T dO   (dO MN-major: 64-column blocks 8 KB apart, 16 rows per K step)
+      // accumulation 0 (dV += P^T dO) -- dK/dV only
+      auto issue_acc0 = [&](int n) {
+        const uint64_t d_i1 = sdesc_sw128(sIn + (n % NSTAGE) * C::STAGE_BYTES + C::I0_BYTES, C::IBLK, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts_w(tmem + C::ACC0, s_col + a_col(kk), d_i1 + (uint64_t)((kk * 2048) >> 4), id_a0,
+        for (int kk = 0; kk < IR / 16; ++kk)
+          mma_ts_w(tmem + C::ACC0, s_cols(n) + a_col(kk), d_i1 + (uint64_t)((kk * 2048) >> 4), id_a0,
                    (n > 0 || kk > 0) ? 1u : 0u);
-          // dK += dS^T Q
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts_w(tmem + C::ACC1, dp_col + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id_a1,
-                   (n > 0 || kk > 0) ? 1u : 0u);
-        } else {
-          // dQ += dS K   (K tile MN-major)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts_w(tmem + C::ACC0, dp_col + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id_a0,
-                   (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit_w(bar(C::B_D + b));
-        mma_commit_w(bar(C::B_IE + st));
       };
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_OUT), 0, abort_flag, p.err));
+      // last accumulation: dK += dS^T Q (dK/dV) or dQ += dS K (dQ)
+      auto issue_acc1 = [&](int n) {
+        const uint64_t d_i0 = sdesc_sw128(sIn + (n % NSTAGE) * C::STAGE_BYTES, C::IBLK, 1024);
+        const uint32_t acc = MODE == kDkdv ? C::ACC1 : C::ACC0;
+        const uint32_t id = MODE == kDkdv ? id_a1 : id_a0;
+#pragma unroll
+        for (int kk = 0; kk < IR / 16; ++kk)
+          mma_ts_w(tmem + acc, s_cols(n) + IR + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+      };
+      auto wait_all = [&](int b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar(b), parity, abort_flag, p.err));
+      };
+      bool ok = wait_all(C::B_OUT, 0);
       for (int n = 0; n < NBUF && n < n_items && ok; ++n) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_IF + n % NSTAGE), (n / NSTAGE) & 1, abort_flag, p.err));
+        ok = wait_all(C::B_IF + n % NSTAGE, (n / NSTAGE) & 1);
         if (!ok) break;
         fence_after();
-        issue_sp(n);
+        issue_s(n);
+        issue_dp(n);
+        mma_commit_w(bar(C::B_S + n % NBUF));
       }
       for (int n = 0; n < n_items && ok; ++n) {
         const int b = n % NBUF;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_P + b), (n / NBUF) & 1, abort_flag, p.err));
+        ok = wait_all(C::B_P + b, (n / NBUF) & 1);
         if (!ok) break;
         fence_after();
-        issue_acc(n);
+        if (MODE == kDkdv) {
+          issue_acc0(n);
+          if (NBUF == 1) mma_commit_w(bar(C::B_D0));
+        }
+        issue_acc1(n);
+        mma_commit_w(bar(C::B_D + b));
+        mma_commit_w(bar(C::B_IE + n % NSTAGE));
         const int m = n + NBUF;
-        if (m < n_items) {
-          // the products of item m reuse buffer b: wait until item n's accumulations read it
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_D + b), (n / NBUF) & 1, abort_flag, p.err) &&
-               mbar_wait(bar(C::B_IF + m % NSTAGE), (m / NSTAGE) & 1, abort_flag, p.err));
+        if (m >= n_items) continue;
+        ok = wait_all(C::B_IF + m % NSTAGE, (m / NSTAGE) & 1);
+        if (!ok) break;
+        if (NBUF == 1) {
+          // S(m) overwrites the columns acc0 (dK/dV) read P^T from; in dQ mode the S columns
+          // were free as soon as the compute warps had loaded them
+          if (MODE == kDkdv) ok = wait_all(C::B_D0, n & 1);
           if (!ok) break;
           fence_after();
-          issue_sp(m);
+          issue_s(m);
+          // dP(m) overwrites the dS the last accumulation reads
+          ok = wait_all(C::B_D + b, n & 1);
+          if (!ok) break;
+          fence_after();
+          issue_dp(m);
+        } else {
+          ok = wait_all(C::B_D + b, (n / NBUF) & 1);
+          if (!ok) break;
+          fence_after();
+          issue_s(m);
+          issue_dp(m);
         }
+        mma_commit_w(bar(C::B_S + m % NBUF));
       }
       mma_commit_w(bar(C::B_DRAIN));
       drain_wait(bar(C::B_DRAIN), 0);
     }
   } else {
     // ------------------------------------------------------------------ elementwise + epilogue
-    const int half = (warp - 2) >> 2;  // which 32 of the item's 64 columns
-    const int col0 = 32 * half;
+    const int half = (warp - 2) >> 2;  // which half of the item's columns
     const int quarter = warp & 3;
     const int r = 32 * quarter + lane;  // TMEM lane = outer row (key for dK/dV, query for dQ)
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
@@ -328,7 +364,6 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     for (int n = 0; n < n_items; ++n) {
       const int b = n % NBUF, st = n % NSTAGE;
       const int h = item_head(n);
-      const int i0 = item_row(n) + col0;  // first inner row of this thread's 32 columns
       bool w = mbar_wait(bar(C::B_S + b), (n / NBUF) & 1, abort_flag, p.err);
       // the LSE / D pairs were written by the producer lanes before their arrive on in_full:
       // acquire that barrier too before reading them
@@ -336,84 +371,89 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       fence_after();
-      const uint32_t s_addr = lane_addr + C::BUF + 128 * b + col0, dp_addr = s_addr + 64;
-      uint32_t sv[32], dv[32];
-      __syncwarp();
-      tmem_ld32(s_addr, sv);
-      tmem_ld32(dp_addr, dv);
       const float *brow = brow_dq;
       if (MODE == kDkdv && p.bias && orow_ok) {
         const int bh = p.bias_heads == 1 ? 0 : h;
         brow = p.bias + (size_t)bh * p.max_kv + orow;  // + (q0 + i) * bias_heads * max_kv per column
       }
-      // is every element of this thread's 32 columns visible (no per-element mask)?
-      bool plain;
-      if (MODE == kDkdv) {
-        const int j = orow, ilast = i0 + 31;
-        plain = orow_ok && ilast < sq.q_len && (!p.causal || j <= i0 + off) &&
-                (p.window <= 0 || j >= ilast + off - p.window + 1);
-      } else {
-        const int i = orow, jlast = i0 + 31;
-        plain = orow_ok && jlast < sq.kv_len && (!p.causal || jlast <= i + off) &&
-                (p.window <= 0 || i0 >= i + off - p.window + 1);
-      }
-      plain = plain && p.bias == nullptr;
-      const float4 *lp = ldbuf + st * 32 + 16 * half;  // this half's 16 column pairs (dK/dV)
-      tmem_ld_wait();
-      uint32_t pk[16], dk[16];
-      if (plain) {
-        // every pair visible, no bias: P = 2^(S log2e scale - LSE2), dS = P (dP - D)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = 2 * e;
-          float4 q4;
-          if (MODE == kDkdv) q4 = lp[e];
-          else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
-          const float pa = ex2(fmaf(__uint_as_float(sv[c]), sl2, q4.x));
-          const float pb = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, q4.y));
-          const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
-          pk[e] = pack2(pa, pb, is_bf16);
-          dk[e] = pack2(pa * ta, pb * tb, is_bf16);
+#pragma unroll 1
+      for (int ch = 0; ch < C::CHUNKS; ++ch) {
+        const int col0 = C::HALF * half + 32 * ch;  // this chunk's first column in the item
+        const int i0 = item_row(n) + col0;          // its first inner row
+        const uint32_t s_addr = lane_addr + C::BUF + 2 * IR * b + col0, dp_addr = s_addr + IR;
+        uint32_t sv[32], dv[32];
+        __syncwarp();
+        tmem_ld32(s_addr, sv);
+        tmem_ld32(dp_addr, dv);
+        // is every element of this thread's 32 columns visible (no per-element mask)?
+        bool plain;
+        if (MODE == kDkdv) {
+          const int j = orow, ilast = i0 + 31;
+          plain = orow_ok && ilast < sq.q_len && (!p.causal || j <= i0 + off) &&
+                  (p.window <= 0 || j >= ilast + off - p.window + 1);
+        } else {
+          const int i = orow, jlast = i0 + 31;
+          plain = orow_ok && jlast < sq.kv_len && (!p.causal || jlast <= i + off) &&
+                  (p.window <= 0 || i0 >= i + off - p.window + 1);
         }
-      } else {
+        plain = plain && p.bias == nullptr;
+        const float4 *lp = ldbuf + st * C::PAIRS + col0 / 2;  // this chunk's 16 pairs (dK/dV)
+        tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+        if (plain) {
+          // every pair visible, no bias: P = 2^(S log2e scale - LSE2), dS = P (dP - D)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = 2 * e;
-          float4 q4;
-          if (MODE == kDkdv) q4 = lp[e];
-          else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
-          float xs[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int i = MODE == kDkdv ? i0 + c + u : orow;
-            const int j = MODE == kDkdv ? orow : i0 + c + u;
-            float x = -INFINITY;
-            if (orow_ok && i < sq.q_len && pair_visible(i, j, off, sq.kv_len, p.causal, p.window)) {
-              x = __uint_as_float(sv[c + u]) * sl2;
-              if (brow) {
-                const float bv = MODE == kDkdv
-                                     ? __ldg(brow + (size_t)(sq.q0 + i) * p.bias_heads * (size_t)p.max_kv)
-                                     : __ldg(brow + j);
-                x = fmaf(bv, kLog2e, x);
-              }
-            }
-            xs[u] = x;
+          for (int e = 0; e < 16; ++e) {
+            const int c = 2 * e;
+            float4 q4;
+            if (MODE == kDkdv) q4 = lp[e];
+            else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
+            const float pa = ex2(fmaf(__uint_as_float(sv[c]), sl2, q4.x));
+            const float pb = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, q4.y));
+            const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
+            pk[e] = pack2(pa, pb, is_bf16);
+            dk[e] = pack2(pa * ta, pb * tb, is_bf16);
           }
-          // masked logits (-inf) and rows without keys (-LSE2 = -inf) give P = 0
-          const float pa = ex2(xs[0] + q4.x), pb = ex2(xs[1] + q4.y);
-          const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
-          pk[e] = pack2(pa, pb, is_bf16);
-          dk[e] = pack2(pa * ta, pb * tb, is_bf16);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = 2 * e;
+            float4 q4;
+            if (MODE == kDkdv) q4 = lp[e];
+            else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
+            float xs[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int i = MODE == kDkdv ? i0 + c + u : orow;
+              const int j = MODE == kDkdv ? orow : i0 + c + u;
+              float x = -INFINITY;
+              if (orow_ok && i < sq.q_len && pair_visible(i, j, off, sq.kv_len, p.causal, p.window)) {
+                x = __uint_as_float(sv[c + u]) * sl2;
+                if (brow) {
+                  const float bv = MODE == kDkdv
+                                       ? __ldg(brow + (size_t)(sq.q0 + i) * p.bias_heads * (size_t)p.max_kv)
+                                       : __ldg(brow + j);
+                  x = fmaf(bv, kLog2e, x);
+                }
+              }
+              xs[u] = x;
+            }
+            // masked logits (-inf) and rows without keys (-LSE2 = -inf) give P = 0
+            const float pa = ex2(xs[0] + q4.x), pb = ex2(xs[1] + q4.y);
+            const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
+            pk[e] = pack2(pa, pb, is_bf16);
+            dk[e] = pack2(pa * ta, pb * tb, is_bf16);
+          }
         }
+        __syncwarp();
+        if (MODE == kDkdv) tmem_st16(s_addr, pk);
+        tmem_st16(dp_addr, dk);
       }
-      __syncwarp();
-      if (MODE == kDkdv) tmem_st16(s_addr, pk);
-      tmem_st16(dp_addr, dk);
       tmem_st_wait();
       fence_before();
       mbar_arrive(bar(C::B_P + b));
     }
-    // epilogue: the last item's accumulations complete every MMA of the CTA
+    // epilogue: the last item's last accumulation completes every MMA of the CTA
     if (ok && n_items > 0)
       ok = mbar_wait(bar(C::B_D + (n_items - 1) % NBUF), ((n_items - 1) / NBUF) & 1, abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
@@ -467,9 +507,9 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   }
 }
 
-template <int MODE, int DQK, int DV, int NBUF, int NSTAGE>
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE>
 cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
-  using C = BwdCfg<MODE, DQK, DV, NBUF, NSTAGE>;
+  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE>;
   const int bf = p.dtype == VLF_BF16;
   BwdMaps m;
   const uint64_t tq = p.total_q, tk = p.total_kv;
@@ -477,19 +517,19 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   if (MODE == kDkdv) {
     ok = make_tmap_16bit(&m.outer0, p.k, tk, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, 128, bf) &&
          make_tmap_16bit(&m.outer1, p.v, tk, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, 128, bf) &&
-         make_tmap_16bit(&m.inner0, p.q, tq, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, 64, bf) &&
-         make_tmap_16bit(&m.inner1, p.dout, tq, (uint64_t)p.h_q * DV, (uint64_t)p.h_q * DV, 64, bf);
+         make_tmap_16bit(&m.inner0, p.q, tq, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, IR, bf) &&
+         make_tmap_16bit(&m.inner1, p.dout, tq, (uint64_t)p.h_q * DV, (uint64_t)p.h_q * DV, IR, bf);
   } else {
     ok = make_tmap_16bit(&m.outer0, p.q, tq, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, 128, bf) &&
          make_tmap_16bit(&m.outer1, p.dout, tq, (uint64_t)p.h_q * DV, (uint64_t)p.h_q * DV, 128, bf) &&
-         make_tmap_16bit(&m.inner0, p.k, tk, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, 64, bf) &&
-         make_tmap_16bit(&m.inner1, p.v, tk, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, 64, bf);
+         make_tmap_16bit(&m.inner0, p.k, tk, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, IR, bf) &&
+         make_tmap_16bit(&m.inner1, p.v, tk, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, IR, bf);
   }
   if (!ok) return cudaErrorInvalidValue;
   const dim3 grid(MODE == kDkdv ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128,
                   MODE == kDkdv ? p.h_kv : p.h_q, p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  auto kern = tc_bwd_kernel<MODE, DQK, DV, NBUF, NSTAGE>;
+  auto kern = tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 320, C::SMEM, st>>>(m, p);
@@ -498,15 +538,19 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   return e;
 }
 
-template <int DQK, int DV, int NBUF_KV>
+// Per head width: item rows, buffers and stages of the dK/dV kernel (IR_KV, NBUF_KV, NST_KV)
+// and of the dQ kernel (IR_Q, NBUF_Q, NST_Q).  dK/dV keeps 64-row items with two S/dP buffers
+// (its four products per item overlap the elementwise pass); dQ takes 128-row items where the
+// head width leaves room.
+template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int IR_Q, int NBUF_Q, int NST_Q>
 cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   cudaError_t e;
   if ((e = mark(ev, 0, st)) != cudaSuccess) return e;
   if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDkdv, DQK, DV, NBUF_KV, 3>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV>(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDq, DQK, DV, 2, 3>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDq, DQK, DV, IR_Q, NBUF_Q, NST_Q>(p, st)) != cudaSuccess) return e;
   return mark(ev, 3, st);
 }
 
@@ -520,9 +564,9 @@ bool tc_backward_supported(const Params &p) {
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   if (p.total_q == 0 || p.total_kv == 0) return simt_backward(p, st, ev);
-  if (p.d_qk == 64) return bwd_shape<64, 64, 2>(p, st, ev);
-  if (p.d_qk == 128) return bwd_shape<128, 128, 2>(p, st, ev);
-  return bwd_shape<192, 128, 1>(p, st, ev);
+  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 3, 128, 1, 3>(p, st, ev);
+  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 3, 128, 1, 2>(p, st, ev);
+  return bwd_shape<192, 128, 64, 1, 3, 64, 2, 3>(p, st, ev);
 }
 
 // The tensor-core backward writes dQ directly (no fp32 accumulator); only the row dot
