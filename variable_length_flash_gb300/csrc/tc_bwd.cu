@@ -94,7 +94,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE>
+// BF16: element type of the 16-bit tensors (bf16, else fp16), fixed at compile time so the
+// per-element conversions carry no runtime branch.
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, bool BF16>
 __global__ void __launch_bounds__(320, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE>;
@@ -166,7 +168,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int is_bf16 = p.dtype == VLF_BF16;
+  constexpr int is_bf16 = BF16 ? 1 : 0;
 
   // item n -> (query head, first inner row) ; inner rows are queries (dK/dV) or keys (dQ)
   auto item_head = [&](int n) { return MODE == kDkdv ? hk * p.group + n / nq_tiles : head_outer; };
@@ -529,7 +531,8 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   const dim3 grid(MODE == kDkdv ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128,
                   MODE == kDkdv ? p.h_kv : p.h_q, p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  auto kern = tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE>;
+  auto kern = bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, true>
+                 : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 320, C::SMEM, st>>>(m, p);

@@ -6,18 +6,24 @@
 //
 //  * A CTA owns two 128-row query tiles of one sequence: consecutive row blocks of one head, or,
 //    when a kv head serves an even number of query heads (GQA), the same rows of two query
-//    heads that share K/V.  Each K/V tile brought into shared memory feeds both.
-//  * Warp roles (320 threads): warp 0 issues TMA loads (Q once, then K and V tiles into rings);
-//    warp 1 allocates TMEM and issues the MMAs from one thread; warps 2-5 run the softmax of
-//    query tile 0 and warps 6-9 that of tile 1, one thread per query row (TMEM lane = row).
-//  * TMEM (512 columns): S_t at column 128 t, O_t at 256 + 128 t.  P_t (16-bit) is written over
-//    the first half of S_t and fed to the P.V MMA straight from TMEM.
+//    heads that share K/V.  Each 64-key K/V tile brought into shared memory feeds both.
+//  * Warp roles (416 threads): warp 0 issues TMA loads (Q once, then K and V tiles into rings);
+//    warps 1, 10, 11 and 12 issue the MMAs (S and P.V of each query tile, one issuer per SM
+//    sub-partition), warp 1 also owns the TMEM allocation; warps 2-5 run the softmax of query
+//    tile 0 and warps 6-9 that of tile 1, one thread per query row (TMEM lane = row).
+//  * TMEM (512 columns): query tile t owns two 64-column S buffers at 128 t and 128 t + 64 and
+//    its O accumulator at 256 + 128 t.  KV tile n of a query tile lands in S buffer n mod 2, so
+//    S(n+1) is computed while the softmax of S(n) runs and the softmax warps go from one tile
+//    to the next without waiting for the tensor core.  P(n) (16-bit) is written over the first
+//    32 columns of its S buffer and fed to the P.V MMA straight from TMEM; S(n+2) reuses the
+//    buffer once that P.V has completed.
 //  * Tile scheduler (mtlattn 0.3.0, "Use"): each query tile visits only the KV tiles of its
 //    causal / window band; the per-element mask is applied only in the tiles the band cuts.
-//    Tiles start at multiples of 128 keys, so skipping changes no bit of the result.
+//    Tiles start at multiples of 64 keys, so skipping changes no bit of the result.
 //  * Online softmax in base 2 with the scale folded into one FMA; the running max used for the
 //    exponent is only moved (and O rescaled) when the row max grows by more than 8 (P <= 256),
-//    which leaves the result mathematically unchanged.  O is normalised by the sum of the
+//    which leaves the result mathematically unchanged.  A rescale waits for the previous P.V
+//    (the only time the softmax waits on the tensor core).  O is normalised by the sum of the
 //    16-bit P values the MMA actually multiplies (a one-hot row returns its V row unchanged);
 //    LSE uses the fp32 sum.
 //  * Every wait is bounded (see tc_common.cuh); a timeout records VLF_ERR_TIMEOUT and the CTA
@@ -37,6 +43,7 @@ using namespace tc;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kBN = 64;                    // keys per KV tile
 
 struct FwdMaps {
   CUtensorMap q, k, v;
@@ -45,20 +52,25 @@ struct FwdMaps {
 template <int DQK, int DV, int NK, int NV>
 struct FwdCfg {
   static constexpr int KBQ = DQK / 64, KBV = DV / 64;  // 64-column (128-byte) swizzle blocks
-  static constexpr int BLK = 128 * 128;                // bytes of one 128-row x 64-col block
-  static constexpr int Q_BYTES = KBQ * BLK, K_BYTES = KBQ * BLK, V_BYTES = KBV * BLK;
+  static constexpr int QBLK = 128 * 128;               // one 128-row x 64-col block of Q
+  static constexpr int KVBLK = kBN * 128;              // one 64-row x 64-col block of K or V
+  static constexpr int Q_BYTES = KBQ * QBLK, K_BYTES = KBQ * KVBLK, V_BYTES = KBV * KVBLK;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NK * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * V_BYTES;
-  // barriers: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2],
-  // o_done[2], drain
+  // barriers: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], then per query tile t
+  // and S buffer b (index 2 t + b): s_full, p_full, o_done (the P.V that read buffer b); drain
+  // (one per MMA-issuing warp)
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NK, B_VF = B_KE + NK, B_VE = B_VF + NV;
-  static constexpr int B_S = B_VE + NV, B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2;
-  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int B_S = B_VE + NV, B_P = B_S + 4, B_O = B_P + 4, B_DRAIN = B_O + 4;
+  static constexpr int NBAR = B_DRAIN + 4;  // one drain barrier per MMA-issuing warp
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 416;
+  // the MMA warp needs K three tiles ahead of V: with fewer than 3 V stages the producer would
+  // wait for a V slot the MMA warp frees only after it has the K tile it is waiting for
+  static_assert(NV >= 3 && NK >= 3, "ring depth");
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "tile shapes");
   static_assert(SMEM <= 232448, "shared memory");
 };
@@ -88,7 +100,7 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
       kv_band(ti.row0[t], min(ti.row0[t] + 128, sq.q_len), sq.q_len, sq.kv_len, p.causal,
               p.window, klo, khi);
       if (p.flags & VLF_FLAG_NO_SKIP) { klo = 0; khi = sq.kv_len; }
-      if (khi > klo) { jl = klo / 128; jh = (khi + 127) / 128; }
+      if (khi > klo) { jl = klo / kBN; jh = (khi + kBN - 1) / kBN; }
     }
     ti.jlo[t] = jl;
     ti.jhi[t] = jh;
@@ -100,8 +112,17 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
   else { ti.lo = min(ti.jlo[0], ti.jlo[1]); ti.hi = max(ti.jhi[0], ti.jhi[1]); }
 }
 
-template <int DQK, int DV, int NK, int NV>
-__global__ void __launch_bounds__(320, 1)
+// Barrier phases.  Each (tile, buffer) barrier completes once per use of that buffer, and a use
+// n + 2 never starts before use n has been consumed (S(n+2) is issued after P.V(n) completed;
+// P.V(n+2) after the softmax of S(n+2)), so every waiter is at most one phase behind and the
+// parity (n >> 1) & 1 is unambiguous.  tcgen05.commit arrives when every MMA the committing
+// thread issued before it has completed; the P.V MMAs of a query tile come from one warp, so the
+// o_done of P.V(n) also covers P.V(n-1).
+
+// BF16: element type of Q/K/V/O (bf16, else fp16), fixed at compile time so the per-element
+// conversions carry no runtime branch.
+template <int DQK, int DV, int NK, int NV, bool BF16>
+__global__ void __launch_bounds__(416, 1)
 tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   using C = FwdCfg<DQK, DV, NK, NV>;
   extern __shared__ uint8_t smem_raw[];
@@ -130,14 +151,15 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_Q), 1);
-    for (int i = 0; i < NK; ++i) { mbar_init(bar(C::B_KF + i), 1); mbar_init(bar(C::B_KE + i), 1); }
-    for (int i = 0; i < NV; ++i) { mbar_init(bar(C::B_VF + i), 1); mbar_init(bar(C::B_VE + i), 1); }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar(C::B_S + t), 1);
-      mbar_init(bar(C::B_P + t), 128);
-      mbar_init(bar(C::B_O + t), 1);
+    // a K or V slot is free once both query tiles' issuers have released it
+    for (int i = 0; i < NK; ++i) { mbar_init(bar(C::B_KF + i), 1); mbar_init(bar(C::B_KE + i), 2); }
+    for (int i = 0; i < NV; ++i) { mbar_init(bar(C::B_VF + i), 1); mbar_init(bar(C::B_VE + i), 2); }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(C::B_S + i), 1);
+      mbar_init(bar(C::B_P + i), 128);
+      mbar_init(bar(C::B_O + i), 1);
+      mbar_init(bar(C::B_DRAIN + i), 1);
     }
-    mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -150,7 +172,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   fence_after();
   const uint32_t tmem = *tmem_holder;
   const int hk = ti.head[0] / p.group;  // both query tiles read the same kv head
-  const int is_bf16 = p.dtype == VLF_BF16;
+  constexpr int is_bf16 = BF16 ? 1 : 0;
   const int lo = ti.lo, hi = ti.hi;
 
   if (warp == 0) {
@@ -165,7 +187,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       for (int t = 0; t < 2; ++t) {
         if (ti.row0[t] >= sq.q_len) continue;
         for (int c = 0; c < C::KBQ; ++c)
-          tma_load_2d(sQ + t * C::Q_BYTES + c * C::BLK, &maps.q, ti.head[t] * DQK + 64 * c,
+          tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q, ti.head[t] * DQK + 64 * c,
                       sq.q0 + ti.row0[t], bar(C::B_Q));
       }
       int k_issued[NK] = {0}, v_issued[NV] = {0};
@@ -177,15 +199,15 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         if (!ok) break;
         mbar_expect_tx(bar(C::B_KF + ks), C::K_BYTES);
         for (int c = 0; c < C::KBQ; ++c)
-          tma_load_2d(sK + ks * C::K_BYTES + c * C::BLK, &maps.k, hk * DQK + 64 * c,
-                      sq.k0 + j * 128, bar(C::B_KF + ks));
+          tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, &maps.k, hk * DQK + 64 * c,
+                      sq.k0 + j * kBN, bar(C::B_KF + ks));
         ++k_issued[ks];
         if (it >= NV) ok = mbar_wait(bar(C::B_VE + vs), ((it / NV) - 1) & 1, abort_flag, p.err);
         if (!ok) break;
         mbar_expect_tx(bar(C::B_VF + vs), C::V_BYTES);
         for (int c = 0; c < C::KBV; ++c)
-          tma_load_2d(sV + vs * C::V_BYTES + c * C::BLK, &maps.v, hk * DV + 64 * c,
-                      sq.k0 + j * 128, bar(C::B_VF + vs));
+          tma_load_2d(sV + vs * C::V_BYTES + c * C::KVBLK, &maps.v, hk * DV + 64 * c,
+                      sq.k0 + j * kBN, bar(C::B_VF + vs));
         ++v_issued[vs];
       }
       // make sure no copy is still landing in shared memory when the CTA leaves
@@ -195,78 +217,81 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       for (int i = 0; i < NV; ++i)
         if (v_issued[i]) drain_wait(bar(C::B_VF + i), (v_issued[i] - 1) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    // the whole warp runs the issue loop (uniform operands); elect.sync picks the issuing lane
+  } else if (warp == 1 || warp >= 10) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Four warps issue MMAs, one per SM sub-partition: S = Q K^T of query tile 0 (warp 1) and
+    // tile 1 (warp 11), O += P V of tile 0 (warp 12) and tile 1 (warp 10).  An MMA issue returns
+    // only once the tensor pipe accepts it, so an issuer that waits (for a P, or for a P.V to
+    // free an S buffer) would leave the pipe idle if it were the only one; and a warp blocked in
+    // MMA issue slows the other warps of its sub-partition, so the issue load is spread evenly
+    // over the softmax warps.  Each issuer walks every KV tile of the CTA's range (to release
+    // its share of the K or V ring slot) and issues the MMAs of its own query tile; it runs its
+    // loop as a whole warp (uniform operands) and elect.sync picks the issuing lane.
+    const bool is_s = warp == 1 || warp == 11;
+    const int t = (warp == 1 || warp == 12) ? 0 : 1;
+    const int drain = C::B_DRAIN + (warp == 1 ? 0 : warp - 9);
     if (hi > lo) {
-      const uint32_t id_s = idesc_f16(is_bf16, 128, 128, 0, 0);  // S = Q K^T, both K-major
-      const uint32_t id_o = idesc_f16(is_bf16, 128, DV, 0, 1);   // O += P V, V MN-major
-      int pv_count[2] = {0, 0}, p_count[2] = {0, 0};
-      auto part = [&](int t, int j) { return j >= ti.jlo[t] && j < ti.jhi[t]; };
-      auto issue_s = [&](int t, int j) {
-        const uint32_t ks = (uint32_t)((j - lo) % NK);
+      const int jlo = ti.jlo[t], jhi = ti.jhi[t];
+      bool ok = true;
+      if (is_s) {
+        const uint32_t id_s = idesc_f16(is_bf16, 128, kBN, 0, 0);  // both operands K-major
         const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
-        const uint64_t dk = sdesc_sw128(sK + ks * C::K_BYTES, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          // a K step adds its byte offset / 16 to the descriptor's start-address field
-          const uint64_t off = (uint64_t)(((kk >> 2) * C::BLK + (kk & 3) * 32) >> 4);
-          mma_ss_w(tmem + 128 * t, dq + off, dk + off, id_s, kk > 0);
-        }
-        mma_commit_w(bar(C::B_S + t));
-      };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t vs = (uint32_t)((j - lo) % NV);
-        const uint64_t dv = sdesc_sw128(sV + vs * C::V_BYTES, C::BLK, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk)
-          mma_ts_w(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, dv + (uint64_t)((kk * 2048) >> 4),
-                   id_o, (j > ti.jlo[t] || kk > 0) ? 1u : 0u);
-        mma_commit_w(bar(C::B_O + t));
-        ++pv_count[t];
-      };
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_Q), 0, abort_flag, p.err) &&
-                mbar_wait(bar(C::B_KF + 0), 0, abort_flag, p.err));
-      if (ok) {
-        fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (part(t, lo)) issue_s(t, lo);
-        mma_commit_w(bar(C::B_KE + 0));
-      }
-      for (int j = lo; j < hi && ok; ++j) {
-        const int it = j - lo;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_VF + it % NV), (it / NV) & 1, abort_flag, p.err));
-        if (!ok) break;
-        fence_after();
-        bool k_next = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (part(t, j)) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_P + t), p_count[t] & 1, abort_flag, p.err));
-            if (!ok) break;
-            ++p_count[t];
-            fence_after();
-            issue_pv(t, j);
-          }
-          if (j + 1 < hi && part(t, j + 1)) {
-            if (!k_next) {
-              ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KF + (it + 1) % NK), ((it + 1) / NK) & 1, abort_flag, p.err));
+        const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_Q), 0, abort_flag, p.err));
+        for (int j = lo; j < hi && ok; ++j) {
+          const int it = j - lo;
+          // every issuer waits for each K tile, used or not: its release of the slot then never
+          // runs a full ring ahead of the other tile's, which keeps the two-arrival phases apart
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KF + it % NK), (it / NK) & 1, abort_flag, p.err));
+          if (!ok) break;
+          if (j >= jlo && j < jhi) {
+            const int n = j - jlo, b = n & 1;
+            if (n >= 2) {
+              // S(n) overwrites the buffer P(n-2) was read from: wait for that P.V
+              const int np = n - 2;
+              ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_O + 2 * t + b), (np >> 1) & 1, abort_flag, p.err));
               if (!ok) break;
-              k_next = true;
             }
-            // S_t(j+1) overwrites the TMEM columns P_t(j) was read from: wait for that P.V
-            if (part(t, j)) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_O + t), (pv_count[t] - 1) & 1, abort_flag, p.err));
+            fence_after();
+            const uint64_t dk = dk0 + (uint64_t)(((it % NK) * C::K_BYTES) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < DQK / 16; ++kk) {
+              // a K step adds its byte offset / 16 to the descriptor's start-address field
+              const uint64_t oq = (uint64_t)(((kk >> 2) * C::QBLK + (kk & 3) * 32) >> 4);
+              const uint64_t okk = (uint64_t)(((kk >> 2) * C::KVBLK + (kk & 3) * 32) >> 4);
+              mma_ss_w(tmem + 128 * t + 64 * b, dq + oq, dk + okk, id_s, kk > 0);
+            }
+            mma_commit_w(bar(C::B_S + 2 * t + b));
+          }
+          // this tile's share of releasing the K slot (arrives once its S MMAs have read it)
+          mma_commit_w(bar(C::B_KE + it % NK));
+        }
+      } else {
+        const uint32_t id_o = idesc_f16(is_bf16, 128, DV, 0, 1);  // V is MN-major
+        const uint64_t dv0 = sdesc_sw128(sV, C::KVBLK, 1024);
+        for (int j = lo; j < hi && ok; ++j) {
+          const int it = j - lo;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_VF + it % NV), (it / NV) & 1, abort_flag, p.err));
+          if (!ok) break;
+          if (j >= jlo && j < jhi) {
+            const int n = j - jlo, b = n & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_P + 2 * t + b), (n >> 1) & 1, abort_flag, p.err));
             if (!ok) break;
             fence_after();
-            issue_s(t, j + 1);
+            const uint64_t dv = dv0 + (uint64_t)(((it % NV) * C::V_BYTES) >> 4);
+            const uint32_t pcol = tmem + 128 * t + 64 * b;
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts_w(tmem + 256 + 128 * t, pcol + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), id_o,
+                       (n > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_w(bar(C::B_O + 2 * t + b));
           }
+          mma_commit_w(bar(C::B_VE + it % NV));
         }
-        if (!ok) break;
-        mma_commit_w(bar(C::B_VE + it % NV));
-        if (j + 1 < hi) mma_commit_w(bar(C::B_KE + (it + 1) % NK));
       }
-      // drain: every MMA this thread issued has completed before TMEM is released
-      mma_commit_w(bar(C::B_DRAIN));
-      drain_wait(bar(C::B_DRAIN), 0);
+      // drain: every MMA this warp issued has completed before TMEM is released
+      mma_commit_w(bar(drain));
+      drain_wait(bar(drain), 0);
     }
   } else {
     // ------------------------------------------------------------------ softmax / epilogue
@@ -290,39 +315,36 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     const int jlo = ti.jlo[t], jhi = ti.jhi[t];
     bool ok = true;
     for (int j = jlo; j < jhi; ++j) {
-      const int n = j - jlo;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_S + t), n & 1, abort_flag, p.err));
+      const int n = j - jlo, b = n & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_S + 2 * t + b), (n >> 1) & 1, abort_flag, p.err));
       if (!ok) break;
       fence_after();
-      const int kb = j * 128;
-      const bool full = row_ok && (kb + 127 < sq.kv_len) && (!p.causal || kb + 127 <= i + off) &&
+      const uint32_t sb = s_addr + 64 * b;
+      const int kb = j * kBN;
+      const bool full = row_ok && (kb + kBN - 1 < sq.kv_len) && (!p.causal || kb + kBN - 1 <= i + off) &&
                         (p.window <= 0 || kb >= i + off - p.window + 1);
       const bool plain = full && brow == nullptr;
-      // the whole S row (128 fp32) in registers: four TMEM loads, one wait
-      uint32_t v[128];
+      // the whole S row (64 fp32) in registers: two TMEM loads, one wait
+      uint32_t v[kBN];
       __syncwarp();
-      tmem_ld32_at(s_addr + 0, v, 0);
-      tmem_ld32_at(s_addr + 32, v, 32);
-      tmem_ld32_at(s_addr + 64, v, 64);
-      tmem_ld32_at(s_addr + 96, v, 96);
+      tmem_ld32_at(sb + 0, v, 0);
+      tmem_ld32_at(sb + 32, v, 32);
       tmem_ld_wait();
       // row max of the base-2 logits.  plain rows keep raw q.k in v (the scale goes into the
       // exponent FMA); other rows get v = scale*log2e*q.k + log2e*bias, or -inf where masked.
       float mx;
       if (plain) {
-        float m8[16];
+        float m8[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < 8; ++q) {
           const float *f = reinterpret_cast<const float *>(v) + 8 * q;
           m8[q] = fmax3(fmax3(f[0], f[1], f[2]), fmax3(f[3], f[4], f[5]), fmaxf(f[6], f[7]));
         }
-#pragma unroll
-        for (int q = 0; q < 5; ++q) m8[q] = fmax3(m8[q], m8[q + 5], m8[q + 10]);
-        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), m8[3], fmaxf(m8[4], m8[15])) * sl2;
+        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sl2;
       } else {
         mx = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 128; ++e) {
+        for (int e = 0; e < kBN; ++e) {
           const int kj = kb + e;
           float x = -INFINITY;
           if (row_ok && pair_visible(i, kj, off, sq.kv_len, p.causal, p.window)) {
@@ -341,10 +363,14 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         alpha = ex2(m_ref - m_new);  // m_ref == -inf -> 0
         move = true;
       }
-      // O_t holds earlier tiles' P.V (complete: S_t(j) was issued after it); rescale rows whose
-      // reference moved and that have accumulated something
+      // rows whose reference moved and that have accumulated something rescale O_t, once the
+      // P.V of the previous KV tile (and so every earlier one) has completed
       const bool need = move && n > 0 && l > 0.f;
       if (__any_sync(0xffffffffu, need)) {
+        const int np = n - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_O + 2 * t + (np & 1)), (np >> 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        fence_after();
         const float a = need ? alpha : 1.f;
 #pragma unroll 1
         for (int ch = 0; ch < DV / 32; ++ch) {
@@ -361,16 +387,16 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         lf *= alpha;
         m_ref = m_new;
       }
-      // P = 2^(logit2 - m_ref) two at a time (packed FMA), written in 16-bit over the first half
-      // of S_t.  A row still without any visible key has every logit at -inf: its exponent
-      // offset is taken as 0 so that P = 0.
+      // P = 2^(logit2 - m_ref) two at a time (packed FMA), written in 16-bit over the first 32
+      // columns of the S buffer.  A row still without any visible key has every logit at -inf:
+      // its exponent offset is taken as 0 so that P = 0.
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
       const uint64_t scale2 = f2pack(plain ? sl2 : 1.f, plain ? sl2 : 1.f);
       const uint64_t negm2 = f2pack(neg_m, neg_m);
       uint64_t sumf2 = f2pack(0.f, 0.f);
       float sumr = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < kBN / 32; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -385,7 +411,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           sumr = add_halves(sumr, pk[e], is_bf16);
         }
         __syncwarp();
-        tmem_st16(s_addr + ch * 16, pk);
+        tmem_st16(sb + ch * 16, pk);
       }
       const float2 sf = f2unpack(sumf2);
       l += sumr;
@@ -393,11 +419,14 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       __syncwarp();
       tmem_st_wait();
       fence_before();
-      mbar_arrive(bar(C::B_P + t));
+      mbar_arrive(bar(C::B_P + 2 * t + b));
     }
     // epilogue: O / l in the output dtype, LSE in natural log
     const int nt = jhi - jlo;
-    if (ok && nt > 0) ok = mbar_wait(bar(C::B_O + t), (nt - 1) & 1, abort_flag, p.err);
+    if (ok && nt > 0) {
+      const int np = nt - 1;
+      ok = mbar_wait(bar(C::B_O + 2 * t + (np & 1)), (np >> 1) & 1, abort_flag, p.err);
+    }
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       fence_after();
@@ -486,15 +515,15 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   const int bf = p.dtype == VLF_BF16;
   if (p.total_q == 0 || p.total_kv == 0) return simt_forward(p, st);  // nothing to stage
   if (!make_tmap_16bit(&maps.q, p.q, p.total_q, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, 128, bf) ||
-      !make_tmap_16bit(&maps.k, p.k, p.total_kv, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, 128, bf) ||
-      !make_tmap_16bit(&maps.v, p.v, p.total_kv, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, 128, bf))
+      !make_tmap_16bit(&maps.k, p.k, p.total_kv, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, kBN, bf) ||
+      !make_tmap_16bit(&maps.v, p.v, p.total_kv, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, kBN, bf))
     return cudaErrorInvalidValue;
   const bool pair_heads = (p.group % 2 == 0);
   const int rows_per_cta = pair_heads ? 128 : 256;
   const dim3 grid((p.max_q + rows_per_cta - 1) / rows_per_cta, pair_heads ? p.h_q / 2 : p.h_q,
                   p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  auto kern = tc_fwd_kernel<DQK, DV, NK, NV>;
+  auto kern = bf ? tc_fwd_kernel<DQK, DV, NK, NV, true> : tc_fwd_kernel<DQK, DV, NK, NV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(maps, p);
@@ -505,9 +534,9 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
 }  // namespace
 
 cudaError_t tc_forward(const Params &p, cudaStream_t st) {
-  if (p.d_qk == 64) return launch_fwd<64, 64, 3, 3>(p, st);
-  if (p.d_qk == 128) return launch_fwd<128, 128, 2, 2>(p, st);
-  return launch_fwd<192, 128, 2, 1>(p, st);
+  if (p.d_qk == 64) return launch_fwd<64, 64, 6, 6>(p, st);
+  if (p.d_qk == 128) return launch_fwd<128, 128, 4, 4>(p, st);
+  return launch_fwd<192, 128, 3, 3>(p, st);
 }
 
 }  // namespace vlf
