@@ -121,6 +121,23 @@ __device__ __forceinline__ bool pair_visible(int i, int j, int off, int kv_len, 
   return true;
 }
 
+// The keys pair_visible accepts for row i form one interval: pair_visible(i, j, ...) holds
+// exactly when lo <= j < hi (hi <= lo: the row sees nothing).
+__device__ __forceinline__ void visible_range(int i, int off, int kv_len, int causal, int window,
+                                              int &lo, int &hi) {
+  const long long diag = (long long)i + off;
+  lo = window > 0 ? (int)max(0ll, min((long long)kv_len, diag - window + 1)) : 0;
+  hi = causal ? (int)max(0ll, min((long long)kv_len, diag + 1)) : kv_len;
+}
+// The same for a key j: the query rows i with pair_visible(i, j, ...) are exactly lo <= i < hi
+// (for 0 <= j < kv_len).
+__device__ __forceinline__ void visible_rows(int j, int off, int q_len, int causal, int window,
+                                             int &lo, int &hi) {
+  const long long first = (long long)j - off;  // the first row whose diagonal reaches j
+  lo = causal ? (int)max(0ll, min((long long)q_len, first)) : 0;
+  hi = window > 0 ? (int)max(0ll, min((long long)q_len, first + window)) : q_len;
+}
+
 // Bias element (row = global query row, column = sequence-local key), 64-bit offsets.
 __device__ __forceinline__ float bias_at(const Params &p, int grow, int h, int j) {
   const int bh = p.bias_heads == 1 ? 0 : h;

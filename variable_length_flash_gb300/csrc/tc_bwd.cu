@@ -350,6 +350,11 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     const float sl2 = p.scale_log2;
     const int orow = tile0 + r;  // this thread's outer row
     const bool orow_ok = MODE == kDkdv ? orow < sq.kv_len : orow < sq.q_len;
+    // the columns this row may see form one interval (query rows for dK/dV, keys for dQ)
+    int vis_lo, vis_hi;
+    if (MODE == kDkdv) visible_rows(orow, off, sq.q_len, p.causal, p.window, vis_lo, vis_hi);
+    else visible_range(orow, off, sq.kv_len, p.causal, p.window, vis_lo, vis_hi);
+    if (!orow_ok) vis_hi = vis_lo;
     float row_nl = -INFINITY, row_nd = 0.f;  // dQ: this row's -LSE (base 2) and -D
     const float *brow_dq = nullptr;
     if (MODE == kDq && orow_ok) {
@@ -426,19 +431,16 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             float xs[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int i = MODE == kDkdv ? i0 + c + u : orow;
-              const int j = MODE == kDkdv ? orow : i0 + c + u;
-              float x = -INFINITY;
-              if (orow_ok && i < sq.q_len && pair_visible(i, j, off, sq.kv_len, p.causal, p.window)) {
-                x = __uint_as_float(sv[c + u]) * sl2;
-                if (brow) {
-                  const float bv = MODE == kDkdv
-                                       ? __ldg(brow + (size_t)(sq.q0 + i) * p.bias_heads * (size_t)p.max_kv)
-                                       : __ldg(brow + j);
-                  x = fmaf(bv, kLog2e, x);
-                }
+              const int cc = i0 + c + u;  // sequence-local column: query row (dK/dV) or key (dQ)
+              float x = __uint_as_float(sv[c + u]) * sl2;
+              if (brow) {
+                // (clamped into the sequence: masked columns read a valid address)
+                const float bv = MODE == kDkdv
+                                     ? __ldg(brow + (size_t)(sq.q0 + min(cc, sq.q_len - 1)) * p.bias_heads * (size_t)p.max_kv)
+                                     : __ldg(brow + min(cc, sq.kv_len - 1));
+                x = fmaf(bv, kLog2e, x);
               }
-              xs[u] = x;
+              xs[u] = (cc >= vis_lo && cc < vis_hi) ? x : -INFINITY;
             }
             // masked logits (-inf) and rows without keys (-LSE2 = -inf) give P = 0
             const float pa = ex2(xs[0] + q4.x), pb = ex2(xs[1] + q4.y);

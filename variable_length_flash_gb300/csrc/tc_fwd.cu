@@ -330,92 +330,127 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       tmem_ld32_at(sb + 0, v, 0);
       tmem_ld32_at(sb + 32, v, 32);
       tmem_ld_wait();
-      // row max of the base-2 logits.  plain rows keep raw q.k in v (the scale goes into the
-      // exponent FMA); other rows get v = scale*log2e*q.k + log2e*bias, or -inf where masked.
-      float mx;
-      if (plain) {
+      // P = 2^(logit2 - m_ref) two at a time (packed FMA), written in 16-bit over the first 32
+      // columns of the S buffer, 16 pairs at a time; with the fp32 row sum and the sum of the
+      // rounded P the MMA consumes (so the weights that multiply V are normalised exactly: a
+      // one-hot row returns its V row unchanged).  Two accumulators each keep the dependent add
+      // chains short.
+      float sumr = 0.f, lsum = 0.f;
+      auto exp_pass = [&](float scale, float neg_m) {
+        const uint64_t scale2 = f2pack(scale, scale), negm2 = f2pack(neg_m, neg_m);
+        uint64_t sf0 = f2pack(0.f, 0.f), sf1 = sf0;
+        float sr0 = 0.f, sr1 = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < kBN / 32; ++ch) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = 32 * ch + 2 * e;
+            const float2 x = f2unpack(fma2(f2pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                           scale2, negm2));
+            const float pa = ex2(x.x), pb = ex2(x.y);
+            pk[e] = pack2(pa, pb, is_bf16);
+            if (e & 1) {
+              sf1 = add2(sf1, f2pack(pa, pb));
+              sr1 = add_halves(sr1, pk[e], is_bf16);
+            } else {
+              sf0 = add2(sf0, f2pack(pa, pb));
+              sr0 = add_halves(sr0, pk[e], is_bf16);
+            }
+          }
+          __syncwarp();
+          tmem_st16(sb + ch * 16, pk);
+        }
+        const float2 f0 = f2unpack(sf0), f1 = f2unpack(sf1);
+        lsum = (f0.x + f0.y) + (f1.x + f1.y);
+        sumr = sr0 + sr1;
+      };
+      // Speculative pass: when every row of the warp is an unmasked tile that already has a
+      // reference max, P is computed with that reference while the row max is found alongside
+      // (no dependency between the two).  Only a row max beyond the threshold sends the warp
+      // through the general pass below, which recomputes P; otherwise the reference stays put
+      // and the result is exactly what the general pass gives.
+      bool done = false;
+      if (__all_sync(0xffffffffu, plain && m_ref != -INFINITY)) {
+        exp_pass(sl2, -m_ref);
         float m8[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float *f = reinterpret_cast<const float *>(v) + 8 * q;
           m8[q] = fmax3(fmax3(f[0], f[1], f[2]), fmax3(f[3], f[4], f[5]), fmaxf(f[6], f[7]));
         }
-        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sl2;
-      } else {
-        mx = -INFINITY;
+        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sl2;
+        done = !__any_sync(0xffffffffu, mx > m_ref + kRescaleThreshold);
+        // the general pass rewrites P: let the speculative stores land first
+        if (!done) tmem_st_wait();
+      }
+      if (!done) {
+        // row max of the base-2 logits.  plain rows keep raw q.k in v (the scale goes into the
+        // exponent FMA); other rows get v = scale*log2e*q.k + log2e*bias, or -inf where masked.
+        float mx;
+        if (plain) {
+          float m8[8];
 #pragma unroll
-        for (int e = 0; e < kBN; ++e) {
-          const int kj = kb + e;
-          float x = -INFINITY;
-          if (row_ok && pair_visible(i, kj, off, sq.kv_len, p.causal, p.window)) {
-            x = __uint_as_float(v[e]) * sl2;
-            if (brow) x = fmaf(__ldg(brow + kj), kLog2e, x);
+          for (int q = 0; q < 8; ++q) {
+            const float *f = reinterpret_cast<const float *>(v) + 8 * q;
+            m8[q] = fmax3(fmax3(f[0], f[1], f[2]), fmax3(f[3], f[4], f[5]), fmaxf(f[6], f[7]));
           }
-          v[e] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sl2;
+        } else {
+          // the visible keys of this row are one interval: mask by two compares per element
+          int vlo, vhi;
+          visible_range(i, off, sq.kv_len, p.causal, p.window, vlo, vhi);
+          if (!row_ok) vhi = vlo;
+          const int elo = vlo - kb, ehi = vhi - kb;
+          mx = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < kBN; ++e) {
+            float x = __uint_as_float(v[e]) * sl2;
+            // (the bias column is clamped into the row: masked elements read a valid address)
+            if (brow) x = fmaf(__ldg(brow + min(kb + e, sq.kv_len - 1)), kLog2e, x);
+            x = (e >= elo && e < ehi) ? x : -INFINITY;
+            v[e] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
         }
-      }
-      // move the reference max only when it grows by more than the threshold
-      const float m_new = fmaxf(m_ref, mx);
-      float alpha = 1.f;
-      bool move = false;
-      if (m_new != -INFINITY && m_new > m_ref + kRescaleThreshold) {
-        alpha = ex2(m_ref - m_new);  // m_ref == -inf -> 0
-        move = true;
-      }
-      // rows whose reference moved and that have accumulated something rescale O_t, once the
-      // P.V of the previous KV tile (and so every earlier one) has completed
-      const bool need = move && n > 0 && l > 0.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const int np = n - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_O + 2 * t + (np & 1)), (np >> 1) & 1, abort_flag, p.err));
-        if (!ok) break;
-        fence_after();
-        const float a = need ? alpha : 1.f;
+        // move the reference max only when it grows by more than the threshold
+        const float m_new = fmaxf(m_ref, mx);
+        float alpha = 1.f;
+        bool move = false;
+        if (m_new != -INFINITY && m_new > m_ref + kRescaleThreshold) {
+          alpha = ex2(m_ref - m_new);  // m_ref == -inf -> 0
+          move = true;
+        }
+        // rows whose reference moved and that have accumulated something rescale O_t, once the
+        // P.V of the previous KV tile (and so every earlier one) has completed
+        const bool need = move && n > 0 && l > 0.f;
+        if (__any_sync(0xffffffffu, need)) {
+          const int np = n - 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_O + 2 * t + (np & 1)), (np >> 1) & 1, abort_flag, p.err));
+          if (!ok) break;
+          fence_after();
+          const float a = need ? alpha : 1.f;
 #pragma unroll 1
-        for (int ch = 0; ch < DV / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + ch * 32, o);
-          tmem_ld_wait();
+          for (int ch = 0; ch < DV / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + ch * 32, o);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-          tmem_st32(o_addr + ch * 32, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+            tmem_st32(o_addr + ch * 32, o);
+          }
         }
-      }
-      if (move) {
-        l *= alpha;
-        lf *= alpha;
-        m_ref = m_new;
-      }
-      // P = 2^(logit2 - m_ref) two at a time (packed FMA), written in 16-bit over the first 32
-      // columns of the S buffer.  A row still without any visible key has every logit at -inf:
-      // its exponent offset is taken as 0 so that P = 0.
-      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      const uint64_t scale2 = f2pack(plain ? sl2 : 1.f, plain ? sl2 : 1.f);
-      const uint64_t negm2 = f2pack(neg_m, neg_m);
-      uint64_t sumf2 = f2pack(0.f, 0.f);
-      float sumr = 0.f;
-#pragma unroll
-      for (int ch = 0; ch < kBN / 32; ++ch) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = ch * 32 + 2 * e;
-          const float2 x = f2unpack(fma2(f2pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
-                                         scale2, negm2));
-          const float pa = ex2(x.x), pb = ex2(x.y);
-          sumf2 = add2(sumf2, f2pack(pa, pb));
-          pk[e] = pack2(pa, pb, is_bf16);
-          // the row sum adds the rounded P the MMA consumes, so the weights that multiply V are
-          // normalised exactly (a one-hot row returns its V row unchanged)
-          sumr = add_halves(sumr, pk[e], is_bf16);
+        if (move) {
+          l *= alpha;
+          lf *= alpha;
+          m_ref = m_new;
         }
-        __syncwarp();
-        tmem_st16(sb + ch * 16, pk);
+        // a row still without any visible key has every logit at -inf: its exponent offset is
+        // taken as 0 so that P = 0
+        exp_pass(plain ? sl2 : 1.f, m_ref == -INFINITY ? 0.f : -m_ref);
       }
-      const float2 sf = f2unpack(sumf2);
       l += sumr;
-      lf += sf.x + sf.y;
+      lf += lsum;
       __syncwarp();
       tmem_st_wait();
       fence_before();
