@@ -14,19 +14,19 @@
 //          IR-key K / V items of its band: S = Q K^T, dP = dO V^T, dS in TMEM, dQ += dS K.
 // Item width IR: an MMA of 128 x N x 16 with both operands in shared memory runs at full rate
 // only for N >= 128 (at N = 64 it is limited by shared-memory bandwidth), but 128-row items
-// leave TMEM room for one S/dP buffer only.  The dQ kernel (three products per item) uses
-// 128-row items for head widths 64 and 128; the dK/dV kernel (four products) keeps 64-row items
-// with two S/dP buffers so the next item's products overlap this item's elementwise pass; the
-// latent head (QK width 192) uses 64-row items in both.
-// Warp roles (320 threads): warp 0 stages tiles with TMA and, with all its lanes, the item's LSE
-// and D columns into the same shared-memory stage; warp 1 allocates TMEM and issues the MMAs
-// from the whole converged warp (elect.sync picks the issuing lane); warps 2-9 are two compute
+// leave TMEM room for one S/dP buffer only.  Measured, two buffers of 64-row items win in both
+// kernels (the next item's products overlap this item's elementwise pass); the single-buffer
+// form serves the dK/dV kernel of the latent head (QK width 192), whose dK accumulator leaves
+// room for one buffer only.
+// Warp roles (384 threads): warp 0 stages tiles with TMA and, with all its lanes, the item's LSE
+// and D columns into the same shared-memory stage; warps 1, 11 and 10 issue the S, dP and
+// accumulation MMAs (warp 1 also owns the TMEM allocation); warps 2-9 are two compute
 // warpgroups, each owning half of the item's columns (one thread per TMEM lane).  Each warpgroup
 // writes its 16-bit P / dS over its own S / dP columns.
-// MMA order with one S/dP buffer: after item n's P / dS are ready the accumulations of n are
-// queued; S(n+1) is issued as soon as the accumulation that reads the S columns has completed
-// (it then queues behind the other accumulation), dP(n+1) once the dP columns are released.
-// With two buffers item n+2's products follow the completion of item n's accumulations.
+// MMA order with one S/dP buffer: after item n's P / dS are ready its accumulations are issued;
+// S(n+1) follows as soon as the accumulation that reads the S columns has completed, dP(n+1)
+// once the dP columns are released.  With two buffers item n+2's products follow the
+// completion of item n's accumulations.
 // Tiles outside the causal / window band are skipped (they contribute exact zeros).  Every wait
 // is bounded.
 #include <cudaTypedefs.h>
@@ -66,12 +66,12 @@ struct BwdCfg {
   static constexpr int PAIRS = IR / 2;
   static constexpr int OFF_LD = OFF_IN + NSTAGE * STAGE_BYTES;
   static constexpr int OFF_BAR = OFF_LD + NSTAGE * PAIRS * 16;
-  // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE], s_full[NBUF], p_ready[NBUF],
-  // acc0_done (dV; single buffer only), acc_done[NBUF] (dK or dQ: the item's last accumulation),
-  // drain
+  // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE], s_full[NBUF] (S and dP issued:
+  // two arrivals), p_ready[NBUF], acc0_done (dV; single buffer only), acc_done[NBUF] (dK or dQ:
+  // the item's last accumulation), drain[3]
   static constexpr int B_OUT = 0, B_IF = 1, B_IE = B_IF + NSTAGE, B_S = B_IE + NSTAGE;
   static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + 1, B_DRAIN = B_D + NBUF;
-  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int NBAR = B_DRAIN + 3;  // one drain barrier per MMA-issuing warp
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   // TMEM: accumulators first, then NBUF x (S IR cols, dP IR cols)
@@ -97,7 +97,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // BF16: element type of the 16-bit tensors (bf16, else fp16), fixed at compile time so the
 // per-element conversions carry no runtime branch.
 template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE>;
   extern __shared__ uint8_t smem_raw[];
@@ -151,12 +151,12 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     // writing its LSE / D pairs); p_ready: all 256 compute threads
     for (int i = 0; i < NSTAGE; ++i) { mbar_init(bar(C::B_IF + i), 33); mbar_init(bar(C::B_IE + i), 1); }
     for (int b = 0; b < NBUF; ++b) {
-      mbar_init(bar(C::B_S + b), 1);
+      mbar_init(bar(C::B_S + b), 2);
       mbar_init(bar(C::B_P + b), 256);
       mbar_init(bar(C::B_D + b), 1);
     }
     mbar_init(bar(C::B_D0), 1);
-    mbar_init(bar(C::B_DRAIN), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(bar(C::B_DRAIN + i), 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -240,8 +240,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           if (issued[i]) drain_wait(bar(C::B_IF + i), (issued[i] - 1) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp >= 10) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Three warps on three SM sub-partitions: warp 1 issues S (dK/dV: S^T), warp 11 dP (dP^T),
+    // warp 10 the two accumulations that take their A operand from TMEM.  An MMA issue returns
+    // only once the tensor pipe accepts it, so one issuer waiting on a completion would leave
+    // the pipe idle; split, each waits only for what its own products need.  Each runs its
+    // loop as a whole converged warp (uniform operands) and elect.sync picks the issuing lane.
+    const int role = warp == 1 ? 0 : (warp == 11 ? 1 : 2);  // 0: S, 1: dP, 2: accumulations
     if (n_items > 0) {
       // S / dP: M = 128 outer rows, N = IR inner rows, both operands K-major
       const uint32_t id_sp = idesc_f16(is_bf16, 128, IR, 0, 0);
@@ -292,54 +298,52 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       auto wait_all = [&](int b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar(b), parity, abort_flag, p.err));
       };
-      bool ok = wait_all(C::B_OUT, 0);
-      for (int n = 0; n < NBUF && n < n_items && ok; ++n) {
-        ok = wait_all(C::B_IF + n % NSTAGE, (n / NSTAGE) & 1);
-        if (!ok) break;
-        fence_after();
-        issue_s(n);
-        issue_dp(n);
-        mma_commit_w(bar(C::B_S + n % NBUF));
-      }
-      for (int n = 0; n < n_items && ok; ++n) {
-        const int b = n % NBUF;
-        ok = wait_all(C::B_P + b, (n / NBUF) & 1);
-        if (!ok) break;
-        fence_after();
-        if (MODE == kDkdv) {
-          issue_acc0(n);
-          if (NBUF == 1) mma_commit_w(bar(C::B_D0));
+      bool ok = true;
+      if (role < 2) {
+        // products of item m, once its inner tile has landed and its TMEM columns are free
+        ok = wait_all(C::B_OUT, 0);
+        for (int m = 0; m < n_items && ok; ++m) {
+          const int b = m % NBUF;
+          ok = wait_all(C::B_IF + m % NSTAGE, (m / NSTAGE) & 1);
+          if (!ok) break;
+          if (m >= NBUF) {
+            const int n = m - NBUF;  // the item that used these columns before
+            if (NBUF == 2) {
+              // both S and dP columns are free once item n's accumulations have completed
+              ok = wait_all(C::B_D + b, (n / NBUF) & 1);
+            } else if (role == 0) {
+              // S(m) overwrites the columns accumulation 0 (dK/dV) read P^T from; in dQ mode
+              // they were free as soon as the compute warps had loaded them
+              ok = MODE == kDkdv ? wait_all(C::B_D0, n & 1) : wait_all(C::B_P + b, n & 1);
+            } else {
+              // dP(m) overwrites the dS the last accumulation reads
+              ok = wait_all(C::B_D + b, n & 1);
+            }
+            if (!ok) break;
+          }
+          fence_after();
+          if (role == 0) issue_s(m);
+          else issue_dp(m);
+          mma_commit_w(bar(C::B_S + b));
         }
-        issue_acc1(n);
-        mma_commit_w(bar(C::B_D + b));
-        mma_commit_w(bar(C::B_IE + n % NSTAGE));
-        const int m = n + NBUF;
-        if (m >= n_items) continue;
-        ok = wait_all(C::B_IF + m % NSTAGE, (m / NSTAGE) & 1);
-        if (!ok) break;
-        if (NBUF == 1) {
-          // S(m) overwrites the columns acc0 (dK/dV) read P^T from; in dQ mode the S columns
-          // were free as soon as the compute warps had loaded them
-          if (MODE == kDkdv) ok = wait_all(C::B_D0, n & 1);
+      } else {
+        for (int n = 0; n < n_items && ok; ++n) {
+          const int b = n % NBUF;
+          ok = wait_all(C::B_P + b, (n / NBUF) & 1);
           if (!ok) break;
           fence_after();
-          issue_s(m);
-          // dP(m) overwrites the dS the last accumulation reads
-          ok = wait_all(C::B_D + b, n & 1);
-          if (!ok) break;
-          fence_after();
-          issue_dp(m);
-        } else {
-          ok = wait_all(C::B_D + b, (n / NBUF) & 1);
-          if (!ok) break;
-          fence_after();
-          issue_s(m);
-          issue_dp(m);
+          if (MODE == kDkdv) {
+            issue_acc0(n);
+            if (NBUF == 1) mma_commit_w(bar(C::B_D0));
+          }
+          issue_acc1(n);
+          mma_commit_w(bar(C::B_D + b));
+          mma_commit_w(bar(C::B_IE + n % NSTAGE));
         }
-        mma_commit_w(bar(C::B_S + m % NBUF));
       }
-      mma_commit_w(bar(C::B_DRAIN));
-      drain_wait(bar(C::B_DRAIN), 0);
+      const int drain = C::B_DRAIN + role;
+      mma_commit_w(bar(drain));
+      drain_wait(bar(drain), 0);
     }
   } else {
     // ------------------------------------------------------------------ elementwise + epilogue
@@ -537,16 +541,14 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
                  : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 320, C::SMEM, st>>>(m, p);
+  kern<<<grid, 384, C::SMEM, st>>>(m, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
 }
 
 // Per head width: item rows, buffers and stages of the dK/dV kernel (IR_KV, NBUF_KV, NST_KV)
-// and of the dQ kernel (IR_Q, NBUF_Q, NST_Q).  dK/dV keeps 64-row items with two S/dP buffers
-// (its four products per item overlap the elementwise pass); dQ takes 128-row items where the
-// head width leaves room.
+// and of the dQ kernel (IR_Q, NBUF_Q, NST_Q).
 template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int IR_Q, int NBUF_Q, int NST_Q>
 cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   cudaError_t e;
@@ -569,8 +571,8 @@ bool tc_backward_supported(const Params &p) {
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   if (p.total_q == 0 || p.total_kv == 0) return simt_backward(p, st, ev);
-  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 3, 128, 1, 3>(p, st, ev);
-  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 3, 128, 1, 2>(p, st, ev);
+  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 3, 64, 2, 3>(p, st, ev);
+  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 3, 64, 2, 3>(p, st, ev);
   return bwd_shape<192, 128, 64, 1, 3, 64, 2, 3>(p, st, ev);
 }
 
