@@ -23,10 +23,10 @@
 // accumulation MMAs (warp 1 also owns the TMEM allocation); warps 2-9 are two compute
 // warpgroups, each owning half of the item's columns (one thread per TMEM lane).  Each warpgroup
 // writes its 16-bit P / dS over its own S / dP columns.
-// MMA order with one S/dP buffer: after item n's P / dS are ready its accumulations are issued;
-// S(n+1) follows as soon as the accumulation that reads the S columns has completed, dP(n+1)
-// once the dP columns are released.  With two buffers item n+2's products follow the
-// completion of item n's accumulations.
+// MMA order: after item n's P / dS are ready its accumulations are issued; the products of the
+// item that next uses n's columns (n + NBUF) follow as soon as those columns are released: S
+// once accumulation 0 (dK/dV: dV += P^T dO) has read P^T (dQ: once the compute warps have read
+// S), dP once the last accumulation has read dS.
 // Tiles outside the causal / window band are skipped (they contribute exact zeros).  Every wait
 // is bounded.
 #include <cudaTypedefs.h>
@@ -67,10 +67,10 @@ struct BwdCfg {
   static constexpr int OFF_LD = OFF_IN + NSTAGE * STAGE_BYTES;
   static constexpr int OFF_BAR = OFF_LD + NSTAGE * PAIRS * 16;
   // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE], s_full[NBUF] (S and dP issued:
-  // two arrivals), p_ready[NBUF], acc0_done (dV; single buffer only), acc_done[NBUF] (dK or dQ:
-  // the item's last accumulation), drain[3]
+  // two arrivals), p_ready[NBUF], acc0_done[NBUF] (dV), acc_done[NBUF] (dK or dQ: the item's last
+  // accumulation), drain[3]
   static constexpr int B_OUT = 0, B_IF = 1, B_IE = B_IF + NSTAGE, B_S = B_IE + NSTAGE;
-  static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + 1, B_DRAIN = B_D + NBUF;
+  static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + NBUF, B_DRAIN = B_D + NBUF;
   static constexpr int NBAR = B_DRAIN + 3;  // one drain barrier per MMA-issuing warp
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
@@ -154,8 +154,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       mbar_init(bar(C::B_S + b), 2);
       mbar_init(bar(C::B_P + b), 256);
       mbar_init(bar(C::B_D + b), 1);
+      mbar_init(bar(C::B_D0 + b), 1);
     }
-    mbar_init(bar(C::B_D0), 1);
     for (int i = 0; i < 3; ++i) mbar_init(bar(C::B_DRAIN + i), 1);
     *abort_flag = 0;
     mbar_init_fence();
@@ -308,16 +308,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           if (!ok) break;
           if (m >= NBUF) {
             const int n = m - NBUF;  // the item that used these columns before
-            if (NBUF == 2) {
-              // both S and dP columns are free once item n's accumulations have completed
-              ok = wait_all(C::B_D + b, (n / NBUF) & 1);
-            } else if (role == 0) {
+            const uint32_t par = (n / NBUF) & 1;
+            if (role == 0) {
               // S(m) overwrites the columns accumulation 0 (dK/dV) read P^T from; in dQ mode
-              // they were free as soon as the compute warps had loaded them
-              ok = MODE == kDkdv ? wait_all(C::B_D0, n & 1) : wait_all(C::B_P + b, n & 1);
+              // they are free as soon as the compute warps have loaded them
+              ok = MODE == kDkdv ? wait_all(C::B_D0 + b, par) : wait_all(C::B_P + b, par);
             } else {
               // dP(m) overwrites the dS the last accumulation reads
-              ok = wait_all(C::B_D + b, n & 1);
+              ok = wait_all(C::B_D + b, par);
             }
             if (!ok) break;
           }
@@ -334,7 +332,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           fence_after();
           if (MODE == kDkdv) {
             issue_acc0(n);
-            if (NBUF == 1) mma_commit_w(bar(C::B_D0));
+            mma_commit_w(bar(C::B_D0 + b));
           }
           issue_acc1(n);
           mma_commit_w(bar(C::B_D + b));
