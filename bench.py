@@ -319,41 +319,70 @@ def main():
     # end to end through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "dout", "cu_seqlens_q",
-                                                     "cu_seqlens_kv")}
-        hout = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for k, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-        dbuf = {k: torch.empty_like(x[k]) for k in host}
+        # End to end through the public API with pinned host buffers: every step uploads its
+        # inputs and reads back all of its results (out, lse, dq, dk, dv) inside the timed
+        # region.  Two device / host buffer sets and three streams pipeline the steps the way an
+        # input pipeline would: step k+1's upload and step k-1's read-back run on the copy
+        # engines while step k's kernels run.  (The bias, where a workload has one, stays
+        # resident like a weight.)
+        in_keys = ("q", "k", "v", "dout", "cu_seqlens_q", "cu_seqlens_kv")
+        res_like = {"out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        host = {k: x[k].cpu().pin_memory() for k in in_keys}
+        dset = [{k: torch.empty_like(x[k]) for k in in_keys} for _ in range(2)]
+        rset = [{k: torch.empty_like(t) for k, t in res_like.items()} for _ in range(2)]
+        hres = [{k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for k, t in res_like.items()} for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = sum(t.numel() * t.element_size() for t in hout.values())
+        d2h = sum(t.numel() * t.element_size() for t in hres[0].values())
+        s_up, s_cmp, s_dn = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        ev_up = [torch.cuda.Event() for _ in range(2)]
+        ev_cmp = [torch.cuda.Event() for _ in range(2)]
+        ev_dn = [torch.cuda.Event() for _ in range(2)]
+        for e in ev_cmp + ev_dn:
+            e.record(stream)  # both sets start free
+        torch.cuda.synchronize()
 
-        def e2e_step():
-            for k in host:
-                dbuf[k].copy_(host[k], non_blocking=True)
-            vlf.vlf_attn_varlen_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["cu_seqlens_q"],
-                                    dbuf["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv,
-                                    out=out, lse=lse, **kw)
-            vlf.vlf_attn_varlen_bwd(dbuf["dout"], dbuf["q"], dbuf["k"], dbuf["v"], out, lse,
-                                    dbuf["cu_seqlens_q"], dbuf["cu_seqlens_kv"], w.max_seqlen_q,
-                                    w.max_seqlen_kv, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
-            for k, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-                hout[k].copy_(t, non_blocking=True)
+        def e2e_step(step):
+            i = step % 2
+            d, r, h = dset[i], rset[i], hres[i]
+            with torch.cuda.stream(s_up):
+                s_up.wait_event(ev_cmp[i])  # the kernels of step - 2 are done with set i
+                for k in in_keys:
+                    d[k].copy_(host[k], non_blocking=True)
+                ev_up[i].record(s_up)
+            s_cmp.wait_event(ev_up[i])
+            s_cmp.wait_event(ev_dn[i])  # the read-back of step - 2 is done with set i
+            vlf.vlf_attn_varlen_fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_kv"],
+                                    w.max_seqlen_q, w.max_seqlen_kv, out=r["out"], lse=r["lse"],
+                                    stream=s_cmp, **kw)
+            vlf.vlf_attn_varlen_bwd(d["dout"], d["q"], d["k"], d["v"], r["out"], r["lse"],
+                                    d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q,
+                                    w.max_seqlen_kv, dq=r["dq"], dk=r["dk"], dv=r["dv"],
+                                    workspace=ws, stream=s_cmp, **kw)
+            ev_cmp[i].record(s_cmp)
+            with torch.cuda.stream(s_dn):
+                s_dn.wait_event(ev_cmp[i])
+                for k in res_like:
+                    h[k].copy_(r[k], non_blocking=True)
+                ev_dn[i].record(s_dn)
 
-        for _ in range(args.warmup):
-            e2e_step()
+        for it in range(args.warmup):
+            e2e_step(it)
+        torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        b.record(stream)
+        a.record(s_up)
+        for it in range(args.steps):
+            e2e_step(it)
+        b.record(s_dn)  # after the last read-back, which follows every other stream's work
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
         e2e = {"value": world * pairs * fpp["fwd_bwd"] / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms, "pipelined": "upload / kernels / read-back of consecutive "
+                                                   "steps overlap (3 streams, 2 buffer sets)"}
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_units > 0:
