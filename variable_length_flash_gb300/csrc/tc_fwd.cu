@@ -4,15 +4,20 @@
 // staged once, then for each K/V tile: S = Q K^T, online softmax (running max and sum with a
 // rescale), O += P V -- re-laid out for Blackwell:
 //
-//  * A CTA owns two 128-row query tiles of one sequence: consecutive row blocks of one head, or,
-//    when a kv head serves an even number of query heads (GQA), the same rows of two query
-//    heads that share K/V.  Each 64-key K/V tile brought into shared memory feeds both.
-//  * Warp roles (416 threads): warp 0 issues TMA loads (Q once, then K and V tiles into rings);
-//    warps 1, 10, 11 and 12 issue the MMAs (S and P.V of each query tile, one issuer per SM
-//    sub-partition), warp 1 also owns the TMEM allocation; warps 2-5 run the softmax of query
-//    tile 0 and warps 6-9 that of tile 1, one thread per query row (TMEM lane = row).
-//  * TMEM (512 columns): query tile t owns two 64-column S buffers at 128 t and 128 t + 64 and
-//    its O accumulator at 256 + 128 t.  KV tile n of a query tile lands in S buffer n mod 2, so
+//  * A CTA owns NT 128-row query tiles of one sequence.  NT = 1 (head widths 64 and 128): 256
+//    threads, 256 TMEM columns and under half the SM's shared memory, so two CTAs share an SM
+//    and one's prologue (Q load, first tile) and epilogue overlap the other's main loop -- this
+//    measured faster than sharing K/V between two tiles.  NT = 2 (QK width 192, whose tiles do
+//    not fit twice): consecutive row blocks of one head, or, when a kv head serves an even
+//    number of query heads (GQA), the same rows of two query heads that share K/V; each 64-key
+//    K/V tile brought into shared memory feeds both.
+//  * Warp roles.  NT = 2 (416 threads): warp 0 issues TMA loads (Q once, then K and V tiles
+//    into rings); four warps issue the MMAs, one per SM sub-partition (S and P.V of each query
+//    tile); warps 2-9 run the softmax, 2-5 for tile 0 and 6-9 for tile 1.  NT = 1 (256
+//    threads): warp 0 TMA, warp 1 S MMAs, warp 2 P.V MMAs, warps 4-7 softmax.  One thread per
+//    query row (TMEM lane = row); the S-issuing warp of tile 0 owns the TMEM allocation.
+//  * TMEM: query tile t owns two 64-column S buffers at 128 t and 128 t + 64 and its O
+//    accumulator at 128 NT + 128 t.  KV tile n of a query tile lands in S buffer n mod 2, so
 //    S(n+1) is computed while the softmax of S(n) runs and the softmax warps go from one tile
 //    to the next without waiting for the tensor core.  P(n) (16-bit) is written over the first
 //    32 columns of its S buffer and fed to the P.V MMA straight from TMEM; S(n+2) reuses the
@@ -49,30 +54,38 @@ struct FwdMaps {
   CUtensorMap q, k, v;
 };
 
-template <int DQK, int DV, int NK, int NV>
+// NT: query tiles per CTA.  NT = 2: 416 threads and all 512 TMEM columns, one CTA per SM.
+// NT = 1: 256 threads, 256 TMEM columns and at most half the SM's shared memory, so two CTAs
+// share an SM and one's prologue / epilogue overlaps the other's main loop.
+template <int DQK, int DV, int NK, int NV, int NT>
 struct FwdCfg {
   static constexpr int KBQ = DQK / 64, KBV = DV / 64;  // 64-column (128-byte) swizzle blocks
   static constexpr int QBLK = 128 * 128;               // one 128-row x 64-col block of Q
   static constexpr int KVBLK = kBN * 128;              // one 64-row x 64-col block of K or V
   static constexpr int Q_BYTES = KBQ * QBLK, K_BYTES = KBQ * KVBLK, V_BYTES = KBV * KVBLK;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + NT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NK * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * V_BYTES;
   // barriers: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], then per query tile t
   // and S buffer b (index 2 t + b): s_full, p_full, o_done (the P.V that read buffer b); drain
   // (one per MMA-issuing warp)
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NK, B_VF = B_KE + NK, B_VE = B_VF + NV;
-  static constexpr int B_S = B_VE + NV, B_P = B_S + 4, B_O = B_P + 4, B_DRAIN = B_O + 4;
-  static constexpr int NBAR = B_DRAIN + 4;  // one drain barrier per MMA-issuing warp
+  static constexpr int B_S = B_VE + NV, B_P = B_S + 2 * NT, B_O = B_P + 2 * NT;
+  static constexpr int B_DRAIN = B_O + 2 * NT;
+  static constexpr int NBAR = B_DRAIN + 2 * NT;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
-  static constexpr int THREADS = 416;
-  // the MMA warp needs K three tiles ahead of V: with fewer than 3 V stages the producer would
-  // wait for a V slot the MMA warp frees only after it has the K tile it is waiting for
-  static_assert(NV >= 3 && NK >= 3, "ring depth");
+  static constexpr int THREADS = NT == 2 ? 416 : 256;
+  // TMEM: query tile t's two 64-column S buffers at 128 t, its O at O_COL + 128 t
+  static constexpr uint32_t TMEM_COLS = 256 * NT, O_COL = 128 * NT;
+  // The producer issues K(j + LEAD) before V(j).  A K or V tile waits for its ring slot; with
+  // one query tile a K load must not queue behind a V slot that frees late, so K leads by one.
+  static constexpr int LEAD = NT == 1 ? 1 : 0;
+  static_assert(NT == 1 || NT == 2, "query tiles per CTA");
+  static_assert(NV >= 2 && NK >= 2, "ring depth");
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "tile shapes");
-  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(SMEM <= (NT == 2 ? 232448 : 115712), "shared memory");
 };
 
 // Time-bounded wait that ignores the abort flag (used to drain in-flight work at teardown).
@@ -89,11 +102,14 @@ struct TileInfo {
   int lo, hi;          // union
 };
 
+// Query tiles of CTA (bx, by): NT = 2 takes two row blocks of one head, or the same rows of two
+// heads sharing a kv head (pair_heads); NT = 1 one row block.  Tile 1 of an NT = 1 CTA is empty.
+template <int NT>
 __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx, int by,
                                           bool pair_heads, TileInfo &ti) {
   for (int t = 0; t < 2; ++t) {
-    ti.row0[t] = pair_heads ? bx * 128 : bx * 256 + 128 * t;
-    ti.head[t] = pair_heads ? 2 * by + t : by;
+    ti.row0[t] = NT == 1 ? (t == 0 ? bx * 128 : sq.q_len) : (pair_heads ? bx * 128 : bx * 256 + 128 * t);
+    ti.head[t] = NT == 1 ? by : (pair_heads ? 2 * by + t : by);
     int jl = 0, jh = 0;
     if (ti.row0[t] < sq.q_len && sq.kv_len > 0) {
       int klo, khi;
@@ -121,12 +137,12 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
 
 // BF16: element type of Q/K/V/O (bf16, else fp16), fixed at compile time so the per-element
 // conversions carry no runtime branch.
-template <int DQK, int DV, int NK, int NV, bool BF16>
-__global__ void __launch_bounds__(416, 1)
+template <int DQK, int DV, int NK, int NV, int NT, bool BF16>
+__global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, NT == 1 ? 2 : 1)
 tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
-  using C = FwdCfg<DQK, DV, NK, NV>;
+  using C = FwdCfg<DQK, DV, NK, NV, NT>;
   extern __shared__ uint8_t smem_raw[];
-  const bool pair_heads = (p.group % 2 == 0);
+  const bool pair_heads = NT == 2 && (p.group % 2 == 0);
   const int s = blockIdx.z;
   Seq sq;
   if (!load_seq(p, s, sq)) return;
@@ -136,7 +152,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   // heavy (late, long-band) row blocks first under causal masking
   const int bx = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
   TileInfo ti;
-  tile_info(p, sq, bx, blockIdx.y, pair_heads, ti);
+  tile_info<NT>(p, sq, bx, blockIdx.y, pair_heads, ti);
   if (ti.row0[0] >= sq.q_len) return;  // whole CTA beyond this sequence
 
   const uint32_t raw = smem_u32(smem_raw);
@@ -152,9 +168,9 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_Q), 1);
     // a K or V slot is free once both query tiles' issuers have released it
-    for (int i = 0; i < NK; ++i) { mbar_init(bar(C::B_KF + i), 1); mbar_init(bar(C::B_KE + i), 2); }
-    for (int i = 0; i < NV; ++i) { mbar_init(bar(C::B_VF + i), 1); mbar_init(bar(C::B_VE + i), 2); }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < NK; ++i) { mbar_init(bar(C::B_KF + i), 1); mbar_init(bar(C::B_KE + i), NT); }
+    for (int i = 0; i < NV; ++i) { mbar_init(bar(C::B_VF + i), 1); mbar_init(bar(C::B_VE + i), NT); }
+    for (int i = 0; i < 2 * NT; ++i) {
       mbar_init(bar(C::B_S + i), 1);
       mbar_init(bar(C::B_P + i), 128);
       mbar_init(bar(C::B_O + i), 1);
@@ -164,7 +180,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     mbar_init_fence();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
     tmem_relinquish();
   }
   fence_before();
@@ -192,23 +208,28 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       }
       int k_issued[NK] = {0}, v_issued[NV] = {0};
       bool ok = true;
-      for (int j = lo; j < hi && ok; ++j) {
-        const int it = j - lo;
-        const int ks = it % NK, vs = it % NV;
-        if (it >= NK) ok = mbar_wait(bar(C::B_KE + ks), ((it / NK) - 1) & 1, abort_flag, p.err);
-        if (!ok) break;
-        mbar_expect_tx(bar(C::B_KF + ks), C::K_BYTES);
-        for (int c = 0; c < C::KBQ; ++c)
-          tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, &maps.k, hk * DQK + 64 * c,
-                      sq.k0 + j * kBN, bar(C::B_KF + ks));
-        ++k_issued[ks];
-        if (it >= NV) ok = mbar_wait(bar(C::B_VE + vs), ((it / NV) - 1) & 1, abort_flag, p.err);
-        if (!ok) break;
-        mbar_expect_tx(bar(C::B_VF + vs), C::V_BYTES);
-        for (int c = 0; c < C::KBV; ++c)
-          tma_load_2d(sV + vs * C::V_BYTES + c * C::KVBLK, &maps.v, hk * DV + 64 * c,
-                      sq.k0 + j * kBN, bar(C::B_VF + vs));
-        ++v_issued[vs];
+      for (int j = lo; j < hi + C::LEAD && ok; ++j) {
+        const int kj = j, vj = j - C::LEAD;  // K tile issued ahead of V by LEAD
+        if (kj < hi) {
+          const int it = kj - lo, ks = it % NK;
+          if (it >= NK) ok = mbar_wait(bar(C::B_KE + ks), ((it / NK) - 1) & 1, abort_flag, p.err);
+          if (!ok) break;
+          mbar_expect_tx(bar(C::B_KF + ks), C::K_BYTES);
+          for (int c = 0; c < C::KBQ; ++c)
+            tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, &maps.k, hk * DQK + 64 * c,
+                        sq.k0 + kj * kBN, bar(C::B_KF + ks));
+          ++k_issued[ks];
+        }
+        if (vj >= lo) {
+          const int it = vj - lo, vs = it % NV;
+          if (it >= NV) ok = mbar_wait(bar(C::B_VE + vs), ((it / NV) - 1) & 1, abort_flag, p.err);
+          if (!ok) break;
+          mbar_expect_tx(bar(C::B_VF + vs), C::V_BYTES);
+          for (int c = 0; c < C::KBV; ++c)
+            tma_load_2d(sV + vs * C::V_BYTES + c * C::KVBLK, &maps.v, hk * DV + 64 * c,
+                        sq.k0 + vj * kBN, bar(C::B_VF + vs));
+          ++v_issued[vs];
+        }
       }
       // make sure no copy is still landing in shared memory when the CTA leaves
       drain_wait(bar(C::B_Q), 0);
@@ -217,7 +238,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       for (int i = 0; i < NV; ++i)
         if (v_issued[i]) drain_wait(bar(C::B_VF + i), (v_issued[i] - 1) & 1);
     }
-  } else if (warp == 1 || warp >= 10) {
+  } else if (NT == 2 ? (warp == 1 || warp >= 10) : (warp == 1 || warp == 2)) {
     // ------------------------------------------------------------------ MMA issuers
     // Four warps issue MMAs, one per SM sub-partition: S = Q K^T of query tile 0 (warp 1) and
     // tile 1 (warp 11), O += P V of tile 0 (warp 12) and tile 1 (warp 10).  An MMA issue returns
@@ -227,9 +248,10 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     // over the softmax warps.  Each issuer walks every KV tile of the CTA's range (to release
     // its share of the K or V ring slot) and issues the MMAs of its own query tile; it runs its
     // loop as a whole warp (uniform operands) and elect.sync picks the issuing lane.
-    const bool is_s = warp == 1 || warp == 11;
-    const int t = (warp == 1 || warp == 12) ? 0 : 1;
-    const int drain = C::B_DRAIN + (warp == 1 ? 0 : warp - 9);
+    // NT = 1: warp 1 issues S, warp 2 P.V
+    const bool is_s = NT == 2 ? (warp == 1 || warp == 11) : warp == 1;
+    const int t = NT == 2 ? ((warp == 1 || warp == 12) ? 0 : 1) : 0;
+    const int drain = C::B_DRAIN + (NT == 2 ? (warp == 1 ? 0 : warp - 9) : warp - 1);
     if (hi > lo) {
       const int jlo = ti.jlo[t], jhi = ti.jhi[t];
       bool ok = true;
@@ -282,7 +304,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
             const uint32_t pcol = tmem + 128 * t + 64 * b;
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts_w(tmem + 256 + 128 * t, pcol + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), id_o,
+              mma_ts_w(tmem + C::O_COL + 128 * t, pcol + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), id_o,
                        (n > 0 || kk > 0) ? 1u : 0u);
             mma_commit_w(bar(C::B_O + 2 * t + b));
           }
@@ -293,9 +315,10 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       mma_commit_w(bar(drain));
       drain_wait(bar(drain), 0);
     }
-  } else {
+  } else if (NT == 2 || warp >= 4) {
     // ------------------------------------------------------------------ softmax / epilogue
-    const int t = (warp - 2) >> 2;
+    // (NT = 2: warps 2-9; NT = 1: warps 4-7, warp 3 has no role)
+    const int t = NT == 2 ? (warp - 2) >> 2 : 0;
     const int quarter = warp & 3;
     const int r = 32 * quarter + lane;
     const int i = ti.row0[t] + r;  // sequence-local query row
@@ -303,7 +326,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     const int off = sq.kv_len - sq.q_len;
     const int head = ti.head[t];
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-    const uint32_t s_addr = lane_addr + 128 * t, o_addr = lane_addr + 256 + 128 * t;
+    const uint32_t s_addr = lane_addr + 128 * t, o_addr = lane_addr + C::O_COL + 128 * t;
     const float sl2 = p.scale_log2;
     const float *brow = nullptr;
     if (p.bias && row_ok) {
@@ -499,7 +522,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   __syncthreads();
   if (warp == 1) {
     fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -543,9 +566,9 @@ bool tc_forward_supported(const Params &p) {
 }
 
 namespace {
-template <int DQK, int DV, int NK, int NV>
+template <int DQK, int DV, int NK, int NV, int NT>
 cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
-  using C = FwdCfg<DQK, DV, NK, NV>;
+  using C = FwdCfg<DQK, DV, NK, NV, NT>;
   FwdMaps maps;
   const int bf = p.dtype == VLF_BF16;
   if (p.total_q == 0 || p.total_kv == 0) return simt_forward(p, st);  // nothing to stage
@@ -553,12 +576,12 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
       !make_tmap_16bit(&maps.k, p.k, p.total_kv, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, kBN, bf) ||
       !make_tmap_16bit(&maps.v, p.v, p.total_kv, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, kBN, bf))
     return cudaErrorInvalidValue;
-  const bool pair_heads = (p.group % 2 == 0);
-  const int rows_per_cta = pair_heads ? 128 : 256;
+  const bool pair_heads = NT == 2 && (p.group % 2 == 0);
+  const int rows_per_cta = NT == 1 || pair_heads ? 128 : 256;
   const dim3 grid((p.max_q + rows_per_cta - 1) / rows_per_cta, pair_heads ? p.h_q / 2 : p.h_q,
                   p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  auto kern = bf ? tc_fwd_kernel<DQK, DV, NK, NV, true> : tc_fwd_kernel<DQK, DV, NK, NV, false>;
+  auto kern = bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true> : tc_fwd_kernel<DQK, DV, NK, NV, NT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(maps, p);
@@ -569,9 +592,9 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
 }  // namespace
 
 cudaError_t tc_forward(const Params &p, cudaStream_t st) {
-  if (p.d_qk == 64) return launch_fwd<64, 64, 6, 6>(p, st);
-  if (p.d_qk == 128) return launch_fwd<128, 128, 4, 4>(p, st);
-  return launch_fwd<192, 128, 3, 3>(p, st);
+  if (p.d_qk == 64) return launch_fwd<64, 64, 3, 3, 1>(p, st);
+  if (p.d_qk == 128) return launch_fwd<128, 128, 2, 2, 1>(p, st);
+  return launch_fwd<192, 128, 3, 3, 2>(p, st);
 }
 
 }  // namespace vlf
