@@ -46,7 +46,10 @@ namespace {
 using namespace tc;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kDkdv = 0, kDq = 1;
+// kDq keeps dS in the dP columns and double-buffers S and dP; kDqS writes dS over the S columns
+// instead, so the single dP buffer is free as soon as the compute warps have loaded it and the
+// next item's dP can run during this item's elementwise pass (S stays double-buffered).
+constexpr int kDkdv = 0, kDq = 1, kDqS = 2;
 
 struct BwdMaps {
   CUtensorMap outer0, outer1, inner0, inner1;
@@ -54,37 +57,46 @@ struct BwdMaps {
 
 // outer0/outer1: K, V (dK/dV) or Q, dO (dQ), 128 rows.  inner0/inner1: Q, dO (dK/dV) or K, V
 // (dQ), IR rows per item.
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE>
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1>
 struct BwdCfg {
   static constexpr int KB0 = DQK / 64, KB1 = DV / 64;  // 64-col blocks of tensors 0 / 1
   static constexpr int OBLK = 128 * 128, IBLK = IR * 128;  // bytes per 64-col block
   static constexpr int O0_BYTES = KB0 * OBLK, O1_BYTES = KB1 * OBLK;
   static constexpr int I0_BYTES = KB0 * IBLK, I1_BYTES = KB1 * IBLK;
-  static constexpr int STAGE_BYTES = I0_BYTES + I1_BYTES;
-  static constexpr int OFF_O0 = 0, OFF_O1 = O0_BYTES, OFF_IN = O0_BYTES + O1_BYTES;
-  // per stage: the item's IR columns as IR/2 pairs {-LSE2_c, -LSE2_c+1, -D_c, -D_c+1} (dK/dV)
-  static constexpr int PAIRS = IR / 2;
-  static constexpr int OFF_LD = OFF_IN + NSTAGE * STAGE_BYTES;
+  // two rings of inner tiles: ring 0 (Q for dK/dV, K for dQ; NSTAGE slots) and ring 1 (dO for
+  // dK/dV, V for dQ; NSTAGE1 slots), each slot released as soon as its last reader is done
+  static constexpr int OFF_O0 = 0, OFF_O1 = O0_BYTES, OFF_IN0 = O0_BYTES + O1_BYTES;
+  static constexpr int OFF_IN1 = OFF_IN0 + NSTAGE * I0_BYTES;
+  // per ring-0 slot: the item's IR columns as IR/2 pairs {-LSE2_c, -LSE2_c+1, -D_c, -D_c+1}
+  // (dK/dV only)
+  static constexpr int PAIRS = MODE == kDkdv ? IR / 2 : 0;
+  static constexpr int OFF_LD = OFF_IN1 + NSTAGE1 * I1_BYTES;
   static constexpr int OFF_BAR = OFF_LD + NSTAGE * PAIRS * 16;
-  // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE], s_full[NBUF] (S and dP issued:
+  // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE] (ring 0), in1_full[NSTAGE1],
+  // in1_empty[NSTAGE1] (ring 1), s_full[NBUF] (S and dP issued:
   // two arrivals), p_ready[NBUF], acc0_done[NBUF] (dV), acc_done[NBUF] (dK or dQ: the item's last
-  // accumulation), drain[3]
-  static constexpr int B_OUT = 0, B_IF = 1, B_IE = B_IF + NSTAGE, B_S = B_IE + NSTAGE;
+  // accumulation), drain[3] (one per MMA-issuing warp), dp_free (kDqS)
+  static constexpr int B_OUT = 0, B_IF = 1, B_IE = B_IF + NSTAGE, B_IF1 = B_IE + NSTAGE;
+  static constexpr int B_IE1 = B_IF1 + NSTAGE1, B_S = B_IE1 + NSTAGE1;
   static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + NBUF, B_DRAIN = B_D + NBUF;
-  static constexpr int NBAR = B_DRAIN + 3;  // one drain barrier per MMA-issuing warp
+  static constexpr int B_PF = B_DRAIN + 3;  // kDqS: the compute warps have loaded dP
+  static constexpr int NBAR = B_PF + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
-  // TMEM: accumulators first, then NBUF x (S IR cols, dP IR cols)
+  // TMEM: accumulators first, then NBUF x (S IR cols, dP IR cols); kDqS: NBUF S buffers, then
+  // one dP buffer
   static constexpr uint32_t ACC0 = 0;    // dV (dK/dV) or dQ (dQ)
   static constexpr uint32_t ACC1 = 128;  // dK (dK/dV)
-  static constexpr uint32_t BUF = MODE == kDkdv ? 128 + DQK : 256;
+  static constexpr uint32_t BUF = MODE == kDkdv ? 128 + DQK : (MODE == kDqS ? DQK : 256);
+  __host__ __device__ static constexpr uint32_t s_col(int b) { return MODE == kDqS ? BUF + IR * b : BUF + 2 * IR * b; }
+  __host__ __device__ static constexpr uint32_t dp_col(int b) { return MODE == kDqS ? BUF + NBUF * IR : BUF + 2 * IR * b + IR; }
   static constexpr int HALF = IR / 2;      // columns per compute warpgroup
   static constexpr int CHUNKS = HALF / 32;  // 32-column chunks per compute thread
-  static_assert(BUF + NBUF * 2 * IR <= 512, "TMEM columns");
+  static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * 2 * IR) <= 512, "TMEM columns");
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(DV <= 128 && DQK <= 256 && DQK % 64 == 0 && DV % 64 == 0, "head widths");
   static_assert(IR == 64 || IR == 128, "item rows");
-  static_assert(NBUF == 1 || IR == 64, "double buffering only with 64-row items");
+  static_assert(NBUF == 1 || IR == 64 || MODE == kDqS, "double buffering only with 64-row items");
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -96,10 +108,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 // BF16: element type of the 16-bit tensors (bf16, else fp16), fixed at compile time so the
 // per-element conversions carry no runtime branch.
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, bool BF16>
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, bool BF16>
 __global__ void __launch_bounds__(384, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
-  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE>;
+  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1>;
   extern __shared__ uint8_t smem_raw[];
   const int s = blockIdx.z;
   Seq sq;
@@ -138,7 +150,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
-  const uint32_t sO0 = base + C::OFF_O0, sO1 = base + C::OFF_O1, sIn = base + C::OFF_IN;
+  const uint32_t sO0 = base + C::OFF_O0, sO1 = base + C::OFF_O1;
+  const uint32_t sIn0 = base + C::OFF_IN0, sIn1 = base + C::OFF_IN1;
   float4 *ldbuf = reinterpret_cast<float4 *>(gbase + C::OFF_LD);  // [stage][IR/2 column pairs]
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -150,6 +163,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     // in_full: the TMA bytes plus 33 arrivals (lane 0's expect_tx and every producer lane after
     // writing its LSE / D pairs); p_ready: all 256 compute threads
     for (int i = 0; i < NSTAGE; ++i) { mbar_init(bar(C::B_IF + i), 33); mbar_init(bar(C::B_IE + i), 1); }
+    for (int i = 0; i < NSTAGE1; ++i) { mbar_init(bar(C::B_IF1 + i), 1); mbar_init(bar(C::B_IE1 + i), 1); }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(bar(C::B_S + b), 2);
       mbar_init(bar(C::B_P + b), 256);
@@ -157,6 +171,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       mbar_init(bar(C::B_D0 + b), 1);
     }
     for (int i = 0; i < 3; ++i) mbar_init(bar(C::B_DRAIN + i), 1);
+    mbar_init(bar(C::B_PF), 256);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -190,9 +205,9 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         for (int c = 0; c < C::KB1; ++c)
           tma_load_2d(sO1 + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
       }
-      int issued[NSTAGE] = {0};
+      int issued0[NSTAGE] = {0}, issued1[NSTAGE1] = {0};
       for (int n = 0; n < n_items; ++n) {
-        const int st = n % NSTAGE;
+        const int st = n % NSTAGE, st1 = n % NSTAGE1;
         if (n >= NSTAGE) {
           bool w = true;
           if (lane == 0) w = mbar_wait(bar(C::B_IE + st), ((n / NSTAGE) - 1) & 1, abort_flag, p.err);
@@ -220,24 +235,35 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             ldbuf[st * C::PAIRS + lane + 32 * pp] = make_float4(nl[0], nl[1], nd[0], nd[1]);
           }
         }
+        const int ih = MODE == kDkdv ? item_head(n) : hk;  // head inside the inner tensors
+        const int irow = (MODE == kDkdv ? sq.q0 : sq.k0) + item_row(n);
         if (lane == 0) {
-          const int ih = MODE == kDkdv ? item_head(n) : hk;  // head inside the inner tensors
-          const int irow = (MODE == kDkdv ? sq.q0 : sq.k0) + item_row(n);
-          const uint32_t dst = sIn + st * C::STAGE_BYTES;
-          mbar_expect_tx(bar(C::B_IF + st), C::STAGE_BYTES);
+          mbar_expect_tx(bar(C::B_IF + st), C::I0_BYTES);
           for (int c = 0; c < C::KB0; ++c)
-            tma_load_2d(dst + c * C::IBLK, &maps.inner0, ih * DQK + 64 * c, irow, bar(C::B_IF + st));
-          for (int c = 0; c < C::KB1; ++c)
-            tma_load_2d(dst + C::I0_BYTES + c * C::IBLK, &maps.inner1, ih * DV + 64 * c, irow,
+            tma_load_2d(sIn0 + st * C::I0_BYTES + c * C::IBLK, &maps.inner0, ih * DQK + 64 * c, irow,
                         bar(C::B_IF + st));
-          ++issued[st];
+          ++issued0[st];
         }
         mbar_arrive(bar(C::B_IF + st));
+        bool w1 = true;
+        if (lane == 0) {
+          if (n >= NSTAGE1) w1 = mbar_wait(bar(C::B_IE1 + st1), ((n / NSTAGE1) - 1) & 1, abort_flag, p.err);
+          if (w1) {
+            mbar_expect_tx(bar(C::B_IF1 + st1), C::I1_BYTES);
+            for (int c = 0; c < C::KB1; ++c)
+              tma_load_2d(sIn1 + st1 * C::I1_BYTES + c * C::IBLK, &maps.inner1, ih * DV + 64 * c, irow,
+                          bar(C::B_IF1 + st1));
+            ++issued1[st1];
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, (int)w1, 0)) break;
       }
       if (lane == 0) {
         drain_wait(bar(C::B_OUT), 0);
         for (int i = 0; i < NSTAGE; ++i)
-          if (issued[i]) drain_wait(bar(C::B_IF + i), (issued[i] - 1) & 1);
+          if (issued0[i]) drain_wait(bar(C::B_IF + i), (issued0[i] - 1) & 1);
+        for (int i = 0; i < NSTAGE1; ++i)
+          if (issued1[i]) drain_wait(bar(C::B_IF1 + i), (issued1[i] - 1) & 1);
       }
     }
   } else if (warp == 1 || warp >= 10) {
@@ -257,9 +283,10 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // descriptors are built once; a K step adds its byte offset / 16 to the start-address
       // field (shared addresses stay far below the field's 2^18-byte range, so nothing carries)
       const uint64_t d_o0 = sdesc_sw128(sO0, 16, 1024), d_o1 = sdesc_sw128(sO1, 16, 1024);
-      auto s_cols = [&](int n) { return tmem + C::BUF + 2 * IR * (n % NBUF); };
+      auto s_cols = [&](int n) { return tmem + C::s_col(n % NBUF); };
+      auto dp_cols = [&](int n) { return tmem + C::dp_col(n % NBUF); };
       auto issue_s = [&](int n) {  // S (dK/dV: S^T) of item n
-        const uint64_t d_i0 = sdesc_sw128(sIn + (n % NSTAGE) * C::STAGE_BYTES, 16, 1024);
+        const uint64_t d_i0 = sdesc_sw128(sIn0 + (n % NSTAGE) * C::I0_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
@@ -267,11 +294,11 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         }
       };
       auto issue_dp = [&](int n) {  // dP (dK/dV: dP^T) of item n
-        const uint64_t d_i1 = sdesc_sw128(sIn + (n % NSTAGE) * C::STAGE_BYTES + C::I0_BYTES, 16, 1024);
+        const uint64_t d_i1 = sdesc_sw128(sIn1 + (n % NSTAGE1) * C::I1_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss_w(s_cols(n) + IR, d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
+          mma_ss_w(dp_cols(n), d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
         }
       };
       // the 16-bit A operand of K step kk (16 inner rows) sits in the first half of the 32-column
@@ -279,7 +306,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       auto a_col = [](int kk) { return (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1)); };
       // accumulation 0 (dV += P^T dO) -- dK/dV only
       auto issue_acc0 = [&](int n) {
-        const uint64_t d_i1 = sdesc_sw128(sIn + (n % NSTAGE) * C::STAGE_BYTES + C::I0_BYTES, C::IBLK, 1024);
+        const uint64_t d_i1 = sdesc_sw128(sIn1 + (n % NSTAGE1) * C::I1_BYTES, C::IBLK, 1024);
 #pragma unroll
         for (int kk = 0; kk < IR / 16; ++kk)
           mma_ts_w(tmem + C::ACC0, s_cols(n) + a_col(kk), d_i1 + (uint64_t)((kk * 2048) >> 4), id_a0,
@@ -287,13 +314,13 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       };
       // last accumulation: dK += dS^T Q (dK/dV) or dQ += dS K (dQ)
       auto issue_acc1 = [&](int n) {
-        const uint64_t d_i0 = sdesc_sw128(sIn + (n % NSTAGE) * C::STAGE_BYTES, C::IBLK, 1024);
+        const uint64_t d_i0 = sdesc_sw128(sIn0 + (n % NSTAGE) * C::I0_BYTES, C::IBLK, 1024);
         const uint32_t acc = MODE == kDkdv ? C::ACC1 : C::ACC0;
         const uint32_t id = MODE == kDkdv ? id_a1 : id_a0;
 #pragma unroll
         for (int kk = 0; kk < IR / 16; ++kk)
-          mma_ts_w(tmem + acc, s_cols(n) + IR + a_col(kk), d_i0 + (uint64_t)((kk * 2048) >> 4), id,
-                   (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tmem + acc, (MODE == kDqS ? s_cols(n) : dp_cols(n)) + a_col(kk),
+                   d_i0 + (uint64_t)((kk * 2048) >> 4), id, (n > 0 || kk > 0) ? 1u : 0u);
       };
       auto wait_all = [&](int b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar(b), parity, abort_flag, p.err));
@@ -304,25 +331,34 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         ok = wait_all(C::B_OUT, 0);
         for (int m = 0; m < n_items && ok; ++m) {
           const int b = m % NBUF;
-          ok = wait_all(C::B_IF + m % NSTAGE, (m / NSTAGE) & 1);
+          // S reads ring 0 (Q or K), dP reads ring 1 (dO or V)
+          ok = role == 0 ? wait_all(C::B_IF + m % NSTAGE, (m / NSTAGE) & 1)
+                         : wait_all(C::B_IF1 + m % NSTAGE1, (m / NSTAGE1) & 1);
           if (!ok) break;
-          if (m >= NBUF) {
+          if (MODE == kDqS && role == 1) {
+            // the single dP buffer is free once the compute warps have loaded item m-1's dP
+            if (m >= 1) ok = wait_all(C::B_PF, (m - 1) & 1);
+          } else if (m >= NBUF) {
             const int n = m - NBUF;  // the item that used these columns before
             const uint32_t par = (n / NBUF) & 1;
             if (role == 0) {
-              // S(m) overwrites the columns accumulation 0 (dK/dV) read P^T from; in dQ mode
-              // they are free as soon as the compute warps have loaded them
-              ok = MODE == kDkdv ? wait_all(C::B_D0 + b, par) : wait_all(C::B_P + b, par);
+              // S(m) overwrites the columns accumulation 0 (dK/dV) read P^T from; kDq: they are
+              // free as soon as the compute warps have loaded them; kDqS: once the dQ
+              // accumulation has read the dS written there
+              ok = MODE == kDkdv ? wait_all(C::B_D0 + b, par)
+                                 : (MODE == kDq ? wait_all(C::B_P + b, par) : wait_all(C::B_D + b, par));
             } else {
               // dP(m) overwrites the dS the last accumulation reads
               ok = wait_all(C::B_D + b, par);
             }
-            if (!ok) break;
           }
+          if (!ok) break;
           fence_after();
           if (role == 0) issue_s(m);
           else issue_dp(m);
           mma_commit_w(bar(C::B_S + b));
+          // dQ: V (ring 1) has no reader after dP
+          if (MODE != kDkdv && role == 1) mma_commit_w(bar(C::B_IE1 + m % NSTAGE1));
         }
       } else {
         for (int n = 0; n < n_items && ok; ++n) {
@@ -333,6 +369,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           if (MODE == kDkdv) {
             issue_acc0(n);
             mma_commit_w(bar(C::B_D0 + b));
+            mma_commit_w(bar(C::B_IE1 + n % NSTAGE1));  // dO (ring 1) has no reader after dV
           }
           issue_acc1(n);
           mma_commit_w(bar(C::B_D + b));
@@ -359,7 +396,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     if (!orow_ok) vis_hi = vis_lo;
     float row_nl = -INFINITY, row_nd = 0.f;  // dQ: this row's -LSE (base 2) and -D
     const float *brow_dq = nullptr;
-    if (MODE == kDq && orow_ok) {
+    if (MODE != kDkdv && orow_ok) {
       const size_t gi = (size_t)head_outer * p.total_q + sq.q0 + orow;
       const float L = p.lse[gi];
       row_nl = L == -INFINITY ? -INFINITY : -L * kLog2e;
@@ -389,7 +426,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       for (int ch = 0; ch < C::CHUNKS; ++ch) {
         const int col0 = C::HALF * half + 32 * ch;  // this chunk's first column in the item
         const int i0 = item_row(n) + col0;          // its first inner row
-        const uint32_t s_addr = lane_addr + C::BUF + 2 * IR * b + col0, dp_addr = s_addr + IR;
+        const uint32_t s_addr = lane_addr + C::s_col(b) + col0, dp_addr = lane_addr + C::dp_col(b) + col0;
         uint32_t sv[32], dv[32];
         __syncwarp();
         tmem_ld32(s_addr, sv);
@@ -408,6 +445,11 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         plain = plain && p.bias == nullptr;
         const float4 *lp = ldbuf + st * C::PAIRS + col0 / 2;  // this chunk's 16 pairs (dK/dV)
         tmem_ld_wait();
+        if (MODE == kDqS && ch == C::CHUNKS - 1) {
+          // every dP column of the item is in registers: the next dP may overwrite them
+          fence_before();
+          mbar_arrive(bar(C::B_PF));
+        }
         uint32_t pk[16], dk[16];
         if (plain) {
           // every pair visible, no bias: P = 2^(S log2e scale - LSE2), dS = P (dP - D)
@@ -453,7 +495,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         }
         __syncwarp();
         if (MODE == kDkdv) tmem_st16(s_addr, pk);
-        tmem_st16(dp_addr, dk);
+        tmem_st16(MODE == kDqS ? s_addr : dp_addr, dk);
       }
       tmem_st_wait();
       fence_before();
@@ -513,9 +555,9 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   }
 }
 
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE>
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1>
 cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
-  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE>;
+  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1>;
   const int bf = p.dtype == VLF_BF16;
   BwdMaps m;
   const uint64_t tq = p.total_q, tk = p.total_kv;
@@ -535,8 +577,8 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   const dim3 grid(MODE == kDkdv ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128,
                   MODE == kDkdv ? p.h_kv : p.h_q, p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  auto kern = bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, true>
-                 : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, false>;
+  auto kern = bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true>
+                 : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, C::SMEM, st>>>(m, p);
@@ -546,16 +588,18 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
 }
 
 // Per head width: item rows, buffers and stages of the dK/dV kernel (IR_KV, NBUF_KV, NST_KV)
-// and of the dQ kernel (IR_Q, NBUF_Q, NST_Q).
-template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int IR_Q, int NBUF_Q, int NST_Q>
+// and the mode, item rows, buffers and ring-0 / ring-1 stages of the dQ kernel (MODE_Q, IR_Q,
+// NBUF_Q, NST_Q, NST1_Q).
+template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int MODE_Q, int IR_Q, int NBUF_Q,
+          int NST_Q, int NST1_Q>
 cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   cudaError_t e;
   if ((e = mark(ev, 0, st)) != cudaSuccess) return e;
   if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV, NST_KV>(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDq, DQK, DV, IR_Q, NBUF_Q, NST_Q>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<MODE_Q, DQK, DV, IR_Q, NBUF_Q, NST_Q, NST1_Q>(p, st)) != cudaSuccess) return e;
   return mark(ev, 3, st);
 }
 
@@ -569,9 +613,9 @@ bool tc_backward_supported(const Params &p) {
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   if (p.total_q == 0 || p.total_kv == 0) return simt_backward(p, st, ev);
-  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 3, 64, 2, 3>(p, st, ev);
-  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 3, 64, 2, 3>(p, st, ev);
-  return bwd_shape<192, 128, 64, 1, 3, 64, 2, 3>(p, st, ev);
+  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 3, kDqS, 128, 2, 3, 3>(p, st, ev);
+  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 3, kDqS, 128, 2, 3, 2>(p, st, ev);
+  return bwd_shape<192, 128, 64, 1, 3, kDq, 64, 2, 3, 3>(p, st, ev);
 }
 
 // The tensor-core backward writes dQ directly (no fp32 accumulator); only the row dot
