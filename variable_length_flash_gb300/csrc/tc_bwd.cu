@@ -587,17 +587,18 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   return e;
 }
 
-// Per head width: item rows, buffers and stages of the dK/dV kernel (IR_KV, NBUF_KV, NST_KV)
-// and the mode, item rows, buffers and ring-0 / ring-1 stages of the dQ kernel (MODE_Q, IR_Q,
-// NBUF_Q, NST_Q, NST1_Q).
-template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int MODE_Q, int IR_Q, int NBUF_Q,
-          int NST_Q, int NST1_Q>
+// Per head width: item rows, buffers and ring-0 / ring-1 stages of the dK/dV kernel (IR_KV,
+// NBUF_KV, NST_KV, NST1_KV) and the mode, item rows, buffers and ring stages of the dQ kernel
+// (MODE_Q, IR_Q, NBUF_Q, NST_Q, NST1_Q).  A ring slot is refilled only after its item's last
+// product has read it, so the rings are as deep as shared memory allows.
+template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int NST1_KV, int MODE_Q, int IR_Q,
+          int NBUF_Q, int NST_Q, int NST1_Q>
 cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   cudaError_t e;
   if ((e = mark(ev, 0, st)) != cudaSuccess) return e;
   if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV, NST_KV>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV, NST1_KV>(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
   if ((e = launch_bwd<MODE_Q, DQK, DV, IR_Q, NBUF_Q, NST_Q, NST1_Q>(p, st)) != cudaSuccess) return e;
   return mark(ev, 3, st);
@@ -613,9 +614,9 @@ bool tc_backward_supported(const Params &p) {
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   if (p.total_q == 0 || p.total_kv == 0) return simt_backward(p, st, ev);
-  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 3, kDqS, 128, 2, 3, 3>(p, st, ev);
-  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 3, kDqS, 128, 2, 3, 2>(p, st, ev);
-  return bwd_shape<192, 128, 64, 1, 3, kDq, 64, 2, 3, 3>(p, st, ev);
+  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 6, 6, kDqS, 128, 2, 3, 3>(p, st, ev);
+  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 5, 4, kDqS, 128, 2, 3, 2>(p, st, ev);
+  return bwd_shape<192, 128, 64, 1, 3, 3, kDq, 64, 2, 3, 3>(p, st, ev);
 }
 
 // The tensor-core backward writes dQ directly (no fp32 accumulator); only the row dot
