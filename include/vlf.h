@@ -52,7 +52,8 @@ typedef enum {
   VLF_OK = 0,
   VLF_ERR_INVALID = -1,     /* null pointer, negative size, H_q % H_kv != 0, bias_heads not 1/H_q */
   VLF_ERR_UNSUPPORTED = -2, /* a valid problem this build does not implement (e.g. head width) */
-  VLF_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+  VLF_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned (device: a kernel's shared window
+                               is not 1024-byte aligned) */
   VLF_ERR_LAUNCH = -4,      /* the CUDA runtime refused a launch or a query */
   VLF_ERR_TIMEOUT = -5,     /* device: a pipeline wait exceeded its time limit (kernel bailed out) */
   VLF_ERR_BAD_SEQLENS = -6, /* device: cu_seqlens not in [0, total], decreasing, or longer than max_seqlen */

@@ -75,7 +75,8 @@ struct FwdCfg {
   static constexpr int B_DRAIN = B_O + 2 * NT;
   static constexpr int NBAR = B_DRAIN + 2 * NT;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  // (no alignment slack: the dynamic shared window starts 1024-byte aligned, checked in-kernel)
+  static constexpr int SMEM = OFF_MISC + 16;
   static constexpr int THREADS = NT == 2 ? 416 : 256;
   // TMEM: query tile t's two 64-column S buffers at 128 t, its O at O_COL + 128 t
   static constexpr uint32_t TMEM_COLS = 256 * NT, O_COL = 128 * NT;
@@ -85,7 +86,7 @@ struct FwdCfg {
   static_assert(NT == 1 || NT == 2, "query tiles per CTA");
   static_assert(NV >= 2 && NK >= 2, "ring depth");
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "tile shapes");
-  static_assert(SMEM <= (NT == 2 ? 232448 : 115712), "shared memory");
+  static_assert(SMEM <= (NT == 2 ? 232448 : 115712), "shared memory");  // NT = 1: two per SM
 };
 
 // Time-bounded wait that ignores the abort flag (used to drain in-flight work at teardown).
@@ -141,7 +142,7 @@ template <int DQK, int DV, int NK, int NV, int NT, bool BF16>
 __global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, NT == 1 ? 2 : 1)
 tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   using C = FwdCfg<DQK, DV, NK, NV, NT>;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const bool pair_heads = NT == 2 && (p.group % 2 == 0);
   const int s = blockIdx.z;
   Seq sq;
@@ -155,9 +156,14 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   tile_info<NT>(p, sq, bx, blockIdx.y, pair_heads, ti);
   if (ti.row0[0] >= sq.q_len) return;  // whole CTA beyond this sequence
 
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t *gbase = smem_raw + (base - raw);
+  // The kernel has no static shared memory, so the dynamic window starts 1024-byte aligned, as
+  // the 128-byte swizzle atoms of the TMA tiles and MMA descriptors require; refuse otherwise.
+  const uint32_t base = smem_u32(smem_raw);
+  if (base & 1023u) {
+    if (threadIdx.x == 0) set_error(p.err, VLF_ERR_ALIGN);
+    return;
+  }
+  uint8_t *gbase = smem_raw;
   const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -593,7 +599,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
 
 cudaError_t tc_forward(const Params &p, cudaStream_t st) {
   if (p.d_qk == 64) return launch_fwd<64, 64, 3, 3, 1>(p, st);
-  if (p.d_qk == 128) return launch_fwd<128, 128, 2, 2, 1>(p, st);
+  if (p.d_qk == 128) return launch_fwd<128, 128, 3, 2, 1>(p, st);
   return launch_fwd<192, 128, 3, 3, 2>(p, st);
 }
 
