@@ -95,13 +95,21 @@ _lib = _load()
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # (the argtypes are c_void_p: ctypes takes the integer address, None is NULL)
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, like=None):
+    """The handle of ``stream``, else of the current stream of ``like``'s device.  Asking torch
+    for the raw handle avoids building a Stream object (microseconds per call)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and like is not None:
+        return _raw_stream(like.get_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _check(status: int, what: str = ""):
@@ -227,7 +235,7 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
         cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv,
         _DTYPE[q.dtype], float(scale) if scale else 0.0, int(bool(causal)), int(window or 0),
-        _ptr(bias), bh, _ptr(out), _ptr(lse), _stream(stream), int(flags))
+        _ptr(bias), bh, _ptr(out), _ptr(lse), _stream(stream, q), int(flags))
     _check(st, "vlf_attn_varlen_fwd")
     return out, lse
 
@@ -261,7 +269,7 @@ def vlf_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, ma
         _ptr(cu_seqlens_kv), cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q),
         int(max_seqlen_kv), hq, hkv, dqk, dvv, _DTYPE[q.dtype], float(scale) if scale else 0.0,
         int(bool(causal)), int(window or 0), _ptr(bias), bh, _ptr(dq), _ptr(dk), _ptr(dv),
-        _ptr(workspace), workspace.numel(), _stream(stream), int(flags), *_events(stage_events))
+        _ptr(workspace), workspace.numel(), _stream(stream, q), int(flags), *_events(stage_events))
     _check(st, "vlf_attn_varlen_bwd")
     return dq, dk, dv
 
@@ -295,7 +303,7 @@ def vlf_attn_varlen_bwd_noalloc(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlen
         _ptr(cu_seqlens_kv), cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q),
         int(max_seqlen_kv), hq, hkv, dqk, dvv, _DTYPE[q.dtype], float(scale) if scale else 0.0,
         int(bool(causal)), int(window or 0), _ptr(bias), bh, _ptr(dq), _ptr(dk), _ptr(dv),
-        _stream(stream))
+        _stream(stream, q))
     _check(st, "vlf_attn_varlen_bwd_noalloc")
     return dq, dk, dv
 

@@ -15,6 +15,30 @@ __device__ int g_vlf_error_word = 0;
 namespace vlf {
 static std::atomic<uint64_t> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+cudaError_t set_smem_once(const void *kern, int bytes) {
+  struct Entry {
+    const void *kern;
+    int dev, bytes;
+  };
+  static Entry table[256];
+  static int n_entries = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_entries; ++i)
+    if (table[i].kern == kern && table[i].dev == dev) {
+      if (bytes <= table[i].bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) table[i].bytes = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && n_entries < 256) table[n_entries++] = Entry{kern, dev, bytes};
+  return e;
+}
 }  // namespace vlf
 
 namespace {

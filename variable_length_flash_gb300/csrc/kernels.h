@@ -23,6 +23,10 @@ size_t tc_backward_workspace(int total_q, int h_q, int d_qk);
 
 // Host-side count of successful kernel launches (api.cu).
 void count_launch(int n = 1);
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes), made once per (kernel, device)
+// and raised only when a launch needs more: the runtime call costs microseconds of host time,
+// which small problems would pay on every launch.
+cudaError_t set_smem_once(const void *kern, int bytes);
 
 // Records ev[i] on st when ev is not NULL.
 inline cudaError_t mark(const cudaEvent_t *ev, int i, cudaStream_t st) {

@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(const Params p) {
 template <typename Kern>
 cudaError_t launch(Kern kern, dim3 grid, size_t smem, cudaStream_t st, const Params &p) {
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, st>>>(p);
   e = cudaGetLastError();

@@ -579,7 +579,7 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   if (grid.x == 0) return cudaSuccess;
   auto kern = bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true>
                  : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, C::SMEM, st>>>(m, p);
   e = cudaGetLastError();

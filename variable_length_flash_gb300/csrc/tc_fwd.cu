@@ -588,7 +588,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
                   p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
   auto kern = bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true> : tc_fwd_kernel<DQK, DV, NK, NV, NT, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(maps, p);
   e = cudaGetLastError();
