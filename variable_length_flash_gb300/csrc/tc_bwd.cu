@@ -108,7 +108,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 // BF16: element type of the 16-bit tensors (bf16, else fp16), fixed at compile time so the
 // per-element conversions carry no runtime branch.
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, bool BF16>
+// BIAS: the problem has an additive bias (a separate instantiation, so that kernels without one
+// carry none of its code or registers).
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, bool BF16, bool BIAS>
 __global__ void __launch_bounds__(384, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1>;
@@ -401,7 +403,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       const float L = p.lse[gi];
       row_nl = L == -INFINITY ? -INFINITY : -L * kLog2e;
       row_nd = -p.rowdot[gi];
-      if (p.bias) {
+      if (BIAS) {
         const int bh = p.bias_heads == 1 ? 0 : head_outer;
         brow_dq = p.bias + ((size_t)(sq.q0 + orow) * p.bias_heads + bh) * (size_t)p.max_kv;
       }
@@ -418,7 +420,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       if (!ok) break;
       fence_after();
       const float *brow = brow_dq;
-      if (MODE == kDkdv && p.bias && orow_ok) {
+      if (MODE == kDkdv && BIAS && orow_ok) {
         const int bh = p.bias_heads == 1 ? 0 : h;
         brow = p.bias + (size_t)bh * p.max_kv + orow;  // + (q0 + i) * bias_heads * max_kv per column
       }
@@ -442,7 +444,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           plain = orow_ok && jlast < sq.kv_len && (!p.causal || jlast <= i + off) &&
                   (p.window <= 0 || i0 >= i + off - p.window + 1);
         }
-        plain = plain && p.bias == nullptr;
+        plain = plain && !BIAS;
         const float4 *lp = ldbuf + st * C::PAIRS + col0 / 2;  // this chunk's 16 pairs (dK/dV)
         tmem_ld_wait();
         if (MODE == kDqS && ch == C::CHUNKS - 1) {
@@ -466,6 +468,18 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             dk[e] = pack2(pa * ta, pb * tb, is_bf16);
           }
         } else {
+          // dQ with a bias: the chunk's 32 bias values of this row, 16 bytes at a time when the
+          // row address is 16-byte aligned and the chunk lies inside the row
+          const bool bvec = BIAS && MODE != kDkdv && brow != nullptr &&
+                            (reinterpret_cast<uintptr_t>(brow + i0) & 15u) == 0 && i0 + 32 <= p.max_kv;
+          float bq4[32];
+          if (bvec) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 b = __ldg(reinterpret_cast<const float4 *>(brow + i0) + q);
+              bq4[4 * q] = b.x; bq4[4 * q + 1] = b.y; bq4[4 * q + 2] = b.z; bq4[4 * q + 3] = b.w;
+            }
+          }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = 2 * e;
@@ -477,11 +491,13 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             for (int u = 0; u < 2; ++u) {
               const int cc = i0 + c + u;  // sequence-local column: query row (dK/dV) or key (dQ)
               float x = __uint_as_float(sv[c + u]) * sl2;
-              if (brow) {
-                // (clamped into the sequence: masked columns read a valid address)
+              if (BIAS && brow) {
+                // dQ: this row's bias, 16 bytes at a time when the chunk allows (bq4); else
+                // element by element (clamped into the sequence: masked columns read a valid
+                // address)
                 const float bv = MODE == kDkdv
                                      ? __ldg(brow + (size_t)(sq.q0 + min(cc, sq.q_len - 1)) * p.bias_heads * (size_t)p.max_kv)
-                                     : __ldg(brow + min(cc, sq.kv_len - 1));
+                                     : (bvec ? bq4[c + u] : __ldg(brow + min(cc, sq.kv_len - 1)));
                 x = fmaf(bv, kLog2e, x);
               }
               xs[u] = (cc >= vis_lo && cc < vis_hi) ? x : -INFINITY;
@@ -577,8 +593,10 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   const dim3 grid(MODE == kDkdv ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128,
                   MODE == kDkdv ? p.h_kv : p.h_q, p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  auto kern = bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true>
-                 : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false>;
+  auto kern = p.bias ? (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true, true>
+                           : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false, true>)
+                     : (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true, false>
+                           : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false, false>);
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, C::SMEM, st>>>(m, p);

@@ -138,7 +138,9 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
 
 // BF16: element type of Q/K/V/O (bf16, else fp16), fixed at compile time so the per-element
 // conversions carry no runtime branch.
-template <int DQK, int DV, int NK, int NV, int NT, bool BF16>
+// BIAS: the problem has an additive bias (a separate instantiation, so that kernels without one
+// carry none of its code or registers).
+template <int DQK, int DV, int NK, int NV, int NT, bool BF16, bool BIAS>
 __global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, NT == 1 ? 2 : 1)
 tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   using C = FwdCfg<DQK, DV, NK, NV, NT>;
@@ -335,7 +337,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     const uint32_t s_addr = lane_addr + 128 * t, o_addr = lane_addr + C::O_COL + 128 * t;
     const float sl2 = p.scale_log2;
     const float *brow = nullptr;
-    if (p.bias && row_ok) {
+    if (BIAS && row_ok) {
       const int bh = p.bias_heads == 1 ? 0 : head;
       brow = p.bias + ((size_t)(sq.q0 + i) * (size_t)p.bias_heads + (size_t)bh) * (size_t)p.max_kv;
     }
@@ -352,7 +354,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       const int kb = j * kBN;
       const bool full = row_ok && (kb + kBN - 1 < sq.kv_len) && (!p.causal || kb + kBN - 1 <= i + off) &&
                         (p.window <= 0 || kb >= i + off - p.window + 1);
-      const bool plain = full && brow == nullptr;
+      const bool plain = full && !BIAS;
       // the whole S row (64 fp32) in registers: two TMEM loads, one wait
       uint32_t v[kBN];
       __syncwarp();
@@ -431,13 +433,31 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           visible_range(i, off, sq.kv_len, p.causal, p.window, vlo, vhi);
           if (!row_ok) vhi = vlo;
           const int elo = vlo - kb, ehi = vhi - kb;
+          // logits in base 2; the bias row is read 16 bytes at a time when its address allows
+          // and the tile lies inside it, else element by element (the column clamped into the
+          // row: masked elements read a valid address)
+          if (BIAS && brow && (reinterpret_cast<uintptr_t>(brow) & 15u) == 0 && kb + kBN <= p.max_kv) {
+            const float4 *b4 = reinterpret_cast<const float4 *>(brow + kb);
+#pragma unroll
+            for (int q = 0; q < kBN / 4; ++q) {
+              const float4 bq = __ldg(b4 + q);
+              v[4 * q + 0] = __float_as_uint(fmaf(bq.x, kLog2e, __uint_as_float(v[4 * q + 0]) * sl2));
+              v[4 * q + 1] = __float_as_uint(fmaf(bq.y, kLog2e, __uint_as_float(v[4 * q + 1]) * sl2));
+              v[4 * q + 2] = __float_as_uint(fmaf(bq.z, kLog2e, __uint_as_float(v[4 * q + 2]) * sl2));
+              v[4 * q + 3] = __float_as_uint(fmaf(bq.w, kLog2e, __uint_as_float(v[4 * q + 3]) * sl2));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < kBN; ++e) {
+              float x = __uint_as_float(v[e]) * sl2;
+              if (BIAS && brow) x = fmaf(__ldg(brow + min(kb + e, sq.kv_len - 1)), kLog2e, x);
+              v[e] = __float_as_uint(x);
+            }
+          }
           mx = -INFINITY;
 #pragma unroll
           for (int e = 0; e < kBN; ++e) {
-            float x = __uint_as_float(v[e]) * sl2;
-            // (the bias column is clamped into the row: masked elements read a valid address)
-            if (brow) x = fmaf(__ldg(brow + min(kb + e, sq.kv_len - 1)), kLog2e, x);
-            x = (e >= elo && e < ehi) ? x : -INFINITY;
+            const float x = (e >= elo && e < ehi) ? __uint_as_float(v[e]) : -INFINITY;
             v[e] = __float_as_uint(x);
             mx = fmaxf(mx, x);
           }
@@ -587,7 +607,10 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   const dim3 grid((p.max_q + rows_per_cta - 1) / rows_per_cta, pair_heads ? p.h_q / 2 : p.h_q,
                   p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  auto kern = bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true> : tc_fwd_kernel<DQK, DV, NK, NV, NT, false>;
+  auto kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, true>
+                           : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, true>)
+                     : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, false>
+                           : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, false>);
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(maps, p);
