@@ -313,3 +313,10 @@ __all__ = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_bwd", "vlf_attn_varlen_bwd_wo
            "vlf_version", "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path",
            "vlf_attn_varlen_bwd_noalloc", "vlf_noalloc_scratch_bytes", "VlfError",
            "LIB_PATH", "EXPORTS"]
+
+# differentiable entry points (autograd over the two calls above)
+from .functional import (flash_attn_varlen_func, flash_attn_varlen_kvpacked_func,  # noqa: E402
+                         flash_attn_varlen_qkvpacked_func, varlen_attention)
+
+__all__ += ["varlen_attention", "flash_attn_varlen_func", "flash_attn_varlen_qkvpacked_func",
+            "flash_attn_varlen_kvpacked_func"]
