@@ -149,23 +149,28 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------ CPU oracle
 def oracle_sample(w, x_cpu, units: int):
-    """Time the fp64 oracle on `units` (sequence, head) units of the workload, fwd + bwd.
-    Returns (seconds, pairs) -- test infrastructure, run only for the CPU baseline."""
+    """Time the fp64 oracle on `units` (sequence, head) units of the workload, fwd + bwd (the
+    forward alone for workloads without a backward).  Returns (seconds, pairs) -- test
+    infrastructure, run only for the CPU baseline."""
     import numpy as np
 
     from oracle import attention as orc
-    cu = x_cpu["cu_seqlens_q"].tolist()
+    cu, ck = x_cpu["cu_seqlens_q"].tolist(), x_cpu["cu_seqlens_kv"].tolist()
     pairs, t0 = 0, time.perf_counter()
     for u in range(units):
         s, h = u % w.num_seqs, (u * 7) % w.h_q
         a, b = cu[s], cu[s + 1]
+        c, d = ck[s], ck[s + 1]
         g = w.h_q // w.h_kv
         q = x_cpu["q"][a:b, h].double().numpy()
-        k = x_cpu["k"][a:b, h // g].double().numpy()
-        v = x_cpu["v"][a:b, h // g].double().numpy()
-        do = x_cpu["dout"][a:b, h].double().numpy()
-        orc.head_backward(q, k, v, do, w.softmax_scale, w.causal, w.window)
-        pairs += F.visible_pairs(b - a, b - a, w.causal, w.window)
+        k = x_cpu["k"][c:d, h // g].double().numpy()
+        v = x_cpu["v"][c:d, h // g].double().numpy()
+        if w.backward:
+            do = x_cpu["dout"][a:b, h].double().numpy()
+            orc.head_backward(q, k, v, do, w.softmax_scale, w.causal, w.window)
+        else:
+            orc.head_forward(q, np.arange(b - a), k, v, b - a, w.softmax_scale, w.causal, w.window)
+        pairs += F.visible_pairs(b - a, d - c, w.causal, w.window)
     del np
     return time.perf_counter() - t0, pairs
 
@@ -179,7 +184,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     w = W.workload(args.workload)
-    fpp = F.flops_per_pair(w.d_qk, w.d_v)["fwd_bwd"]
+    fpp = F.flops_per_pair(w.d_qk, w.d_v)["fwd_bwd" if w.backward else "fwd"]
+    what = "fwd+bwd" if w.backward else "fwd"
     x = cpu_inputs(w, 1)
     for _ in range(args.warmup):
         oracle_sample(w, x, 1)
@@ -192,8 +198,8 @@ def run_reference(args, rank, world):
     value = pairs * fpp / total / 1e12
     cores = os.cpu_count()
     sample = (f"{args.steps} x one (sequence, head) unit of {w.name} "
-              f"({w.lengths_q[0]} rows, fwd+bwd, fp64 numpy; BLAS threads = host cores)")
-    line = {"impl": "reference", "metric": "attention TFLOP/s fwd+bwd (unmasked pairs)",
+              f"({w.lengths_q[0]} rows, {what}, fp64 numpy; BLAS threads = host cores)")
+    line = {"impl": "reference", "metric": f"attention TFLOP/s {what} (unmasked pairs)",
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -239,11 +245,19 @@ def main():
         w.total_q, w.total_kv, w.h_q, w.h_kv, w.d_qk, w.d_v, dt), dtype=torch.uint8, device=dev)
     kw = dict(scale=w.scale, causal=w.causal, window=w.window, bias=x["bias"])
 
+    # a step is the forward and the backward; workloads without a backward (decode-sized,
+    # latency-bound) time the forward alone
+    fwd_only = not w.backward
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         vlf.vlf_attn_varlen_fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_kv"],
                                 w.max_seqlen_q, w.max_seqlen_kv, out=out, lse=lse, **kw)
+        if fwd_only:
+            if ev is not None:
+                ev[1].record(stream)
+            return
         vlf.vlf_attn_varlen_bwd(x["dout"], x["q"], x["k"], x["v"], out, lse, x["cu_seqlens_q"],
                                 x["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv, dq=dq, dk=dk,
                                 dv=dv, workspace=ws, stage_events=None if ev is None else ev[1:],
@@ -256,8 +270,8 @@ def main():
     assert st == 0, vlf.vlf_status_string(st)
 
     # events: per step [fwd start, bwd start(=fwd end), after rowdot, after dkdv, after dq]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + vlf.VLF_BWD_STAGES)]
-           for _ in range(args.steps)]
+    n_ev = 2 if fwd_only else 2 + vlf.VLF_BWD_STAGES
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     for row in evs:  # torch creates the CUDA event at its first record()
         for e in row:
             e.record(stream)
@@ -269,8 +283,18 @@ def main():
     n0 = vlf.vlf_launch_count()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    # Inputs larger than L2 stream from HBM every step; smaller ones would stay in L2, so between
+    # their timed steps a buffer twice the L2 size is overwritten (outside each step's events)
+    # and the step time is the mean of the per-step event times.
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    in_bytes = sum(t.numel() * t.element_size() for t in (x["q"], x["k"], x["v"], x["dout"],
+                                                          x["bias"]) if t is not None)
+    flush = in_bytes < 2 * l2_bytes
+    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
     t_start.record(stream)
     for i in range(args.steps):
+        if flush:
+            flush_buf.zero_()
         step(evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -279,13 +303,16 @@ def main():
     clocks = sampler.stop()
     st = vlf.vlf_check_error()
     assert st == 0, vlf.vlf_status_string(st)
-    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
-    ms_step = ms_total / args.steps
-    stage_names = ["fwd"] + list(vlf.BWD_STAGE_NAMES)
+    if flush:
+        ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[-1]) for e in evs), world)
+    else:
+        ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / args.steps
+    stage_names = ["fwd"] + ([] if fwd_only else list(vlf.BWD_STAGE_NAMES))
     stage_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
                 for i, n in enumerate(stage_names)}
     fwd_ms = stage_ms["fwd"]
-    value = world * pairs * fpp["fwd_bwd"] / (ms_step * 1e-3) / 1e12
+    step_flops = fpp["fwd"] if fwd_only else fpp["fwd_bwd"]
+    value = world * pairs * step_flops / (ms_step * 1e-3) / 1e12
     fwd_tflops = pairs * fpp["fwd"] / (fwd_ms * 1e-3) / 1e12
 
     # roofline of the dominant kernel (one launch per stage per step)
@@ -295,11 +322,25 @@ def main():
     dom = max(stage_ms, key=stage_ms.get)
     flops_of = {"fwd": pairs * fpp["fwd"], "dkdv": pairs * fpp["dkdv"], "dq": pairs * fpp["dq"]}
     tc = (fwd_path if dom == "fwd" else bwd_path) == 1
-    if dom == "rowdot":
-        eb = x["q"].element_size()
-        traffic_alg = 2 * w.total_q * w.h_q * w.d_v * eb + 4 * w.total_q * w.h_q
-        achieved = traffic_alg / (stage_ms[dom] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    # Algorithmic bytes per kernel launch (the minimum it moves): its tensors read and written
+    # once, plus the bias once per pass where there is one.
+    eb = x["q"].element_size()
+    nq, nk = w.total_q * w.h_q, w.total_kv * w.h_kv
+    q_b, k_b, v_b = nq * w.d_qk * eb, nk * w.d_qk * eb, nk * w.d_v * eb
+    o_b, row_b = nq * w.d_v * eb, 4 * nq                    # O (or dO), one fp32 per row
+    bias_b = 0 if x["bias"] is None else x["bias"].numel() * 4
+    bytes_of = {"fwd": q_b + k_b + v_b + o_b + row_b + bias_b,
+                "rowdot": 2 * o_b + row_b,
+                "dkdv": q_b + k_b + v_b + o_b + 2 * row_b + k_b + v_b + bias_b,
+                "dq": q_b + k_b + v_b + o_b + 2 * row_b + q_b + bias_b}
+    # the bound is the roof the kernel is closer to: HBM for the row-dot, decode-sized forwards
+    # and bias streaming, the tensor cores for the rest
+    hbm_frac = bytes_of[dom] / (stage_ms[dom] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    ten_frac = flops_of.get(dom, 0) / (stage_ms[dom] * 1e-3) / 1e12 / peaks["bf16_tflops"]
+    if dom == "rowdot" or (tc and hbm_frac > ten_frac):
+        achieved = bytes_of[dom] / (stage_ms[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "algorithmic_bytes": bytes_of[dom]}
     elif tc:
         achieved = flops_of[dom] / (stage_ms[dom] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
@@ -311,7 +352,7 @@ def main():
         achieved = flops_of[dom] / (stage_ms[dom] * 1e-3) / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(dom, w.name) if tc or dom == "rowdot" else None
+    roof["traffic"] = ncu_traffic(dom, w.name) if tc or roof["bound"] == "hbm" else None
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x max SM clock)"
                                              if roof["bound"] == "alu" else "")
@@ -325,8 +366,9 @@ def main():
         # input pipeline would: step k+1's upload and step k-1's read-back run on the copy
         # engines while step k's kernels run.  (The bias, where a workload has one, stays
         # resident like a weight.)
-        in_keys = ("q", "k", "v", "dout", "cu_seqlens_q", "cu_seqlens_kv")
-        res_like = {"out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        in_keys = ("q", "k", "v", "cu_seqlens_q", "cu_seqlens_kv") + (() if fwd_only else ("dout",))
+        res_like = {"out": out, "lse": lse} if fwd_only else {"out": out, "lse": lse, "dq": dq,
+                                                              "dk": dk, "dv": dv}
         host = {k: x[k].cpu().pin_memory() for k in in_keys}
         dset = [{k: torch.empty_like(x[k]) for k in in_keys} for _ in range(2)]
         rset = [{k: torch.empty_like(t) for k, t in res_like.items()} for _ in range(2)]
@@ -355,10 +397,11 @@ def main():
             vlf.vlf_attn_varlen_fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_kv"],
                                     w.max_seqlen_q, w.max_seqlen_kv, out=r["out"], lse=r["lse"],
                                     stream=s_cmp, **kw)
-            vlf.vlf_attn_varlen_bwd(d["dout"], d["q"], d["k"], d["v"], r["out"], r["lse"],
-                                    d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q,
-                                    w.max_seqlen_kv, dq=r["dq"], dk=r["dk"], dv=r["dv"],
-                                    workspace=ws, stream=s_cmp, **kw)
+            if not fwd_only:
+                vlf.vlf_attn_varlen_bwd(d["dout"], d["q"], d["k"], d["v"], r["out"], r["lse"],
+                                        d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q,
+                                        w.max_seqlen_kv, dq=r["dq"], dk=r["dk"], dv=r["dv"],
+                                        workspace=ws, stream=s_cmp, **kw)
             ev_cmp[i].record(s_cmp)
             with torch.cuda.stream(s_dn):
                 s_dn.wait_event(ev_cmp[i])
@@ -379,7 +422,7 @@ def main():
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
-        e2e = {"value": world * pairs * fpp["fwd_bwd"] / (e2e_ms * 1e-3) / 1e12,
+        e2e = {"value": world * pairs * step_flops / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms, "pipelined": "upload / kernels / read-back of consecutive "
                                                    "steps overlap (3 streams, 2 buffer sets)"}
@@ -388,14 +431,15 @@ def main():
     if rank == 0 and world == 1 and args.cpu_units > 0:
         xc = cpu_inputs(w, args.cpu_units)
         secs, p = oracle_sample(w, xc, args.cpu_units)
-        cpu = {"value": p * fpp["fwd_bwd"] / secs / 1e12, "unit": "TFLOP/s",
+        cpu = {"value": p * step_flops / secs / 1e12, "unit": "TFLOP/s",
                "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{args.cpu_units} (sequence, head) units of {w.name}, fwd+bwd, fp64 "
-                         f"numpy, {secs:.1f} s"}
+               "sample": f"{args.cpu_units} (sequence, head) units of {w.name}, "
+                         f"{'fwd' if fwd_only else 'fwd+bwd'}, fp64 numpy, {secs:.1f} s"}
 
     if rank == 0:
         line = {
-            "metric": "attention TFLOP/s fwd+bwd (unmasked pairs)", "value": value,
+            "metric": "attention TFLOP/s " + ("fwd" if fwd_only else "fwd+bwd") + " (unmasked pairs)",
+            "value": value,
             "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1))",
@@ -403,7 +447,10 @@ def main():
                        "num_seqs": w.num_seqs, "h_q": w.h_q, "h_kv": w.h_kv, "d_qk": w.d_qk,
                        "d_v": w.d_v, "causal": w.causal, "window": w.window,
                        "unmasked_pairs": pairs, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (q/k/v/out/dout 134 MB each), no flush",
+                       "l2": (f"inputs {in_bytes / 1e6:.1f} MB < 2 x L2: L2 flushed between "
+                              f"timed steps (a {2 * l2_bytes / 1e6:.0f} MB write), per-step events"
+                              if flush else f"inputs {in_bytes / 1e6:.0f} MB > 2 x L2 "
+                              f"({l2_bytes / 1e6:.0f} MB): streamed from HBM, no flush"),
                        "fwd_path": "tcgen05" if fwd_path == 1 else "simt",
                        "bwd_path": "tcgen05" if bwd_path == 1 else "simt"},
             "fwd_tflops": fwd_tflops, "fwd_frac_of_peak": fwd_tflops / peaks["bf16_tflops"],

@@ -63,6 +63,8 @@ typedef enum {
 /* Extended-call flags (vlf_attn_varlen_fwd_ex / _bwd_ex). */
 #define VLF_FLAG_NO_SKIP 1u    /* visit every KV tile, masking per element (tile-skip check) */
 #define VLF_FLAG_FORCE_SIMT 2u /* use the SIMT fp32-FMA kernels even where a tensor-core one exists */
+#define VLF_FLAG_NO_PACK 4u    /* forward: never pack a kv head's query heads into one tile (the
+                                  decode-size layout); results are identical either way */
 
 /*
  * Forward.  mtlattn 0.3.0, section "Use" (varlen_attention with scale, causal, window, attn_bias).

@@ -120,3 +120,35 @@ def test_full_size_workload(name):
         assert e_dk <= 3 * tol and e_dv <= 3 * tol, (name, s, hk, e_dk, e_dv)
     del x, res
     torch.cuda.empty_cache()
+
+
+def test_decode_full_size_packing_exact():
+    """decode64x8192_bf16_gqa at full size in bench.py's configuration: the forward packs each kv
+    head's 4 query heads into one tile; the unpacked layout gives identical bits (every row's
+    arithmetic is the same), and sampled sequences -- the last included, every head -- match
+    the oracle."""
+    import variable_length_flash_gb300 as vlf
+    w = W.workload("decode64x8192_bf16_gqa")
+    x = W.make_inputs(w, seed=0, device="cuda", with_dout=False)
+    args = (x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_kv"], w.max_seqlen_q,
+            w.max_seqlen_kv)
+    out, lse = vlf.vlf_attn_varlen_fwd(*args, scale=w.scale, causal=True)
+    out2, lse2 = vlf.vlf_attn_varlen_fwd(*args, scale=w.scale, causal=True,
+                                         flags=vlf.VLF_FLAG_NO_PACK)
+    assert vlf.vlf_check_error() == 0
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    rng = np.random.default_rng(0)
+    seqs = sorted({0, w.num_seqs - 1} | set(int(s) for s in rng.integers(0, w.num_seqs, 4)))
+    cq, ck = x["cu_seqlens_q"].tolist(), x["cu_seqlens_kv"].tolist()
+    g = w.h_q // w.h_kv
+    o_err = l_err = 0.0
+    for s in seqs:
+        for h in range(w.h_q):
+            q = _np(x["q"][cq[s]:cq[s + 1], h])
+            k = _np(x["k"][ck[s]:ck[s + 1], h // g])
+            v = _np(x["v"][ck[s]:ck[s + 1], h // g])
+            o_ref, l_ref = orc.head_forward(q, np.arange(q.shape[0]), k, v, q.shape[0],
+                                            w.softmax_scale, True, 0)
+            o_err = max(o_err, max_err(_np(out[cq[s]:cq[s + 1], h]), o_ref))
+            l_err = max(l_err, max_err(_np(lse[h, cq[s]:cq[s + 1]]), l_ref))
+    assert o_err <= TOL["bf16"] and l_err <= LSE_TOL["bf16"], (o_err, l_err)

@@ -35,6 +35,15 @@ CASES = {
     "fp16_d96": W.custom([70, 129], dtype="fp16", h_q=2, d_qk=96, causal=True),
     "bf16_empty_seqs": W.custom([0, 5, 0, 130], [3, 5, 0, 130], dtype="bf16", h_q=2, d_qk=64,
                                 causal=False),
+    # decode-sized problems (the forward packs a kv head's G query heads into one tile)
+    "bf16_decode_gqa4": W.custom([1] * 8, [5, 64, 65, 200, 1, 129, 1000, 3], dtype="bf16",
+                                 h_q=8, h_kv=2, d_qk=128, causal=True),
+    "fp16_decode_mqa16_window": W.custom([1, 2, 3, 1], [300, 17, 64, 1], dtype="fp16", h_q=16,
+                                         h_kv=1, d_qk=64, causal=True, window=40),
+    "bf16_shortq_gqa8": W.custom([16, 5, 16], [40, 300, 16], dtype="bf16", h_q=16, h_kv=2,
+                                 d_qk=128, causal=True),
+    "fp16_decode_gqa2_full": W.custom([1, 1, 2], [33, 700, 2], dtype="fp16", h_q=4, h_kv=2,
+                                      d_qk=64, causal=False),
 }
 
 
@@ -70,6 +79,21 @@ def test_parity_bias(dtype, heads, causal, d, window):
     gpu = gpu_run(w, x)
     ref = oracle_run(w, x)
     assert_within(compare(w, gpu, ref), f"bias {dtype} {heads} {causal} {d}")
+
+
+@pytest.mark.parametrize("heads", [1, 8])
+def test_parity_bias_decode(heads):
+    """A bias on a decode-sized problem (packed query heads: each row reads its own head's
+    bias row)."""
+    w = W.custom([1, 2, 1], [90, 7, 300], dtype="bf16", h_q=8, h_kv=2, d_qk=128, causal=True)
+    x = W.make_inputs(w, seed=13, with_dout=True)
+    g = torch.Generator("cpu").manual_seed(14)
+    b = torch.randn((w.total_q, heads, w.max_seqlen_kv), generator=g)
+    b[torch.rand(b.shape, generator=g) < 0.2] = float("-inf")
+    x["bias"] = b.contiguous()
+    gpu = gpu_run(w, x)
+    ref = oracle_run(w, x)
+    assert_within(compare(w, gpu, ref), f"decode bias {heads}")
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])

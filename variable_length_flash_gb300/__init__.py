@@ -33,6 +33,7 @@ VLF_ERR_INVALID, VLF_ERR_UNSUPPORTED, VLF_ERR_ALIGN, VLF_ERR_LAUNCH = -1, -2, -3
 VLF_ERR_TIMEOUT, VLF_ERR_BAD_SEQLENS, VLF_ERR_WORKSPACE = -5, -6, -7
 VLF_FLAG_NO_SKIP = 1
 VLF_FLAG_FORCE_SIMT = 2
+VLF_FLAG_NO_PACK = 4
 
 _DTYPE = {torch.float16: VLF_F16, torch.bfloat16: VLF_BF16, torch.float32: VLF_F32}
 

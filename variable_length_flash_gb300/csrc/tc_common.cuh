@@ -91,6 +91,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x
       : "memory");
 }
 
+// 3-D tiled load of box {x: 64 elements, y, z} at (x, y, z) (16-byte rule on x as above).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

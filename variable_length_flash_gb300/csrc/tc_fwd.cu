@@ -52,6 +52,7 @@ constexpr int kBN = 64;                    // keys per KV tile
 
 struct FwdMaps {
   CUtensorMap q, k, v;
+  CUtensorMap q3;  // PACK: Q as [tokens][heads][D_qk], box {64, G heads, 128 / G tokens}
 };
 
 // NT: query tiles per CTA.  NT = 2: 416 threads and all 512 TMEM columns, one CTA per SM.
@@ -98,6 +99,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 struct TileInfo {
+  // row0: first sequence-local query row; head: query head (PACK: the kv head)
   int row0[2], head[2];
   int jlo[2], jhi[2];  // KV tile range of each query tile (empty: jlo == jhi)
   int lo, hi;          // union
@@ -105,16 +107,19 @@ struct TileInfo {
 
 // Query tiles of CTA (bx, by): NT = 2 takes two row blocks of one head, or the same rows of two
 // heads sharing a kv head (pair_heads); NT = 1 one row block.  Tile 1 of an NT = 1 CTA is empty.
-template <int NT>
+// PACK (NT = 1): the tile's 128 rows are 128 / G query rows x the G query heads of kv head by
+// (row r = query row r / G of head by G + r mod G), so each K/V tile serves the whole group.
+template <int NT, bool PACK>
 __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx, int by,
                                           bool pair_heads, TileInfo &ti) {
+  const int rows = PACK ? 128 / p.group : 128;  // query rows per tile
   for (int t = 0; t < 2; ++t) {
-    ti.row0[t] = NT == 1 ? (t == 0 ? bx * 128 : sq.q_len) : (pair_heads ? bx * 128 : bx * 256 + 128 * t);
+    ti.row0[t] = NT == 1 ? (t == 0 ? bx * rows : sq.q_len) : (pair_heads ? bx * 128 : bx * 256 + 128 * t);
     ti.head[t] = NT == 1 ? by : (pair_heads ? 2 * by + t : by);
     int jl = 0, jh = 0;
     if (ti.row0[t] < sq.q_len && sq.kv_len > 0) {
       int klo, khi;
-      kv_band(ti.row0[t], min(ti.row0[t] + 128, sq.q_len), sq.q_len, sq.kv_len, p.causal,
+      kv_band(ti.row0[t], min(ti.row0[t] + rows, sq.q_len), sq.q_len, sq.kv_len, p.causal,
               p.window, klo, khi);
       if (p.flags & VLF_FLAG_NO_SKIP) { klo = 0; khi = sq.kv_len; }
       if (khi > klo) { jl = klo / kBN; jh = (khi + kBN - 1) / kBN; }
@@ -140,7 +145,8 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
 // conversions carry no runtime branch.
 // BIAS: the problem has an additive bias (a separate instantiation, so that kernels without one
 // carry none of its code or registers).
-template <int DQK, int DV, int NK, int NV, int NT, bool BF16, bool BIAS>
+// PACK (NT = 1 only): the G query heads of a kv head share each tile (decode-sized problems).
+template <int DQK, int DV, int NK, int NV, int NT, bool BF16, bool BIAS, bool PACK>
 __global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, NT == 1 ? 2 : 1)
 tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   using C = FwdCfg<DQK, DV, NK, NV, NT>;
@@ -155,7 +161,8 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   // heavy (late, long-band) row blocks first under causal masking
   const int bx = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
   TileInfo ti;
-  tile_info<NT>(p, sq, bx, blockIdx.y, pair_heads, ti);
+  static_assert(!PACK || NT == 1, "packed heads use one query tile per CTA");
+  tile_info<NT, PACK>(p, sq, bx, blockIdx.y, pair_heads, ti);
   if (ti.row0[0] >= sq.q_len) return;  // whole CTA beyond this sequence
 
   // The kernel has no static shared memory, so the dynamic window starts 1024-byte aligned, as
@@ -195,7 +202,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int hk = ti.head[0] / p.group;  // both query tiles read the same kv head
+  const int hk = PACK ? ti.head[0] : ti.head[0] / p.group;  // both query tiles read one kv head
   constexpr int is_bf16 = BF16 ? 1 : 0;
   const int lo = ti.lo, hi = ti.hi;
 
@@ -210,9 +217,14 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       mbar_expect_tx(bar(C::B_Q), nq * C::Q_BYTES);
       for (int t = 0; t < 2; ++t) {
         if (ti.row0[t] >= sq.q_len) continue;
-        for (int c = 0; c < C::KBQ; ++c)
-          tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q, ti.head[t] * DQK + 64 * c,
-                      sq.q0 + ti.row0[t], bar(C::B_Q));
+        for (int c = 0; c < C::KBQ; ++c) {
+          if (PACK)  // rows (token, head of the group): one 3-D box
+            tma_load_3d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q3, 64 * c, hk * p.group,
+                        sq.q0 + ti.row0[t], bar(C::B_Q));
+          else
+            tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q, ti.head[t] * DQK + 64 * c,
+                        sq.q0 + ti.row0[t], bar(C::B_Q));
+        }
       }
       int k_issued[NK] = {0}, v_issued[NV] = {0};
       bool ok = true;
@@ -329,10 +341,10 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     const int t = NT == 2 ? (warp - 2) >> 2 : 0;
     const int quarter = warp & 3;
     const int r = 32 * quarter + lane;
-    const int i = ti.row0[t] + r;  // sequence-local query row
+    const int i = ti.row0[t] + (PACK ? r / p.group : r);  // sequence-local query row
     const bool row_ok = i < sq.q_len;
     const int off = sq.kv_len - sq.q_len;
-    const int head = ti.head[t];
+    const int head = PACK ? hk * p.group + r % p.group : ti.head[t];  // this row's query head
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     const uint32_t s_addr = lane_addr + 128 * t, o_addr = lane_addr + C::O_COL + 128 * t;
     const float sl2 = p.scale_log2;
@@ -592,25 +604,61 @@ bool tc_forward_supported(const Params &p) {
 }
 
 namespace {
+// 3-D map over Q as [tokens][heads][D] (16-bit): box {64 columns, box_heads, box_tokens},
+// 128-byte swizzle -- 128 dense 128-byte rows (token-major, head-minor) as a 2-D box gives.
+bool make_tmap_q3(CUtensorMap *m, const void *base, uint64_t tokens, uint64_t heads, uint64_t d,
+                  uint32_t box_heads, uint32_t box_tokens, int is_bf16) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc || tokens == 0 || heads == 0 || d == 0) return false;
+  cuuint64_t dims[3] = {d, heads, tokens};
+  cuuint64_t strides[2] = {d * 2, heads * d * 2};
+  cuuint32_t box[3] = {64, box_heads, box_tokens};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   3, const_cast<void *>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int DQK, int DV, int NK, int NV, int NT>
 cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   using C = FwdCfg<DQK, DV, NK, NV, NT>;
   FwdMaps maps;
   const int bf = p.dtype == VLF_BF16;
   if (p.total_q == 0 || p.total_kv == 0) return simt_forward(p, st);  // nothing to stage
+  // Decode-sized problems (every sequence's query rows fit one tile per kv head) pack the G
+  // query heads of a kv head into one tile, so each K/V tile is read once for the group.
+  const bool pack = NT == 1 && p.group >= 2 && 128 % p.group == 0 && p.max_q * p.group <= 128 &&
+                    !(p.flags & VLF_FLAG_NO_PACK);
   if (!make_tmap_16bit(&maps.q, p.q, p.total_q, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, 128, bf) ||
       !make_tmap_16bit(&maps.k, p.k, p.total_kv, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, kBN, bf) ||
       !make_tmap_16bit(&maps.v, p.v, p.total_kv, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, kBN, bf))
     return cudaErrorInvalidValue;
+  if (pack && !make_tmap_q3(&maps.q3, p.q, p.total_q, p.h_q, DQK, p.group, 128 / p.group, bf))
+    return cudaErrorInvalidValue;
+  if (!pack) maps.q3 = maps.q;
   const bool pair_heads = NT == 2 && (p.group % 2 == 0);
-  const int rows_per_cta = NT == 1 || pair_heads ? 128 : 256;
-  const dim3 grid((p.max_q + rows_per_cta - 1) / rows_per_cta, pair_heads ? p.h_q / 2 : p.h_q,
-                  p.num_seqs);
+  const int rows_per_cta = pack ? 128 / p.group : (NT == 1 || pair_heads ? 128 : 256);
+  const dim3 grid((p.max_q + rows_per_cta - 1) / rows_per_cta,
+                  pack ? p.h_kv : (pair_heads ? p.h_q / 2 : p.h_q), p.num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  auto kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, true>
-                           : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, true>)
-                     : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, false>
-                           : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, false>);
+  using K = void (*)(const FwdMaps, const Params);
+  K kern;
+  if (pack) {
+    if constexpr (NT == 1)
+      kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, true, true>
+                          : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, true, true>)
+                    : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, false, true>
+                          : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, false, true>);
+    else
+      return cudaErrorInvalidValue;
+  } else {
+    kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, true, false>
+                        : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, true, false>)
+                  : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, false, false>
+                        : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, false, false>);
+  }
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(maps, p);

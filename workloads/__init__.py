@@ -109,6 +109,11 @@ def workload(name: str, seed: int = 0) -> Workload:
         lens = [8192] * 2
         return Workload(name, "bf16", lens, lens, 128, 128, 192, 128, causal=True,
                         scale=1.0 / math.sqrt(192.0), latent_split=(128, 64))
+    if name == "decode64x8192_bf16_gqa":
+        # one new query row per sequence against an 8192-token cache (end-aligned causal: the
+        # row sees every key), GQA 4, forward only
+        return Workload(name, "bf16", [1] * 64, [8192] * 64, 32, 8, 128, 128, causal=True,
+                        backward=False)
     if name in ("long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix"):
         lens = [49152]
         return Workload(name, "fp16", lens, lens, 16, 16, 128, 128, causal=False, sigma=0.5,
@@ -118,7 +123,7 @@ def workload(name: str, seed: int = 0) -> Workload:
 
 WORKLOADS = ["varlen64_fp16_full", "varlen64_fp16_causal", "dense4x4096_bf16_causal",
              "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
-             "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix"]
+             "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "decode64x8192_bf16_gqa"]
 
 
 def custom(lengths_q, lengths_kv=None, *, dtype="bf16", h_q=4, h_kv=None, d_qk=64, d_v=None,
