@@ -1,6 +1,6 @@
 """GPU vs fp64 oracle, every element, on small varlen problems that still span several tiles
 and ragged tails: dtypes x {self, cross} x {causal, window, GQA/MQA, bias dim1 in {1, H}} x head
-widths {64, 128, 192/128, odd}, lengths including 0, 1, 15-17, 127-129 and thousands of tiny
+widths {64, 96, 128, 192/128, odd}, lengths including 0, 1, 15-17, 127-129 and thousands of tiny
 windows.  Also: tile skipping is exact (skip on/off give identical bits), bad cu_seqlens are
 reported through the device error word, and the SIMT and tensor-core paths both pass."""
 import numpy as np
@@ -33,6 +33,10 @@ CASES = {
     "fp32_d40_window": W.custom([50, 90], dtype="fp32", h_q=2, h_kv=1, d_qk=40, d_v=24,
                                 causal=True, window=7),
     "fp16_d96": W.custom([70, 129], dtype="fp16", h_q=2, d_qk=96, causal=True),
+    "bf16_d96_gqa_window": W.custom([300, 1, 129, 64], dtype="bf16", h_q=6, h_kv=2, d_qk=96,
+                                    causal=True, window=100),
+    "fp16_d96_decode_gqa4": W.custom([1, 1, 3], [200, 1, 700], dtype="fp16", h_q=8, h_kv=2,
+                                     d_qk=96, causal=True),
     "bf16_empty_seqs": W.custom([0, 5, 0, 130], [3, 5, 0, 130], dtype="bf16", h_q=2, d_qk=64,
                                 causal=False),
     # decode-sized problems (the forward packs a kv head's G query heads into one tile)

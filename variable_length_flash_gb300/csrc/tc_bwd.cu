@@ -59,7 +59,11 @@ struct BwdMaps {
 // (dQ), IR rows per item.
 template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1>
 struct BwdCfg {
-  static constexpr int KB0 = DQK / 64, KB1 = DV / 64;  // 64-col blocks of tensors 0 / 1
+  // 64-col blocks of tensors 0 / 1; a width that is not a multiple of 64 (96) is padded to
+  // whole blocks (next head's values or zero fill): products step over the real width along K,
+  // accumulations run at the padded N and the extra accumulator columns are never stored
+  static constexpr int KB0 = (DQK + 63) / 64, KB1 = (DV + 63) / 64;
+  static constexpr int NQ_PAD = KB0 * 64, NV_PAD = KB1 * 64;
   static constexpr int OBLK = 128 * 128, IBLK = IR * 128;  // bytes per 64-col block
   static constexpr int O0_BYTES = KB0 * OBLK, O1_BYTES = KB1 * OBLK;
   static constexpr int I0_BYTES = KB0 * IBLK, I1_BYTES = KB1 * IBLK;
@@ -87,14 +91,14 @@ struct BwdCfg {
   // one dP buffer
   static constexpr uint32_t ACC0 = 0;    // dV (dK/dV) or dQ (dQ)
   static constexpr uint32_t ACC1 = 128;  // dK (dK/dV)
-  static constexpr uint32_t BUF = MODE == kDkdv ? 128 + DQK : (MODE == kDqS ? DQK : 256);
+  static constexpr uint32_t BUF = MODE == kDkdv ? 128 + NQ_PAD : (MODE == kDqS ? NQ_PAD : 256);
   __host__ __device__ static constexpr uint32_t s_col(int b) { return MODE == kDqS ? BUF + IR * b : BUF + 2 * IR * b; }
   __host__ __device__ static constexpr uint32_t dp_col(int b) { return MODE == kDqS ? BUF + NBUF * IR : BUF + 2 * IR * b + IR; }
   static constexpr int HALF = IR / 2;      // columns per compute warpgroup
   static constexpr int CHUNKS = HALF / 32;  // 32-column chunks per compute thread
   static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * 2 * IR) <= 512, "TMEM columns");
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(DV <= 128 && DQK <= 256 && DQK % 64 == 0 && DV % 64 == 0, "head widths");
+  static_assert(NV_PAD <= 128 && NQ_PAD <= 256 && DQK % 32 == 0 && DV % 32 == 0, "head widths");
   static_assert(IR == 64 || IR == 128, "item rows");
   static_assert(NBUF == 1 || IR == 64 || MODE == kDqS, "double buffering only with 64-row items");
 };
@@ -280,8 +284,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // S / dP: M = 128 outer rows, N = IR inner rows, both operands K-major
       const uint32_t id_sp = idesc_f16(is_bf16, 128, IR, 0, 0);
       // accumulations: A from TMEM (K = IR inner rows), B = inner tile MN-major
-      const uint32_t id_a0 = idesc_f16(is_bf16, 128, MODE == kDkdv ? DV : DQK, 0, 1);
-      const uint32_t id_a1 = idesc_f16(is_bf16, 128, DQK, 0, 1);
+      const uint32_t id_a0 = idesc_f16(is_bf16, 128, MODE == kDkdv ? C::NV_PAD : C::NQ_PAD, 0, 1);
+      const uint32_t id_a1 = idesc_f16(is_bf16, 128, C::NQ_PAD, 0, 1);
       // descriptors are built once; a K step adds its byte offset / 16 to the start-address
       // field (shared addresses stay far below the field's 2^18-byte range, so nothing carries)
       const uint64_t d_o0 = sdesc_sw128(sO0, 16, 1024), d_o1 = sdesc_sw128(sO1, 16, 1024);
@@ -558,7 +562,11 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         if (half == 0) store_acc(C::ACC0, 0, DV, DV, p.dv, p.h_kv, hk, 1.f);
         else store_acc(C::ACC1, 0, DQK, DQK, p.dk, p.h_kv, hk, p.scale);
       } else {
-        store_acc(C::ACC0, half * (DQK / 2), DQK / 2, DQK, p.dq, p.h_q, head_outer, p.scale);
+        // the two halves split dQ's 32-column chunks (an odd count: the first takes one more)
+        constexpr int nch = DQK / 32, first = (nch + 1) / 2;
+        if (half == 0) store_acc(C::ACC0, 0, 32 * first, DQK, p.dq, p.h_q, head_outer, p.scale);
+        else if (nch > first)
+          store_acc(C::ACC0, 32 * first, 32 * (nch - first), DQK, p.dq, p.h_q, head_outer, p.scale);
       }
     }
   }
@@ -626,13 +634,14 @@ cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
 
 bool tc_backward_supported(const Params &p) {
   if (p.dtype != VLF_F16 && p.dtype != VLF_BF16) return false;
-  return (p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 128 && p.d_v == 128) ||
-         (p.d_qk == 192 && p.d_v == 128);
+  return (p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 96 && p.d_v == 96) ||
+         (p.d_qk == 128 && p.d_v == 128) || (p.d_qk == 192 && p.d_v == 128);
 }
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   if (p.total_q == 0 || p.total_kv == 0) return simt_backward(p, st, ev);
   if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 6, 6, kDqS, 128, 2, 3, 3>(p, st, ev);
+  if (p.d_qk == 96) return bwd_shape<96, 96, 64, 2, 5, 4, kDqS, 128, 2, 3, 2>(p, st, ev);
   if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 5, 4, kDqS, 128, 2, 3, 2>(p, st, ev);
   return bwd_shape<192, 128, 64, 1, 3, 3, kDq, 64, 2, 3, 3>(p, st, ev);
 }

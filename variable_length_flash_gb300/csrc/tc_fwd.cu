@@ -60,7 +60,12 @@ struct FwdMaps {
 // share an SM and one's prologue / epilogue overlaps the other's main loop.
 template <int DQK, int DV, int NK, int NV, int NT>
 struct FwdCfg {
-  static constexpr int KBQ = DQK / 64, KBV = DV / 64;  // 64-column (128-byte) swizzle blocks
+  // 64-column (128-byte) swizzle blocks per row.  A width that is not a multiple of 64 (96) is
+  // padded to whole blocks: the extra columns hold the next head's values (or the tensor's zero
+  // fill); the QK^T products step only over the real width, the P.V product runs at the padded
+  // N and its extra O columns are never stored.
+  static constexpr int KBQ = (DQK + 63) / 64, KBV = (DV + 63) / 64;
+  static constexpr int NV_PAD = KBV * 64;  // N of the P.V product
   static constexpr int QBLK = 128 * 128;               // one 128-row x 64-col block of Q
   static constexpr int KVBLK = kBN * 128;              // one 64-row x 64-col block of K or V
   static constexpr int Q_BYTES = KBQ * QBLK, K_BYTES = KBQ * KVBLK, V_BYTES = KBV * KVBLK;
@@ -86,7 +91,7 @@ struct FwdCfg {
   static constexpr int LEAD = NT == 1 ? 1 : 0;
   static_assert(NT == 1 || NT == 2, "query tiles per CTA");
   static_assert(NV >= 2 && NK >= 2, "ring depth");
-  static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "tile shapes");
+  static_assert(DQK % 32 == 0 && DV % 32 == 0 && NV_PAD <= 128, "tile shapes");
   static_assert(SMEM <= (NT == 2 ? 232448 : 115712), "shared memory");  // NT = 1: two per SM
 };
 
@@ -309,7 +314,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           mma_commit_w(bar(C::B_KE + it % NK));
         }
       } else {
-        const uint32_t id_o = idesc_f16(is_bf16, 128, DV, 0, 1);  // V is MN-major
+        const uint32_t id_o = idesc_f16(is_bf16, 128, C::NV_PAD, 0, 1);  // V is MN-major
         const uint64_t dv0 = sdesc_sw128(sV, C::KVBLK, 1024);
         for (int j = lo; j < hi && ok; ++j) {
           const int it = j - lo;
@@ -598,8 +603,8 @@ bool make_tmap_16bit(CUtensorMap *m, const void *base, uint64_t rows, uint64_t c
 
 bool tc_forward_supported(const Params &p) {
   if (p.dtype != VLF_F16 && p.dtype != VLF_BF16) return false;
-  const bool shape = (p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 128 && p.d_v == 128) ||
-                     (p.d_qk == 192 && p.d_v == 128);
+  const bool shape = (p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 96 && p.d_v == 96) ||
+                     (p.d_qk == 128 && p.d_v == 128) || (p.d_qk == 192 && p.d_v == 128);
   return shape;
 }
 
@@ -670,6 +675,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
 
 cudaError_t tc_forward(const Params &p, cudaStream_t st) {
   if (p.d_qk == 64) return launch_fwd<64, 64, 3, 3, 1>(p, st);
+  if (p.d_qk == 96) return launch_fwd<96, 96, 3, 2, 1>(p, st);
   if (p.d_qk == 128) return launch_fwd<128, 128, 3, 2, 1>(p, st);
   return launch_fwd<192, 128, 3, 3, 2>(p, st);
 }

@@ -101,6 +101,10 @@ def workload(name: str, seed: int = 0) -> Workload:
     if name == "dense4x4096_bf16_causal":
         lens = [4096] * 4
         return Workload(name, "bf16", lens, lens, 32, 32, 128, 128, causal=True)
+    if name == "dense4x4096_bf16_causal_d96":
+        # the dense configuration at head width 96 (a width the pages list beside 64/128/256)
+        lens = [4096] * 4
+        return Workload(name, "bf16", lens, lens, 32, 32, 96, 96, causal=True)
     if name == "ragged64_gqa_window_bf16":
         g = torch.Generator("cpu").manual_seed(seed)
         lens = ragged_lengths(64, 128, 8192, g)
@@ -123,7 +127,8 @@ def workload(name: str, seed: int = 0) -> Workload:
 
 WORKLOADS = ["varlen64_fp16_full", "varlen64_fp16_causal", "dense4x4096_bf16_causal",
              "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
-             "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "decode64x8192_bf16_gqa"]
+             "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "decode64x8192_bf16_gqa",
+             "dense4x4096_bf16_causal_d96"]
 
 
 def custom(lengths_q, lengths_kv=None, *, dtype="bf16", h_q=4, h_kv=None, d_qk=64, d_v=None,
