@@ -171,10 +171,10 @@ __global__ void __launch_bounds__(256) rowdot_kernel(const Params p) {
   if (lane == 0) p.rowdot[(size_t)h * p.total_q + row] = acc;
 }
 
-// The same for 16-bit tensors whose width is 8 G (G = 8 or 16 threads per pair): (row, head)
-// pairs are contiguous d_v-element segments, so G threads each take one 16-byte load of O and of
-// dO, and the group sums by shuffles.  Many wide loads in flight keep HBM busy.
-template <typename T, int G>
+// The same for 16-bit tensors whose width is 8 G L (G threads per pair, a power of two, each
+// taking L 16-byte loads of O and of dO): (row, head) pairs are contiguous d_v-element segments,
+// and the group sums by shuffles.  Many wide loads in flight keep HBM busy.
+template <typename T, int G, int L>
 __global__ void __launch_bounds__(256) rowdot16_kernel(const Params p) {
   const long long gtid = (long long)blockIdx.x * 256 + threadIdx.x;
   const long long pair = gtid / G;
@@ -182,11 +182,15 @@ __global__ void __launch_bounds__(256) rowdot16_kernel(const Params p) {
   const long long pairs = (long long)p.total_q * p.h_q;
   float acc = 0.f;
   if (pair < pairs) {
-    const uint4 o = __ldg(reinterpret_cast<const uint4 *>(static_cast<const T *>(p.out) + pair * (8 * G)) + part);
-    const uint4 d = __ldg(reinterpret_cast<const uint4 *>(static_cast<const T *>(p.dout) + pair * (8 * G)) + part);
-    const T *oe = reinterpret_cast<const T *>(&o), *de = reinterpret_cast<const T *>(&d);
+    const uint4 *o4 = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.out) + pair * (8 * G * L));
+    const uint4 *d4 = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.dout) + pair * (8 * G * L));
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc = fmaf(to_f32<T>(oe[e]), to_f32<T>(de[e]), acc);
+    for (int l = 0; l < L; ++l) {
+      const uint4 o = __ldg(o4 + part * L + l), d = __ldg(d4 + part * L + l);
+      const T *oe = reinterpret_cast<const T *>(&o), *de = reinterpret_cast<const T *>(&d);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(to_f32<T>(oe[e]), to_f32<T>(de[e]), acc);
+    }
   }
 #pragma unroll
   for (int s = G / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
@@ -450,17 +454,21 @@ cudaError_t simt_forward(const Params &p, cudaStream_t st) {
 cudaError_t rowdot_forward(const Params &p, cudaStream_t st) {
   if (p.total_q == 0) return cudaSuccess;
   const long long pairs = (long long)p.total_q * p.h_q;
-  if (p.dtype != VLF_F32 && (p.d_v == 64 || p.d_v == 128)) {
+  if (p.dtype != VLF_F32 && (p.d_v == 64 || p.d_v == 96 || p.d_v == 128)) {
     // (16-byte loads: the API requires 16-byte aligned tensors, and every segment starts at a
-    // multiple of d_v elements)
-    const int g = p.d_v / 8;
+    // multiple of d_v elements, itself a multiple of 8)
+    const int g = p.d_v == 96 ? 4 : p.d_v / 8;
     const unsigned blocks = (unsigned)((pairs * g + 255) / 256);
-    if (p.dtype == VLF_F16) {
-      if (g == 8) rowdot16_kernel<__half, 8><<<blocks, 256, 0, st>>>(p);
-      else rowdot16_kernel<__half, 16><<<blocks, 256, 0, st>>>(p);
+    const bool f16 = p.dtype == VLF_F16;
+    if (p.d_v == 64) {
+      if (f16) rowdot16_kernel<__half, 8, 1><<<blocks, 256, 0, st>>>(p);
+      else rowdot16_kernel<__nv_bfloat16, 8, 1><<<blocks, 256, 0, st>>>(p);
+    } else if (p.d_v == 96) {
+      if (f16) rowdot16_kernel<__half, 4, 3><<<blocks, 256, 0, st>>>(p);
+      else rowdot16_kernel<__nv_bfloat16, 4, 3><<<blocks, 256, 0, st>>>(p);
     } else {
-      if (g == 8) rowdot16_kernel<__nv_bfloat16, 8><<<blocks, 256, 0, st>>>(p);
-      else rowdot16_kernel<__nv_bfloat16, 16><<<blocks, 256, 0, st>>>(p);
+      if (f16) rowdot16_kernel<__half, 16, 1><<<blocks, 256, 0, st>>>(p);
+      else rowdot16_kernel<__nv_bfloat16, 16, 1><<<blocks, 256, 0, st>>>(p);
     }
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) count_launch();
