@@ -51,8 +51,8 @@ CASES = {
 }
 
 
-def _bias_case(dtype, heads, causal, d, window=0):
-    w = W.custom([70, 1, 140], dtype=dtype, h_q=4, h_kv=2, d_qk=d, causal=causal, window=window)
+def _bias_case(dtype, heads, causal, d, window=0, lengths=(70, 1, 140)):
+    w = W.custom(list(lengths), dtype=dtype, h_q=4, h_kv=2, d_qk=d, causal=causal, window=window)
     x = W.make_inputs(w, seed=11, with_dout=True)
     g = torch.Generator("cpu").manual_seed(12)
     b = torch.randn((w.total_q, heads, w.max_seqlen_kv), generator=g)
@@ -71,11 +71,16 @@ def test_parity_case(name):
     assert_within(compare(w, gpu, ref), name)
 
 
-@pytest.mark.parametrize("dtype,heads,causal,d,window", [
-    ("fp16", 4, False, 64, 0), ("bf16", 1, True, 128, 0), ("fp16", 4, True, 128, 33),
-    ("bf16", 4, False, 192, 0), ("fp32", 1, True, 64, 0)])
-def test_parity_bias(dtype, heads, causal, d, window):
-    w, x = _bias_case(dtype, heads, causal, d, window)
+@pytest.mark.parametrize("dtype,heads,causal,d,window,lengths", [
+    ("fp16", 4, False, 64, 0, (70, 1, 140)), ("bf16", 1, True, 128, 0, (70, 1, 140)),
+    ("fp16", 4, True, 128, 33, (70, 1, 140)), ("bf16", 4, False, 192, 0, (70, 1, 140)),
+    ("fp32", 1, True, 64, 0, (70, 1, 140)),
+    # max_seqlen_kv not a multiple of 4: bias rows are read row by row instead of through TMA
+    ("bf16", 4, True, 128, 0, (70, 1, 141))])
+def test_parity_bias(dtype, heads, causal, d, window, lengths):
+    """Bias tiles through TMA (D 64/128, rows 16-byte aligned), row by row otherwise, with the
+    heads of a row block run together for a head-broadcast bias."""
+    w, x = _bias_case(dtype, heads, causal, d, window, lengths)
     if d == 192:
         w.d_v = 128
         x["v"] = x["v"][:, :, :128].contiguous()

@@ -31,6 +31,9 @@ struct Params {
   float *dq_acc;  // [total_q, h_q, d_qk] fp32 (tensor-core backward)
   int *err;       // per-device error word
   unsigned flags;
+  // set by a launcher: grid x enumerates heads (y the row blocks), so that the CTAs reading the
+  // same tiles of a head-broadcast bias run together and share them through L2
+  int heads_fast = 0;
 };
 
 // ---------------------------------------------------------------- element access

@@ -125,9 +125,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   const int off = sq.kv_len - sq.q_len;
   // the CTA's outer tile and its item range (items start at multiples of IR)
   int tile0, head_outer, hk, n_items, lo = 0, nq_tiles = 0;
+  // heads_fast (a head-broadcast bias): grid x enumerates heads, y the 128-row tiles, so that the
+  // heads of one tile run together and share its bias tiles in L2
+  const int bxr = p.heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  const int gx = p.heads_fast ? (int)gridDim.y : (int)gridDim.x;
+  const int byh = p.heads_fast ? (int)blockIdx.x : (int)blockIdx.y;
   if (MODE == kDkdv) {
-    tile0 = blockIdx.x * 128;  // first key
-    hk = blockIdx.y;
+    tile0 = bxr * 128;  // first key
+    hk = byh;
     head_outer = hk;
     if (tile0 >= sq.kv_len) return;
     int qlo = 0, qhi = 0;
@@ -139,9 +144,9 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     nq_tiles = qhi > qlo ? (qhi - lo + IR - 1) / IR : 0;
     n_items = nq_tiles * p.group;
   } else {
-    const int bx = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    const int bx = p.causal ? gx - 1 - bxr : bxr;
     tile0 = bx * 128;  // first query row
-    head_outer = blockIdx.y;
+    head_outer = byh;
     hk = head_outer / p.group;
     if (tile0 >= sq.q_len) return;
     int klo = 0, khi = 0;
@@ -598,16 +603,19 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
          make_tmap_16bit(&m.inner1, p.v, tk, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, IR, bf);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const dim3 grid(MODE == kDkdv ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128,
-                  MODE == kDkdv ? p.h_kv : p.h_q, p.num_seqs);
-  if (grid.x == 0) return cudaSuccess;
+  const unsigned tiles = MODE == kDkdv ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128;
+  const unsigned heads = MODE == kDkdv ? p.h_kv : p.h_q;
+  if (tiles == 0) return cudaSuccess;
+  Params pl = p;
+  pl.heads_fast = p.bias != nullptr && p.bias_heads == 1;
+  const dim3 grid = pl.heads_fast ? dim3(heads, tiles, p.num_seqs) : dim3(tiles, heads, p.num_seqs);
   auto kern = p.bias ? (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true, true>
                            : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false, true>)
                      : (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true, false>
                            : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false, false>);
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 384, C::SMEM, st>>>(m, p);
+  kern<<<grid, 384, C::SMEM, st>>>(m, pl);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;

@@ -52,13 +52,15 @@ constexpr int kBN = 64;                    // keys per KV tile
 
 struct FwdMaps {
   CUtensorMap q, k, v;
-  CUtensorMap q3;  // PACK: Q as [tokens][heads][D_qk], box {64, G heads, 128 / G tokens}
+  CUtensorMap q3;    // PACK: Q as [tokens][heads][D_qk], box {64, G heads, 128 / G tokens}
+  CUtensorMap bias;  // bias through TMA: [total_q][bias_heads x max_kv] fp32, box {32, 128}
 };
 
 // NT: query tiles per CTA.  NT = 2: 416 threads and all 512 TMEM columns, one CTA per SM.
 // NT = 1: 256 threads, 256 TMEM columns and at most half the SM's shared memory, so two CTAs
 // share an SM and one's prologue / epilogue overlaps the other's main loop.
-template <int DQK, int DV, int NK, int NV, int NT>
+// NBS: stages of the bias ring (0: no bias through TMA).
+template <int DQK, int DV, int NK, int NV, int NT, int NBS = 0>
 struct FwdCfg {
   // 64-column (128-byte) swizzle blocks per row.  A width that is not a multiple of 64 (96) is
   // padded to whole blocks: the extra columns hold the next head's values (or the tensor's zero
@@ -72,14 +74,19 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NK * K_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NV * V_BYTES;
+  // bias tile of a 128-row query tile and a 64-key KV tile: two 32-column boxes (128-byte rows)
+  static constexpr int BIAS_BOX = 128 * 128, BIAS_STAGE = 2 * BIAS_BOX;
+  static constexpr int NBS_ = NBS > 0 ? NBS : 1;  // (a nonzero divisor where there is no ring)
+  static constexpr int OFF_B = OFF_V + NV * V_BYTES;
+  static constexpr int OFF_BAR = OFF_B + NBS * BIAS_STAGE;
   // barriers: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], then per query tile t
   // and S buffer b (index 2 t + b): s_full, p_full, o_done (the P.V that read buffer b); drain
   // (one per MMA-issuing warp)
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NK, B_VF = B_KE + NK, B_VE = B_VF + NV;
   static constexpr int B_S = B_VE + NV, B_P = B_S + 2 * NT, B_O = B_P + 2 * NT;
   static constexpr int B_DRAIN = B_O + 2 * NT;
-  static constexpr int NBAR = B_DRAIN + 2 * NT;
+  static constexpr int B_BF = B_DRAIN + 2 * NT, B_BE = B_BF + NBS;  // bias full / empty
+  static constexpr int NBAR = B_BE + NBS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // (no alignment slack: the dynamic shared window starts 1024-byte aligned, checked in-kernel)
   static constexpr int SMEM = OFF_MISC + 16;
@@ -92,7 +99,7 @@ struct FwdCfg {
   static_assert(NT == 1 || NT == 2, "query tiles per CTA");
   static_assert(NV >= 2 && NK >= 2, "ring depth");
   static_assert(DQK % 32 == 0 && DV % 32 == 0 && NV_PAD <= 128, "tile shapes");
-  static_assert(SMEM <= (NT == 2 ? 232448 : 115712), "shared memory");  // NT = 1: two per SM
+  static_assert(SMEM <= (NT == 2 || NBS > 0 ? 232448 : 115712), "shared memory");  // NT = 1: two per SM
 };
 
 // Time-bounded wait that ignores the abort flag (used to drain in-flight work at teardown).
@@ -148,13 +155,16 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
 
 // BF16: element type of Q/K/V/O (bf16, else fp16), fixed at compile time so the per-element
 // conversions carry no runtime branch.
-// BIAS: the problem has an additive bias (a separate instantiation, so that kernels without one
-// carry none of its code or registers).
+// BIAS: 0 no bias, 1 bias rows read from global memory, 2 bias tiles staged through TMA (NT = 1,
+// not PACK); separate instantiations, so that kernels without a bias carry none of its code or
+// registers.
 // PACK (NT = 1 only): the G query heads of a kv head share each tile (decode-sized problems).
-template <int DQK, int DV, int NK, int NV, int NT, bool BF16, bool BIAS, bool PACK>
+template <int DQK, int DV, int NK, int NV, int NT, bool BF16, int BIAS, bool PACK>
 __global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, NT == 1 ? 2 : 1)
 tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
-  using C = FwdCfg<DQK, DV, NK, NV, NT>;
+  constexpr int NBS = BIAS == 2 ? 2 : 0;
+  static_assert(BIAS != 2 || (NT == 1 && !PACK), "bias tiles through TMA: one unpacked tile");
+  using C = FwdCfg<DQK, DV, NK, NV, NT, NBS>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const bool pair_heads = NT == 2 && (p.group % 2 == 0);
   const int s = blockIdx.z;
@@ -163,11 +173,15 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   if (s == 0 && (__ldg(p.cu_q) != 0 || __ldg(p.cu_kv) != 0)) set_error(p.err, VLF_ERR_BAD_SEQLENS);
   if (s == p.num_seqs - 1 && (sq.q0 + sq.q_len != p.total_q || sq.k0 + sq.kv_len != p.total_kv))
     set_error(p.err, VLF_ERR_BAD_SEQLENS);
-  // heavy (late, long-band) row blocks first under causal masking
-  const int bx = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  // heavy (late, long-band) row blocks first under causal masking; heads_fast swaps the grid's
+  // x and y so that the heads of one row block run together
+  const int bxr = p.heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  const int gx = p.heads_fast ? (int)gridDim.y : (int)gridDim.x;
+  const int bx = p.causal ? gx - 1 - bxr : bxr;
+  const int by = p.heads_fast ? (int)blockIdx.x : (int)blockIdx.y;
   TileInfo ti;
   static_assert(!PACK || NT == 1, "packed heads use one query tile per CTA");
-  tile_info<NT, PACK>(p, sq, bx, blockIdx.y, pair_heads, ti);
+  tile_info<NT, PACK>(p, sq, bx, by, pair_heads, ti);
   if (ti.row0[0] >= sq.q_len) return;  // whole CTA beyond this sequence
 
   // The kernel has no static shared memory, so the dynamic window starts 1024-byte aligned, as
@@ -179,6 +193,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   }
   uint8_t *gbase = smem_raw;
   const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t sB = base + C::OFF_B;
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
@@ -196,6 +211,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       mbar_init(bar(C::B_O + i), 1);
       mbar_init(bar(C::B_DRAIN + i), 1);
     }
+    for (int i = 0; i < NBS; ++i) { mbar_init(bar(C::B_BF + i), 1); mbar_init(bar(C::B_BE + i), 128); }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -231,10 +247,23 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
                         sq.q0 + ti.row0[t], bar(C::B_Q));
         }
       }
-      int k_issued[NK] = {0}, v_issued[NV] = {0};
+      int k_issued[NK] = {0}, v_issued[NV] = {0}, b_issued[NBS > 0 ? NBS : 1] = {0};
+      if (BIAS == 2) tma_prefetch_desc(&maps.bias);
+      const int bcol = BIAS == 2 ? (p.bias_heads == 1 ? 0 : ti.head[0]) * p.max_kv : 0;
       bool ok = true;
       for (int j = lo; j < hi + C::LEAD && ok; ++j) {
         const int kj = j, vj = j - C::LEAD;  // K tile issued ahead of V by LEAD
+        if (BIAS == 2 && kj < hi) {
+          // the query tile's bias columns of KV tile kj: rows row0 .. row0 + 127
+          const int it = kj - lo, bs = it % C::NBS_;
+          if (it >= C::NBS_) ok = mbar_wait(bar(C::B_BE + bs), ((it / C::NBS_) - 1) & 1, abort_flag, p.err);
+          if (!ok) break;
+          mbar_expect_tx(bar(C::B_BF + bs), C::BIAS_STAGE);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sB + bs * C::BIAS_STAGE + c * C::BIAS_BOX, &maps.bias, bcol + kj * kBN + 32 * c,
+                        sq.q0 + ti.row0[0], bar(C::B_BF + bs));
+          ++b_issued[bs];
+        }
         if (kj < hi) {
           const int it = kj - lo, ks = it % NK;
           if (it >= NK) ok = mbar_wait(bar(C::B_KE + ks), ((it / NK) - 1) & 1, abort_flag, p.err);
@@ -262,6 +291,8 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         if (k_issued[i]) drain_wait(bar(C::B_KF + i), (k_issued[i] - 1) & 1);
       for (int i = 0; i < NV; ++i)
         if (v_issued[i]) drain_wait(bar(C::B_VF + i), (v_issued[i] - 1) & 1);
+      for (int i = 0; i < NBS; ++i)
+        if (b_issued[i]) drain_wait(bar(C::B_BF + i), (b_issued[i] - 1) & 1);
     }
   } else if (NT == 2 ? (warp == 1 || warp >= 10) : (warp == 1 || warp == 2)) {
     // ------------------------------------------------------------------ MMA issuers
@@ -453,7 +484,26 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           // logits in base 2; the bias row is read 16 bytes at a time when its address allows
           // and the tile lies inside it, else element by element (the column clamped into the
           // row: masked elements read a valid address)
-          if (BIAS && brow && (reinterpret_cast<uintptr_t>(brow) & 15u) == 0 && kb + kBN <= p.max_kv) {
+          if (BIAS == 2) {
+            // the tile's bias, staged by the producer: this row of the two 32-column boxes
+            // (128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r mod 8))
+            const int it = j - jlo, bs = it % C::NBS_;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_BF + bs), (it / C::NBS_) & 1, abort_flag, p.err));
+            if (!ok) break;
+            const uint32_t rowb = sB + bs * C::BIAS_STAGE + r * 128;
+#pragma unroll
+            for (int q = 0; q < kBN / 4; ++q) {
+              const uint32_t a = rowb + (q >> 3) * C::BIAS_BOX + (((q & 7) ^ (r & 7)) << 4);
+              float4 bq;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(bq.x), "=f"(bq.y), "=f"(bq.z), "=f"(bq.w) : "r"(a));
+              v[4 * q + 0] = __float_as_uint(fmaf(bq.x, kLog2e, __uint_as_float(v[4 * q + 0]) * sl2));
+              v[4 * q + 1] = __float_as_uint(fmaf(bq.y, kLog2e, __uint_as_float(v[4 * q + 1]) * sl2));
+              v[4 * q + 2] = __float_as_uint(fmaf(bq.z, kLog2e, __uint_as_float(v[4 * q + 2]) * sl2));
+              v[4 * q + 3] = __float_as_uint(fmaf(bq.w, kLog2e, __uint_as_float(v[4 * q + 3]) * sl2));
+            }
+            mbar_arrive(bar(C::B_BE + bs));  // the slot may be refilled
+          } else if (BIAS && brow && (reinterpret_cast<uintptr_t>(brow) & 15u) == 0 && kb + kBN <= p.max_kv) {
             const float4 *b4 = reinterpret_cast<const float4 *>(brow + kb);
 #pragma unroll
             for (int q = 0; q < kBN / 4; ++q) {
@@ -626,6 +676,21 @@ bool make_tmap_q3(CUtensorMap *m, const void *base, uint64_t tokens, uint64_t he
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the bias as [total_q][bias_heads x max_kv] fp32: box {32 columns, 128 rows},
+// 128-byte swizzle (the softmax threads read their row's chunks at chunk ^ (row mod 8)).
+bool make_tmap_bias(CUtensorMap *m, const float *base, uint64_t rows, uint64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int DQK, int DV, int NK, int NV, int NT>
 cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   using C = FwdCfg<DQK, DV, NK, NV, NT>;
@@ -645,28 +710,48 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   if (!pack) maps.q3 = maps.q;
   const bool pair_heads = NT == 2 && (p.group % 2 == 0);
   const int rows_per_cta = pack ? 128 / p.group : (NT == 1 || pair_heads ? 128 : 256);
-  const dim3 grid((p.max_q + rows_per_cta - 1) / rows_per_cta,
-                  pack ? p.h_kv : (pair_heads ? p.h_q / 2 : p.h_q), p.num_seqs);
-  if (grid.x == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((p.max_q + rows_per_cta - 1) / rows_per_cta);
+  const unsigned heads = pack ? p.h_kv : (pair_heads ? p.h_q / 2 : p.h_q);
+  if (blocks == 0) return cudaSuccess;
+  // A bias whose rows are 16-byte aligned goes through TMA tiles (one unpacked tile per CTA; the
+  // ring takes the room of a second CTA per SM); others are read row by row.
+  const bool bias_tma = NT == 1 && !pack && p.bias != nullptr && p.max_kv % 4 == 0 &&
+                        (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
+  if (bias_tma && !make_tmap_bias(&maps.bias, p.bias, p.total_q, (uint64_t)p.bias_heads * p.max_kv))
+    return cudaErrorInvalidValue;
+  if (!bias_tma) maps.bias = maps.q;
+  // a head-broadcast bias: the heads of one row block run together and share its tiles in L2
+  Params pl = p;
+  pl.heads_fast = p.bias != nullptr && p.bias_heads == 1 && !pack;
+  const dim3 grid = pl.heads_fast ? dim3(heads, blocks, p.num_seqs) : dim3(blocks, heads, p.num_seqs);
   using K = void (*)(const FwdMaps, const Params);
   K kern;
+  int smem = C::SMEM;
   if (pack) {
     if constexpr (NT == 1)
-      kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, true, true>
-                          : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, true, true>)
-                    : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, false, true>
-                          : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, false, true>);
+      kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 1, true>
+                          : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 1, true>)
+                    : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 0, true>
+                          : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 0, true>);
     else
       return cudaErrorInvalidValue;
+  } else if (bias_tma) {
+    if constexpr (NT == 1) {
+      kern = bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 2, false>
+                : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 2, false>;
+      smem = FwdCfg<DQK, DV, NK, NV, NT, 2>::SMEM;
+    } else {
+      return cudaErrorInvalidValue;
+    }
   } else {
-    kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, true, false>
-                        : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, true, false>)
-                  : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, false, false>
-                        : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, false, false>);
+    kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 1, false>
+                        : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 1, false>)
+                  : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 0, false>
+                        : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 0, false>);
   }
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(maps, p);
+  kern<<<grid, C::THREADS, smem, st>>>(maps, pl);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
