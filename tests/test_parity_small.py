@@ -76,7 +76,9 @@ def test_parity_case(name):
     ("fp16", 4, True, 128, 33, (70, 1, 140)), ("bf16", 4, False, 192, 0, (70, 1, 140)),
     ("fp32", 1, True, 64, 0, (70, 1, 140)),
     # max_seqlen_kv not a multiple of 4: bias rows are read row by row instead of through TMA
-    ("bf16", 4, True, 128, 0, (70, 1, 141))])
+    ("bf16", 4, True, 128, 0, (70, 1, 141)),
+    # enough items per CTA that both backward kernels' bias rings wrap several times
+    ("fp16", 4, True, 96, 0, (300, 1, 257)), ("bf16", 1, False, 64, 0, (384, 129, 200))])
 def test_parity_bias(dtype, heads, causal, d, window, lengths):
     """Bias tiles through TMA (D 64/128, rows 16-byte aligned), row by row otherwise, with the
     heads of a row block run together for a head-broadcast bias."""

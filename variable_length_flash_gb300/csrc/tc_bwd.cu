@@ -40,6 +40,8 @@ namespace vlf {
 
 bool make_tmap_16bit(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
                      uint64_t pitch_elems, uint32_t box_rows, int is_bf16);
+bool make_tmap_bias(CUtensorMap *m, const float *base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows, bool swizzle);
 
 namespace {
 
@@ -52,12 +54,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kDkdv = 0, kDq = 1, kDqS = 2;
 
 struct BwdMaps {
-  CUtensorMap outer0, outer1, inner0, inner1;
+  CUtensorMap outer0, outer1, inner0, inner1, bias;
 };
 
 // outer0/outer1: K, V (dK/dV) or Q, dO (dQ), 128 rows.  inner0/inner1: Q, dO (dK/dV) or K, V
-// (dQ), IR rows per item.
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1>
+// (dQ), IR rows per item.  NBS: stages of the bias ring (0: no bias through TMA).
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS = 0>
 struct BwdCfg {
   // 64-col blocks of tensors 0 / 1; a width that is not a multiple of 64 (96) is padded to
   // whole blocks (next head's values or zero fill): products step over the real width along K,
@@ -75,7 +77,16 @@ struct BwdCfg {
   // (dK/dV only)
   static constexpr int PAIRS = MODE == kDkdv ? IR / 2 : 0;
   static constexpr int OFF_LD = OFF_IN1 + NSTAGE1 * I1_BYTES;
-  static constexpr int OFF_BAR = OFF_LD + NSTAGE * PAIRS * 16;
+  // bias ring: per item its 128 x IR fp32 tile as 32-column boxes.  dK/dV: 4 boxes {32 keys, IR
+  // query rows}, unswizzled (the 32 keys of a warp read one 128-byte row at a time); dQ: IR / 32
+  // boxes {32 keys, 128 query rows}, 128-byte swizzled (each thread reads along its own row).
+  static constexpr int BIAS_BOX = MODE == kDkdv ? 32 * IR * 4 : 32 * 128 * 4;
+  static constexpr int BIAS_STAGE = 128 * IR * 4;
+  static constexpr int NBS_ = NBS > 0 ? NBS : 1;  // (a nonzero divisor where there is no ring)
+  // (swizzled boxes start 1024-byte aligned, unswizzled ones 128-byte aligned)
+  static constexpr int B_ALIGN = MODE == kDkdv ? 128 : 1024;
+  static constexpr int OFF_B = (OFF_LD + NSTAGE * PAIRS * 16 + B_ALIGN - 1) & ~(B_ALIGN - 1);
+  static constexpr int OFF_BAR = OFF_B + NBS * BIAS_STAGE;
   // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE] (ring 0), in1_full[NSTAGE1],
   // in1_empty[NSTAGE1] (ring 1), s_full[NBUF] (S and dP issued:
   // two arrivals), p_ready[NBUF], acc0_done[NBUF] (dV), acc_done[NBUF] (dK or dQ: the item's last
@@ -84,7 +95,8 @@ struct BwdCfg {
   static constexpr int B_IE1 = B_IF1 + NSTAGE1, B_S = B_IE1 + NSTAGE1;
   static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + NBUF, B_DRAIN = B_D + NBUF;
   static constexpr int B_PF = B_DRAIN + 3;  // kDqS: the compute warps have loaded dP
-  static constexpr int NBAR = B_PF + 1;
+  static constexpr int B_BF = B_PF + 1, B_BE = B_BF + NBS;  // bias full / empty
+  static constexpr int NBAR = B_BE + NBS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   // TMEM: accumulators first, then NBUF x (S IR cols, dP IR cols); kDqS: NBUF S buffers, then
@@ -112,12 +124,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 // BF16: element type of the 16-bit tensors (bf16, else fp16), fixed at compile time so the
 // per-element conversions carry no runtime branch.
-// BIAS: the problem has an additive bias (a separate instantiation, so that kernels without one
-// carry none of its code or registers).
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, bool BF16, bool BIAS>
+// BIAS: 0 none; 1 the compute threads load their bias values from global memory; 2 the producer
+// stages each item's bias tile through the NBS-stage ring (a separate instantiation each, so that
+// kernels without a bias carry none of its code or registers).
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS, bool BF16,
+          int BIAS>
 __global__ void __launch_bounds__(384, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
-  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1>;
+  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS>;
+  static_assert((BIAS == 2) == (NBS > 0), "the bias ring serves TMA-staged bias only");
   extern __shared__ uint8_t smem_raw[];
   const int s = blockIdx.z;
   Seq sq;
@@ -162,7 +177,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
   const uint32_t sO0 = base + C::OFF_O0, sO1 = base + C::OFF_O1;
-  const uint32_t sIn0 = base + C::OFF_IN0, sIn1 = base + C::OFF_IN1;
+  const uint32_t sIn0 = base + C::OFF_IN0, sIn1 = base + C::OFF_IN1, sBias = base + C::OFF_B;
   float4 *ldbuf = reinterpret_cast<float4 *>(gbase + C::OFF_LD);  // [stage][IR/2 column pairs]
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -183,6 +198,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     }
     for (int i = 0; i < 3; ++i) mbar_init(bar(C::B_DRAIN + i), 1);
     mbar_init(bar(C::B_PF), 256);
+    for (int i = 0; i < NBS; ++i) { mbar_init(bar(C::B_BF + i), 1); mbar_init(bar(C::B_BE + i), 256); }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -208,6 +224,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         tma_prefetch_desc(&maps.outer1);
         tma_prefetch_desc(&maps.inner0);
         tma_prefetch_desc(&maps.inner1);
+        if (BIAS == 2) tma_prefetch_desc(&maps.bias);
         const int orow = (MODE == kDkdv ? sq.k0 : sq.q0) + tile0;
         const int oh = MODE == kDkdv ? hk : head_outer;  // head index inside the outer tensors
         mbar_expect_tx(bar(C::B_OUT), C::O0_BYTES + C::O1_BYTES);
@@ -216,9 +233,37 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         for (int c = 0; c < C::KB1; ++c)
           tma_load_2d(sO1 + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
       }
-      int issued0[NSTAGE] = {0}, issued1[NSTAGE1] = {0};
+      int issued0[NSTAGE] = {0}, issued1[NSTAGE1] = {0}, issuedb[C::NBS_] = {0};
       for (int n = 0; n < n_items; ++n) {
         const int st = n % NSTAGE, st1 = n % NSTAGE1;
+        if (BIAS == 2) {
+          // the item's bias tile (needed last, by the compute warps; its slot frees earliest)
+          const int bs = n % C::NBS_;
+          bool wb = true;
+          if (lane == 0) {
+            if (n >= C::NBS_) wb = mbar_wait(bar(C::B_BE + bs), ((n / C::NBS_) - 1) & 1, abort_flag, p.err);
+            if (wb) {
+              const uint32_t dst = sBias + bs * C::BIAS_STAGE;
+              mbar_expect_tx(bar(C::B_BF + bs), C::BIAS_STAGE);
+              // bias columns: bias head * max_seqlen_kv + sequence-local key; rows: global query
+              // rows.  Boxes past the tensor are zero-filled; columns past the sequence's keys
+              // and rows past its queries are masked by the compute threads.
+              if (MODE == kDkdv) {
+                const int x = (p.bias_heads == 1 ? 0 : item_head(n)) * p.max_kv + tile0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  tma_load_2d(dst + c * C::BIAS_BOX, &maps.bias, x + 32 * c, sq.q0 + item_row(n), bar(C::B_BF + bs));
+              } else {
+                const int x = (p.bias_heads == 1 ? 0 : head_outer) * p.max_kv + item_row(n);
+#pragma unroll
+                for (int c = 0; c < IR / 32; ++c)
+                  tma_load_2d(dst + c * C::BIAS_BOX, &maps.bias, x + 32 * c, sq.q0 + tile0, bar(C::B_BF + bs));
+              }
+              ++issuedb[bs];
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, (int)wb, 0)) break;
+        }
         if (n >= NSTAGE) {
           bool w = true;
           if (lane == 0) w = mbar_wait(bar(C::B_IE + st), ((n / NSTAGE) - 1) & 1, abort_flag, p.err);
@@ -275,6 +320,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           if (issued0[i]) drain_wait(bar(C::B_IF + i), (issued0[i] - 1) & 1);
         for (int i = 0; i < NSTAGE1; ++i)
           if (issued1[i]) drain_wait(bar(C::B_IF1 + i), (issued1[i] - 1) & 1);
+        for (int i = 0; i < NBS; ++i)
+          if (issuedb[i]) drain_wait(bar(C::B_BF + i), (issuedb[i] - 1) & 1);
       }
     }
   } else if (warp == 1 || warp >= 10) {
@@ -412,7 +459,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       const float L = p.lse[gi];
       row_nl = L == -INFINITY ? -INFINITY : -L * kLog2e;
       row_nd = -p.rowdot[gi];
-      if (BIAS) {
+      if (BIAS == 1) {
         const int bh = p.bias_heads == 1 ? 0 : head_outer;
         brow_dq = p.bias + ((size_t)(sq.q0 + orow) * p.bias_heads + bh) * (size_t)p.max_kv;
       }
@@ -425,11 +472,12 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // the LSE / D pairs were written by the producer lanes before their arrive on in_full:
       // acquire that barrier too before reading them
       if (MODE == kDkdv && w) w = mbar_wait(bar(C::B_IF + st), (n / NSTAGE) & 1, abort_flag, p.err);
+      if (BIAS == 2 && w) w = mbar_wait(bar(C::B_BF + n % C::NBS_), (n / C::NBS_) & 1, abort_flag, p.err);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       fence_after();
       const float *brow = brow_dq;
-      if (MODE == kDkdv && BIAS && orow_ok) {
+      if (MODE == kDkdv && BIAS == 1 && orow_ok) {
         const int bh = p.bias_heads == 1 ? 0 : h;
         brow = p.bias + (size_t)bh * p.max_kv + orow;  // + (q0 + i) * bias_heads * max_kv per column
       }
@@ -453,8 +501,26 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           plain = orow_ok && jlast < sq.kv_len && (!p.causal || jlast <= i + off) &&
                   (p.window <= 0 || i0 >= i + off - p.window + 1);
         }
-        plain = plain && !BIAS;
+        plain = plain && BIAS != 1;
         const float4 *lp = ldbuf + st * C::PAIRS + col0 / 2;  // this chunk's 16 pairs (dK/dV)
+        // TMA-staged bias: the chunk's 32 values of this thread -- dQ: along its row, from the
+        // chunk's swizzled box; dK/dV: down its key's column, one 128-byte box row per query row
+        float bq4[32];
+        if (BIAS == 2) {
+          const uint32_t bstage = sBias + (n % C::NBS_) * C::BIAS_STAGE;
+          if (MODE == kDkdv) {
+            const uint32_t bcol = bstage + quarter * C::BIAS_BOX + lane * 4 + col0 * 128;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) bq4[k] = lds_f32(bcol + k * 128);
+          } else {
+            const uint32_t rowb = bstage + (col0 / 32) * C::BIAS_BOX + r * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 b = lds_f32x4(rowb + ((q ^ (r & 7)) << 4));
+              bq4[4 * q] = b.x; bq4[4 * q + 1] = b.y; bq4[4 * q + 2] = b.z; bq4[4 * q + 3] = b.w;
+            }
+          }
+        }
         tmem_ld_wait();
         if (MODE == kDqS && ch == C::CHUNKS - 1) {
           // every dP column of the item is in registers: the next dP may overwrite them
@@ -463,25 +529,29 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         }
         uint32_t pk[16], dk[16];
         if (plain) {
-          // every pair visible, no bias: P = 2^(S log2e scale - LSE2), dS = P (dP - D)
+          // every pair visible: P = 2^(S log2e scale - LSE2 [+ bias log2e]), dS = P (dP - D)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = 2 * e;
             float4 q4;
             if (MODE == kDkdv) q4 = lp[e];
             else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
-            const float pa = ex2(fmaf(__uint_as_float(sv[c]), sl2, q4.x));
-            const float pb = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, q4.y));
+            float xa = fmaf(__uint_as_float(sv[c]), sl2, q4.x);
+            float xb = fmaf(__uint_as_float(sv[c + 1]), sl2, q4.y);
+            if (BIAS == 2) {
+              xa = fmaf(bq4[c], kLog2e, xa);
+              xb = fmaf(bq4[c + 1], kLog2e, xb);
+            }
+            const float pa = ex2(xa), pb = ex2(xb);
             const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
             pk[e] = pack2(pa, pb, is_bf16);
             dk[e] = pack2(pa * ta, pb * tb, is_bf16);
           }
         } else {
-          // dQ with a bias: the chunk's 32 bias values of this row, 16 bytes at a time when the
-          // row address is 16-byte aligned and the chunk lies inside the row
-          const bool bvec = BIAS && MODE != kDkdv && brow != nullptr &&
+          // dQ with a bias from global memory: the chunk's 32 bias values of this row, 16 bytes
+          // at a time when the row address is 16-byte aligned and the chunk lies inside the row
+          const bool bvec = BIAS == 1 && MODE != kDkdv && brow != nullptr &&
                             (reinterpret_cast<uintptr_t>(brow + i0) & 15u) == 0 && i0 + 32 <= p.max_kv;
-          float bq4[32];
           if (bvec) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -500,10 +570,11 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             for (int u = 0; u < 2; ++u) {
               const int cc = i0 + c + u;  // sequence-local column: query row (dK/dV) or key (dQ)
               float x = __uint_as_float(sv[c + u]) * sl2;
-              if (BIAS && brow) {
-                // dQ: this row's bias, 16 bytes at a time when the chunk allows (bq4); else
-                // element by element (clamped into the sequence: masked columns read a valid
-                // address)
+              if (BIAS == 2) {
+                x = fmaf(bq4[c + u], kLog2e, x);
+              } else if (BIAS == 1 && brow) {
+                // element by element unless the chunk was loaded 16 bytes at a time (bq4),
+                // clamped into the sequence so that masked columns read a valid address
                 const float bv = MODE == kDkdv
                                      ? __ldg(brow + (size_t)(sq.q0 + min(cc, sq.q_len - 1)) * p.bias_heads * (size_t)p.max_kv)
                                      : (bvec ? bq4[c + u] : __ldg(brow + min(cc, sq.kv_len - 1)));
@@ -522,6 +593,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         if (MODE == kDkdv) tmem_st16(s_addr, pk);
         tmem_st16(MODE == kDqS ? s_addr : dp_addr, dk);
       }
+      if (BIAS == 2) mbar_arrive(bar(C::B_BE + n % C::NBS_));  // the bias slot may be refilled
       tmem_st_wait();
       fence_before();
       mbar_arrive(bar(C::B_P + b));
@@ -584,9 +656,10 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   }
 }
 
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1>
+// NBS > 0: the problem's bias is staged through TMA (the caller checked that it can be).
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS>
 cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
-  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1>;
+  using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS>;
   const int bf = p.dtype == VLF_BF16;
   BwdMaps m;
   const uint64_t tq = p.total_q, tk = p.total_kv;
@@ -602,6 +675,11 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
          make_tmap_16bit(&m.inner0, p.k, tk, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, IR, bf) &&
          make_tmap_16bit(&m.inner1, p.v, tk, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, IR, bf);
   }
+  if (NBS > 0)
+    ok = ok && make_tmap_bias(&m.bias, p.bias, tq, (uint64_t)p.bias_heads * p.max_kv,
+                              MODE == kDkdv ? IR : 128, MODE != kDkdv);
+  else
+    m.bias = m.inner0;  // (unused)
   if (!ok) return cudaErrorInvalidValue;
   const unsigned tiles = MODE == kDkdv ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128;
   const unsigned heads = MODE == kDkdv ? p.h_kv : p.h_q;
@@ -609,10 +687,16 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   Params pl = p;
   pl.heads_fast = p.bias != nullptr && p.bias_heads == 1;
   const dim3 grid = pl.heads_fast ? dim3(heads, tiles, p.num_seqs) : dim3(tiles, heads, p.num_seqs);
-  auto kern = p.bias ? (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true, true>
-                           : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false, true>)
-                     : (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, true, false>
-                           : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, false, false>);
+  void (*kern)(const BwdMaps, const Params);
+  if constexpr (NBS > 0) {
+    kern = bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, true, 2>
+              : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, false, 2>;
+  } else {
+    kern = p.bias ? (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, 0, true, 1>
+                        : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, 0, false, 1>)
+                  : (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, 0, true, 0>
+                        : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, 0, false, 0>);
+  }
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, C::SMEM, st>>>(m, pl);
@@ -621,20 +705,21 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   return e;
 }
 
-// Per head width: item rows, buffers and ring-0 / ring-1 stages of the dK/dV kernel (IR_KV,
-// NBUF_KV, NST_KV, NST1_KV) and the mode, item rows, buffers and ring stages of the dQ kernel
-// (MODE_Q, IR_Q, NBUF_Q, NST_Q, NST1_Q).  A ring slot is refilled only after its item's last
-// product has read it, so the rings are as deep as shared memory allows.
-template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int NST1_KV, int MODE_Q, int IR_Q,
-          int NBUF_Q, int NST_Q, int NST1_Q>
+// Per head width: item rows, buffers, ring-0 / ring-1 stages and bias stages of the dK/dV kernel
+// (IR_KV, NBUF_KV, NST_KV, NST1_KV, NBS_KV) and the mode, item rows, buffers, ring stages and
+// bias stages of the dQ kernel (MODE_Q, IR_Q, NBUF_Q, NST_Q, NST1_Q, NBS_Q).  A ring slot is
+// refilled only after its item's last product has read it, so the rings are as deep as shared
+// memory allows.
+template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int NST1_KV, int NBS_KV, int MODE_Q,
+          int IR_Q, int NBUF_Q, int NST_Q, int NST1_Q, int NBS_Q>
 cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   cudaError_t e;
   if ((e = mark(ev, 0, st)) != cudaSuccess) return e;
   if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV, NST1_KV>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV, NST1_KV, NBS_KV>(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<MODE_Q, DQK, DV, IR_Q, NBUF_Q, NST_Q, NST1_Q>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<MODE_Q, DQK, DV, IR_Q, NBUF_Q, NST_Q, NST1_Q, NBS_Q>(p, st)) != cudaSuccess) return e;
   return mark(ev, 3, st);
 }
 
@@ -648,10 +733,20 @@ bool tc_backward_supported(const Params &p) {
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   if (p.total_q == 0 || p.total_kv == 0) return simt_backward(p, st, ev);
-  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 6, 6, kDqS, 128, 2, 3, 3>(p, st, ev);
-  if (p.d_qk == 96) return bwd_shape<96, 96, 64, 2, 5, 4, kDqS, 128, 2, 3, 2>(p, st, ev);
-  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 5, 4, kDqS, 128, 2, 3, 2>(p, st, ev);
-  return bwd_shape<192, 128, 64, 1, 3, 3, kDq, 64, 2, 3, 3>(p, st, ev);
+  // A bias whose rows start 16-byte aligned streams through TMA in 64-row items (bias tiles take
+  // a third of shared memory: the Q / dO and K / V rings are shallower); other bias shapes load
+  // their values from global memory in the compute threads.
+  const bool bias_tma = p.bias != nullptr && p.max_kv % 4 == 0 &&
+                        (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0 && p.d_qk <= 128;
+  if (bias_tma) {
+    if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 4, 4, 3, kDq, 64, 2, 4, 4, 3>(p, st, ev);
+    if (p.d_qk == 96) return bwd_shape<96, 96, 64, 2, 2, 2, 3, kDq, 64, 2, 2, 2, 3>(p, st, ev);
+    return bwd_shape<128, 128, 64, 2, 2, 2, 3, kDq, 64, 2, 2, 2, 3>(p, st, ev);
+  }
+  if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 6, 6, 0, kDqS, 128, 2, 3, 3, 0>(p, st, ev);
+  if (p.d_qk == 96) return bwd_shape<96, 96, 64, 2, 5, 4, 0, kDqS, 128, 2, 3, 2, 0>(p, st, ev);
+  if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 5, 4, 0, kDqS, 128, 2, 3, 2, 0>(p, st, ev);
+  return bwd_shape<192, 128, 64, 1, 3, 3, 0, kDq, 64, 2, 3, 3, 0>(p, st, ev);
 }
 
 // The tensor-core backward writes dQ directly (no fp32 accumulator); only the row dot

@@ -334,5 +334,18 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// Shared-memory loads of data a TMA copy wrote (volatile: never hoisted above the mbarrier wait
+// that made it visible).
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float x;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(x) : "r"(a));
+  return x;
+}
+__device__ __forceinline__ float4 lds_f32x4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+
 }  // namespace tc
 }  // namespace vlf

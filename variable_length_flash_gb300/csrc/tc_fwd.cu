@@ -494,9 +494,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
 #pragma unroll
             for (int q = 0; q < kBN / 4; ++q) {
               const uint32_t a = rowb + (q >> 3) * C::BIAS_BOX + (((q & 7) ^ (r & 7)) << 4);
-              float4 bq;
-              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                           : "=f"(bq.x), "=f"(bq.y), "=f"(bq.z), "=f"(bq.w) : "r"(a));
+              const float4 bq = lds_f32x4(a);
               v[4 * q + 0] = __float_as_uint(fmaf(bq.x, kLog2e, __uint_as_float(v[4 * q + 0]) * sl2));
               v[4 * q + 1] = __float_as_uint(fmaf(bq.y, kLog2e, __uint_as_float(v[4 * q + 1]) * sl2));
               v[4 * q + 2] = __float_as_uint(fmaf(bq.z, kLog2e, __uint_as_float(v[4 * q + 2]) * sl2));
@@ -651,6 +649,24 @@ bool make_tmap_16bit(CUtensorMap *m, const void *base, uint64_t rows, uint64_t c
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the bias as [total_q][bias_heads x max_kv] fp32: box {32 columns, box_rows rows}
+// (128-byte rows), optionally 128-byte swizzled (threads that read along a row then take chunk
+// c at c ^ (row mod 8)).
+bool make_tmap_bias(CUtensorMap *m, const float *base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows, bool swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool tc_forward_supported(const Params &p) {
   if (p.dtype != VLF_F16 && p.dtype != VLF_BF16) return false;
   const bool shape = (p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 96 && p.d_v == 96) ||
@@ -672,21 +688,6 @@ bool make_tmap_q3(CUtensorMap *m, const void *base, uint64_t tokens, uint64_t he
   CUresult r = enc(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                    3, const_cast<void *>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// 2-D map over the bias as [total_q][bias_heads x max_kv] fp32: box {32 columns, 128 rows},
-// 128-byte swizzle (the softmax threads read their row's chunks at chunk ^ (row mod 8)).
-bool make_tmap_bias(CUtensorMap *m, const float *base, uint64_t rows, uint64_t cols) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (!enc || rows == 0 || cols == 0) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 4};
-  cuuint32_t box[2] = {32, 128};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -717,7 +718,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   // ring takes the room of a second CTA per SM); others are read row by row.
   const bool bias_tma = NT == 1 && !pack && p.bias != nullptr && p.max_kv % 4 == 0 &&
                         (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
-  if (bias_tma && !make_tmap_bias(&maps.bias, p.bias, p.total_q, (uint64_t)p.bias_heads * p.max_kv))
+  if (bias_tma && !make_tmap_bias(&maps.bias, p.bias, p.total_q, (uint64_t)p.bias_heads * p.max_kv, 128, true))
     return cudaErrorInvalidValue;
   if (!bias_tma) maps.bias = maps.q;
   // a head-broadcast bias: the heads of one row block run together and share its tiles in L2
