@@ -244,6 +244,13 @@ def main():
     ws = torch.empty(vlf.vlf_attn_varlen_bwd_workspace_size(
         w.total_q, w.total_kv, w.h_q, w.h_kv, w.d_qk, w.d_v, dt), dtype=torch.uint8, device=dev)
     kw = dict(scale=w.scale, causal=w.causal, window=w.window, bias=x["bias"])
+    # small-batch / decode shapes split each CTA's KV band (the library's choice); the parts'
+    # workspace is allocated once, outside the timed region
+    n_split = vlf.vlf_fwd_num_splits(w.num_seqs, w.max_seqlen_q, w.max_seqlen_kv, w.h_q, w.h_kv,
+                                     w.d_qk, w.d_v, dt)
+    fws = [torch.empty(max(1, vlf.vlf_attn_varlen_fwd_split_workspace_size(
+        w.total_q, w.h_q, w.d_v, n_split)), dtype=torch.uint8, device=dev) for _ in range(2)]
+    fkw = dict(num_splits=n_split)
 
     # a step is the forward and the backward; workloads without a backward (decode-sized,
     # latency-bound) time the forward alone
@@ -253,7 +260,8 @@ def main():
         if ev is not None:
             ev[0].record(stream)
         vlf.vlf_attn_varlen_fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_kv"],
-                                w.max_seqlen_q, w.max_seqlen_kv, out=out, lse=lse, **kw)
+                                w.max_seqlen_q, w.max_seqlen_kv, out=out, lse=lse,
+                                workspace=fws[0], **fkw, **kw)
         if fwd_only:
             if ev is not None:
                 ev[1].record(stream)
@@ -396,7 +404,7 @@ def main():
             s_cmp.wait_event(ev_dn[i])  # the read-back of step - 2 is done with set i
             vlf.vlf_attn_varlen_fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_kv"],
                                     w.max_seqlen_q, w.max_seqlen_kv, out=r["out"], lse=r["lse"],
-                                    stream=s_cmp, **kw)
+                                    stream=s_cmp, workspace=fws[i], **fkw, **kw)
             if not fwd_only:
                 vlf.vlf_attn_varlen_bwd(d["dout"], d["q"], d["k"], d["v"], r["out"], r["lse"],
                                         d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q,
@@ -452,6 +460,7 @@ def main():
                               if flush else f"inputs {in_bytes / 1e6:.0f} MB > 2 x L2 "
                               f"({l2_bytes / 1e6:.0f} MB): streamed from HBM, no flush"),
                        "fwd_path": "tcgen05" if fwd_path == 1 else "simt",
+                       "kv_splits": n_split,
                        "bwd_path": "tcgen05" if bwd_path == 1 else "simt"},
             "fwd_tflops": fwd_tflops, "fwd_frac_of_peak": fwd_tflops / peaks["bf16_tflops"],
             "fwd_bwd_frac_of_peak": value / world / peaks["bf16_tflops"],

@@ -57,7 +57,7 @@ typedef enum {
   VLF_ERR_LAUNCH = -4,      /* the CUDA runtime refused a launch or a query */
   VLF_ERR_TIMEOUT = -5,     /* device: a pipeline wait exceeded its time limit (kernel bailed out) */
   VLF_ERR_BAD_SEQLENS = -6, /* device: cu_seqlens not in [0, total], decreasing, or longer than max_seqlen */
-  VLF_ERR_WORKSPACE = -7    /* backward workspace missing or smaller than the size query returns */
+  VLF_ERR_WORKSPACE = -7    /* a workspace missing or smaller than its size query returns */
 } vlf_status;
 
 /* Extended-call flags (vlf_attn_varlen_fwd_ex / _bwd_ex). */
@@ -87,7 +87,8 @@ typedef enum {
  *   lse          NULL or fp32 [h_q, total_q]: natural-log log-sum-exp of each row's logits,
  *                -inf for a row that sees no key (its out row is 0).  Required by the backward.
  * Supported: dtype F16/BF16 with any 1 <= d_qk, d_v <= 256 (tensor-core kernels for
- * (d_qk, d_v) in {(64,64), (128,128), (192,128)}); dtype F32 with d_qk, d_v <= 256 (fp32 FMA).
+ * (d_qk, d_v) in {(64,64), (96,96), (128,128), (192,128)}); dtype F32 with d_qk, d_v <= 256
+ * (fp32 FMA).
  */
 int vlf_attn_varlen_fwd(const void *q, const void *k, const void *v,
                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
@@ -104,6 +105,55 @@ int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
                            float scale, int causal, int window,
                            const float *bias, int bias_heads,
                            void *out, float *lse, vlf_stream_t stream, unsigned flags);
+
+/*
+ * Split-KV forward, for problems whose (query tile, head) CTAs are too few to fill the GPU --
+ * small batches of decode steps (one query row per sequence against a long cache; the
+ * end-aligned causal rule serves cached decode, mtlattn 0.3.0, "Use") or short queries against
+ * long keys.
+ * Each CTA's KV band is cut into num_splits contiguous parts computed in parallel; each part
+ * writes its normalised fp32 result and its log-sum-exp L_s to the workspace, and a combine
+ * kernel writes out = sum_s exp(L_s - LSE) out_s and lse = LSE = log sum_s exp(L_s) -- the
+ * same softmax, summed in another order (results agree with vlf_attn_varlen_fwd to rounding).
+ *
+ *   arguments as vlf_attn_varlen_fwd_ex, plus
+ *   num_splits   0: the library's choice (vlf_fwd_num_splits); 1: unsplit; 2..64: that many
+ *                parts (some may be empty); num_splits * num_seqs <= 65535
+ *   workspace    device buffer of at least vlf_attn_varlen_fwd_split_workspace_size(total_q,
+ *                h_q, d_v, num_splits) bytes, owned by the caller, clobbered; may be NULL when
+ *                the call runs unsplit
+ * Shapes that cannot split (dtype F32, (d_qk, d_v) other than (64,64), (96,96), (128,128)) run
+ * the unsplit forward.  Returns VLF_ERR_WORKSPACE when a split call's workspace is missing or
+ * too small.
+ */
+int vlf_attn_varlen_fwd_split(const void *q, const void *k, const void *v,
+                              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv,
+                              int num_seqs, int total_q, int total_kv, int max_seqlen_q,
+                              int max_seqlen_kv, int h_q, int h_kv, int d_qk, int d_v, int dtype,
+                              float scale, int causal, int window,
+                              const float *bias, int bias_heads,
+                              void *out, float *lse, int num_splits,
+                              void *workspace, size_t workspace_bytes, vlf_stream_t stream,
+                              unsigned flags);
+
+/*
+ * The number of parts vlf_attn_varlen_fwd_split uses for num_splits = 0 (1: no split).  Pure
+ * host arithmetic on the launch shape, with two CTAs resident per SM as the "slots" of a wave:
+ * a grid below one wave is split into as many parts as keep it within one wave, each part at
+ * least 256 keys (at most 64 parts); a grid of one to three waves whose last wave is under 95%
+ * full gets 2 or 3 parts, whichever fills its waves better (the fewer on a tie), each at least
+ * 1024 keys; larger grids are not split.  num_sms <= 0 takes the current device's SM count
+ * (returns 1 if it cannot be queried).
+ */
+int vlf_fwd_num_splits(int num_seqs, int max_seqlen_q, int max_seqlen_kv, int h_q, int h_kv,
+                       int d_qk, int d_v, int dtype, unsigned flags, int num_sms);
+
+/*
+ * Bytes of workspace vlf_attn_varlen_fwd_split needs: fp32 parts [num_splits, total_q, h_q, d_v]
+ * and their log-sum-exps [num_splits, h_q, total_q], each rounded up to 256 bytes; 0 when
+ * num_splits < 2.  Pure host arithmetic.
+ */
+size_t vlf_attn_varlen_fwd_split_workspace_size(int total_q, int h_q, int d_v, int num_splits);
 
 /*
  * Bytes of fp32 workspace vlf_attn_varlen_bwd needs: the row dot products D = rowsum(dO o O),

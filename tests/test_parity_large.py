@@ -122,21 +122,26 @@ def test_full_size_workload(name):
     torch.cuda.empty_cache()
 
 
-def test_decode_full_size_packing_exact():
-    """decode64x8192_bf16_gqa at full size in bench.py's configuration: the forward packs each kv
-    head's 4 query heads into one tile; the unpacked layout gives identical bits (every row's
-    arithmetic is the same), and sampled sequences -- the last included, every head -- match
-    the oracle."""
+@pytest.mark.parametrize("name", ["decode64x8192_bf16_gqa", "decode4x32768_bf16_gqa"])
+def test_decode_full_size_packing_exact(name):
+    """The decode workloads at full size: the forward packs each kv head's 4 query heads into
+    one tile; unsplit, the unpacked layout gives identical bits (every row's arithmetic is the
+    same); in bench.py's configuration (the library's split of each cache: 2 and 9 parts)
+    sampled sequences -- the last included, every head -- match the oracle."""
     import variable_length_flash_gb300 as vlf
-    w = W.workload("decode64x8192_bf16_gqa")
+    w = W.workload(name)
     x = W.make_inputs(w, seed=0, device="cuda", with_dout=False)
     args = (x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_kv"], w.max_seqlen_q,
             w.max_seqlen_kv)
-    out, lse = vlf.vlf_attn_varlen_fwd(*args, scale=w.scale, causal=True)
-    out2, lse2 = vlf.vlf_attn_varlen_fwd(*args, scale=w.scale, causal=True,
+    out1, lse1 = vlf.vlf_attn_varlen_fwd(*args, scale=w.scale, causal=True, num_splits=1)
+    out2, lse2 = vlf.vlf_attn_varlen_fwd(*args, scale=w.scale, causal=True, num_splits=1,
                                          flags=vlf.VLF_FLAG_NO_PACK)
     assert vlf.vlf_check_error() == 0
-    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    del out1, lse1, out2, lse2
+    # the configuration bench.py times (the library's choice: each cache split in two parts)
+    out, lse = vlf.vlf_attn_varlen_fwd(*args, scale=w.scale, causal=True)
+    assert vlf.vlf_check_error() == 0
     rng = np.random.default_rng(0)
     seqs = sorted({0, w.num_seqs - 1} | set(int(s) for s in rng.integers(0, w.num_seqs, 4)))
     cq, ck = x["cu_seqlens_q"].tolist(), x["cu_seqlens_kv"].tolist()

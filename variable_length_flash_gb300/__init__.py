@@ -41,7 +41,8 @@ EXPORTS = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_fwd_ex", "vlf_attn_varlen_bwd
            "vlf_attn_varlen_bwd_ex", "vlf_attn_varlen_bwd_workspace_size", "vlf_check_error",
            "vlf_status_string", "vlf_sched_kv_band", "vlf_sched_q_band", "vlf_version",
            "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path", "vlf_attn_varlen_bwd_noalloc",
-           "vlf_noalloc_scratch_bytes"]
+           "vlf_noalloc_scratch_bytes", "vlf_attn_varlen_fwd_split", "vlf_fwd_num_splits",
+           "vlf_attn_varlen_fwd_split_workspace_size"]
 VLF_BWD_STAGES = 3
 BWD_STAGE_NAMES = ["rowdot", "dkdv", "dq"]
 
@@ -82,6 +83,12 @@ def _load():
     lib.vlf_version.restype = I
     lib.vlf_attn_varlen_bwd_noalloc.argtypes = bwd[:23] + [P, P, P, P]  # ... bias_heads, dq, dk, dv, stream
     lib.vlf_attn_varlen_bwd_noalloc.restype = I
+    lib.vlf_attn_varlen_fwd_split.argtypes = fwd[:22] + [I, P, Z, P, U]  # ..., out, lse, splits, ws, bytes, stream, flags
+    lib.vlf_attn_varlen_fwd_split.restype = I
+    lib.vlf_fwd_num_splits.argtypes = [I, I, I, I, I, I, I, I, U, I]
+    lib.vlf_fwd_num_splits.restype = I
+    lib.vlf_attn_varlen_fwd_split_workspace_size.argtypes = [I, I, I, I]
+    lib.vlf_attn_varlen_fwd_split_workspace_size.restype = Z
     lib.vlf_noalloc_scratch_bytes.argtypes = []
     lib.vlf_noalloc_scratch_bytes.restype = Z
     lib.vlf_launch_count.argtypes = []
@@ -167,6 +174,19 @@ def vlf_attn_varlen_bwd_workspace_size(total_q, total_kv, h_q, h_kv, d_qk, d_v, 
     return int(_lib.vlf_attn_varlen_bwd_workspace_size(total_q, total_kv, h_q, h_kv, d_qk, d_v, dt))
 
 
+def vlf_fwd_num_splits(num_seqs, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype,
+                       flags=0, num_sms=0) -> int:
+    """Parts the split-KV forward cuts each CTA's KV band into when left to choose (1: no
+    split); ``num_sms`` <= 0 takes the current device's SM count."""
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(_lib.vlf_fwd_num_splits(num_seqs, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v,
+                                       dt, flags, num_sms))
+
+
+def vlf_attn_varlen_fwd_split_workspace_size(total_q, h_q, d_v, num_splits) -> int:
+    return int(_lib.vlf_attn_varlen_fwd_split_workspace_size(total_q, h_q, d_v, num_splits))
+
+
 def _events(evs):
     if evs is None:
         return None, 0
@@ -209,11 +229,14 @@ def _bias_args(bias, total_q, h_q):
 
 def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_seqlen_kv=None,
                         scale=None, causal=False, window=0, bias=None, out=None, lse=None,
-                        stream=None, flags=0):
+                        stream=None, flags=0, num_splits=None, workspace=None):
     """Forward.  q [Tq,Hq,Dqk], k [Tkv,Hkv,Dqk], v [Tkv,Hkv,Dv] (fp16/bf16/fp32, CUDA,
     contiguous), cu_seqlens int32 [n+1].  Returns out [Tq,Hq,Dv] and lse fp32 [Hq,Tq].
     ``max_seqlen_kv=None`` reads it from cu_seqlens_kv (a host sync); the bias's last dim
-    must equal max_seqlen_kv when a bias is given."""
+    must equal max_seqlen_kv when a bias is given.  ``num_splits``: None lets the library
+    decide whether to split each CTA's KV band (small-batch / decode shapes; the parts' fp32
+    results go to ``workspace``, allocated here when not given), 1 never splits, k > 1 splits
+    into k parts."""
     _req(q, "q"), _req(k, "k", q.dtype), _req(v, "v", q.dtype)
     _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
     if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
@@ -232,6 +255,24 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
     if lse is None:
         lse = torch.empty((hq, tq), dtype=torch.float32, device=q.device)
     _req(out, "out", q.dtype), _req(lse, "lse", torch.float32)
+    nseq = cu_seqlens_q.numel() - 1
+    dt = _DTYPE[q.dtype]
+    if num_splits is None:
+        num_splits = _lib.vlf_fwd_num_splits(nseq, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
+                                             dqk, dv, dt, int(flags), 0)
+    if num_splits >= 2:
+        need = vlf_attn_varlen_fwd_split_workspace_size(tq, hq, dv, int(num_splits))
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        _req(workspace, "workspace")
+        st = _lib.vlf_attn_varlen_fwd_split(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), nseq, tq, tk,
+            int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv, dt,
+            float(scale) if scale else 0.0, int(bool(causal)), int(window or 0), _ptr(bias), bh,
+            _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream, q), int(flags))
+        _check(st, "vlf_attn_varlen_fwd_split")
+        return out, lse
     st = _lib.vlf_attn_varlen_fwd_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
         cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv,

@@ -210,6 +210,71 @@ int vlf_attn_varlen_fwd(const void *q, const void *k, const void *v, const int32
                                 causal, window, bias, bias_heads, out, lse, stream, 0u);
 }
 
+int vlf_fwd_num_splits(int num_seqs, int max_seqlen_q, int max_seqlen_kv, int h_q, int h_kv,
+                       int d_qk, int d_v, int dtype, unsigned flags, int num_sms) {
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 1;
+  }
+  return vlf::fwd_num_splits(num_seqs, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype,
+                             flags, num_sms);
+}
+
+size_t vlf_attn_varlen_fwd_split_workspace_size(int total_q, int h_q, int d_v, int num_splits) {
+  if (total_q < 0 || h_q < 1 || d_v < 1 || num_splits < 2) return 0;
+  const size_t rows = (size_t)num_splits * (size_t)total_q * (size_t)h_q;
+  const size_t o = (rows * (size_t)d_v * sizeof(float) + 255) & ~(size_t)255;
+  return o + ((rows * sizeof(float) + 255) & ~(size_t)255);
+}
+
+int vlf_attn_varlen_fwd_split(const void *q, const void *k, const void *v,
+                              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv,
+                              int num_seqs, int total_q, int total_kv, int max_seqlen_q,
+                              int max_seqlen_kv, int h_q, int h_kv, int d_qk, int d_v, int dtype,
+                              float scale, int causal, int window, const float *bias,
+                              int bias_heads, void *out, float *lse, int num_splits,
+                              void *workspace, size_t workspace_bytes, vlf_stream_t stream,
+                              unsigned flags) {
+  int st = check_common(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+                        max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, bias, bias_heads);
+  if (st != VLF_OK) return st;
+  if (num_splits < 0) return VLF_ERR_INVALID;
+  if (total_q > 0 && !out) return VLF_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(lse) || !aligned16(workspace)) return VLF_ERR_ALIGN;
+  if (num_seqs == 0 || max_seqlen_q == 0) return VLF_OK;
+  vlf::Params p;
+  fill_common(p, q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, max_seqlen_q,
+              max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, scale, causal, window, bias, bias_heads,
+              flags);
+  p.out = out;
+  p.lse = lse;
+  p.err = error_word_ptr();
+  if (!p.err) return VLF_ERR_LAUNCH;
+  if (num_splits == 0)
+    num_splits = vlf_fwd_num_splits(num_seqs, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v,
+                                    dtype, flags, 0);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (num_splits >= 2 && !(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_forward_splittable(p)) {
+    if (num_splits > 64 || (long long)num_splits * num_seqs > 65535) return VLF_ERR_UNSUPPORTED;
+    const size_t need = vlf_attn_varlen_fwd_split_workspace_size(total_q, h_q, d_v, num_splits);
+    if (!workspace || workspace_bytes < need) return VLF_ERR_WORKSPACE;
+    const size_t rows = (size_t)num_splits * (size_t)total_q * (size_t)h_q;
+    p.kv_splits = num_splits;
+    p.o_part = static_cast<float *>(workspace);
+    p.lse_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                           ((rows * (size_t)d_v * sizeof(float) + 255) & ~(size_t)255));
+    e = vlf::tc_forward_split(p, cs);
+  } else if (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_forward_supported(p)) {
+    e = vlf::tc_forward(p, cs);
+  } else {
+    e = vlf::simt_forward(p, cs);
+  }
+  return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
+}
+
 size_t vlf_attn_varlen_bwd_workspace_size(int total_q, int total_kv, int h_q, int h_kv, int d_qk,
                                           int d_v, int dtype) {
   (void)total_kv; (void)h_kv; (void)d_v;

@@ -34,6 +34,12 @@ struct Params {
   // set by a launcher: grid x enumerates heads (y the row blocks), so that the CTAs reading the
   // same tiles of a head-broadcast bias run together and share them through L2
   int heads_fast = 0;
+  // split-KV forward: kv_splits > 1 cuts each CTA's KV band into kv_splits contiguous parts
+  // (grid z = sequence * kv_splits + part); each part writes its normalised fp32 result and its
+  // log-sum-exp, which a combine kernel merges into out / lse
+  int kv_splits = 1;
+  float *o_part = nullptr;    // [kv_splits, total_q, h_q, d_v]
+  float *lse_part = nullptr;  // [kv_splits, h_q, total_q]
 };
 
 // ---------------------------------------------------------------- element access

@@ -17,6 +17,14 @@ cudaError_t simt_backward(const Params &p, cudaStream_t st, const cudaEvent_t *e
 // Tensor-core kernels (tc_fwd.cu / tc_bwd.cu).  `supported` says whether the shape has one.
 bool tc_forward_supported(const Params &p);
 cudaError_t tc_forward(const Params &p, cudaStream_t st);
+// Split-KV forward (p.kv_splits > 1, p.o_part / p.lse_part set): the parts, then their combine.
+// Only shapes with one query tile per CTA split (tc_forward_splittable).
+bool tc_forward_splittable(const Params &p);
+cudaError_t tc_forward_split(const Params &p, cudaStream_t st);
+// The number of parts the library would cut each CTA's KV band into (1: no split), from the
+// problem's launch shape and the device's SM count.
+int fwd_num_splits(int num_seqs, int max_q, int max_kv, int h_q, int h_kv, int d_qk, int d_v,
+                   int dtype, unsigned flags, int num_sms);
 bool tc_backward_supported(const Params &p);
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev);
 size_t tc_backward_workspace(int total_q, int h_q, int d_qk);

@@ -36,6 +36,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -159,15 +161,21 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
 // not PACK); separate instantiations, so that kernels without a bias carry none of its code or
 // registers.
 // PACK (NT = 1 only): the G query heads of a kv head share each tile (decode-sized problems).
-template <int DQK, int DV, int NK, int NV, int NT, bool BF16, int BIAS, bool PACK>
+// SPLIT (NT = 1, BIAS 0 or 1): split-KV part kernel -- the CTA takes part blockIdx.z mod
+// p.kv_splits of its KV band and writes fp32 partial results (a separate instantiation, so that
+// the unsplit kernels carry none of its code or registers).
+template <int DQK, int DV, int NK, int NV, int NT, bool BF16, int BIAS, bool PACK, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, NT == 1 ? 2 : 1)
 tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   constexpr int NBS = BIAS == 2 ? 2 : 0;
   static_assert(BIAS != 2 || (NT == 1 && !PACK), "bias tiles through TMA: one unpacked tile");
+  static_assert(!SPLIT || (NT == 1 && BIAS != 2), "split-KV parts: one tile, no bias ring");
   using C = FwdCfg<DQK, DV, NK, NV, NT, NBS>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const bool pair_heads = NT == 2 && (p.group % 2 == 0);
-  const int s = blockIdx.z;
+  // (split-KV: the part index is recomputed where it is needed, so that it is not held in a
+  // register through the main loop)
+  const int s = SPLIT ? (int)blockIdx.z / p.kv_splits : (int)blockIdx.z;
   Seq sq;
   if (!load_seq(p, s, sq)) return;
   if (s == 0 && (__ldg(p.cu_q) != 0 || __ldg(p.cu_kv) != 0)) set_error(p.err, VLF_ERR_BAD_SEQLENS);
@@ -183,6 +191,15 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   static_assert(!PACK || NT == 1, "packed heads use one query tile per CTA");
   tile_info<NT, PACK>(p, sq, bx, by, pair_heads, ti);
   if (ti.row0[0] >= sq.q_len) return;  // whole CTA beyond this sequence
+  if (SPLIT) {
+    // this part's share of the band, in whole KV tiles (possibly none: it then writes O = 0
+    // and LSE = -inf, which the combine weighs by zero)
+    const int part = (int)blockIdx.z % p.kv_splits;
+    const int per = (ti.hi - ti.lo + p.kv_splits - 1) / p.kv_splits;
+    const int a = min(ti.hi, ti.lo + part * per), b = min(ti.hi, a + per);
+    ti.jlo[0] = ti.lo = a;
+    ti.jhi[0] = ti.hi = b;
+  }
 
   // The kernel has no static shared memory, so the dynamic window starts 1024-byte aligned, as
   // the 128-byte swizzle atoms of the TMA tiles and MMA descriptors require; refuse otherwise.
@@ -577,7 +594,35 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       ok = mbar_wait(bar(C::B_O + 2 * t + (np & 1)), (np >> 1) & 1, abort_flag, p.err);
     }
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    if (SPLIT && ok) {
+      // a part's result for the combine: fp32 O / l and the part's log-sum-exp
+      fence_after();
+      const int part = (int)blockIdx.z % p.kv_splits;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t grow = (size_t)sq.q0 + (size_t)(row_ok ? i : 0);
+      float4 *dst = reinterpret_cast<float4 *>(p.o_part + (((size_t)part * p.total_q + grow) * p.h_q + head) * DV);
+#pragma unroll 1
+      for (int ch = 0; ch < DV / 32; ++ch) {
+        uint32_t v[32];
+        if (nt > 0) {
+          __syncwarp();
+          tmem_ld32(o_addr + ch * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[ch * 8 + q4] = make_float4(__uint_as_float(v[4 * q4]) * inv, __uint_as_float(v[4 * q4 + 1]) * inv,
+                                           __uint_as_float(v[4 * q4 + 2]) * inv, __uint_as_float(v[4 * q4 + 3]) * inv);
+        }
+      }
+      if (row_ok)
+        p.lse_part[((size_t)part * p.h_q + head) * p.total_q + grow] =
+            lf > 0.f ? (m_ref + lg2(lf)) * kLn2 : -INFINITY;
+    } else if (!SPLIT && ok) {
       fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const size_t grow = (size_t)sq.q0 + (size_t)(row_ok ? i : 0);
@@ -615,6 +660,59 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+// Merges the parts of a split-KV forward.  With L_s the parts' log-sum-exps and O_s their
+// normalised results: LSE = log sum_s exp(L_s), O = sum_s exp(L_s - LSE) O_s (a part that saw no
+// key has L_s = -inf and weight 0; a row no part saw gets O = 0, LSE = -inf).  One warp per
+// (query row, head); lane c reads columns c, c + 32, ... of every part (coalesced rows).
+template <int DV, bool BF16>
+__global__ void __launch_bounds__(256) split_combine_kernel(const Params p) {
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (w >= (long long)p.total_q * p.h_q) return;
+  const int lane = threadIdx.x & 31;
+  const int row = (int)(w / p.h_q), head = (int)(w % p.h_q);
+  const int S = p.kv_splits;
+  auto part_lse = [&](int sp) { return p.lse_part[((size_t)sp * p.h_q + head) * p.total_q + row]; };
+  float m = -INFINITY;
+  for (int sp = lane; sp < S; sp += 32) m = fmaxf(m, part_lse(sp));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+  if (m != -INFINITY)
+    for (int sp = lane; sp < S; sp += 32) sum += expf(part_lse(sp) - m);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float lse = m == -INFINITY ? -INFINITY : m + logf(sum);
+  constexpr int NC = DV / 32;
+  float acc[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+  if (lse != -INFINITY) {
+    for (int sp = 0; sp < S; ++sp) {
+      const float wgt = expf(part_lse(sp) - lse);
+      const float *src = p.o_part + (((size_t)sp * p.total_q + row) * p.h_q + head) * DV;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) acc[c] = fmaf(wgt, src[lane + 32 * c], acc[c]);
+    }
+  }
+  T *dst = static_cast<T *>(p.out) + ((size_t)row * p.h_q + head) * DV;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) dst[lane + 32 * c] = from_f32<T>(acc[c]);
+  if (lane == 0 && p.lse) p.lse[(size_t)head * p.total_q + row] = lse;
+}
+
+template <int DV>
+cudaError_t launch_combine(const Params &p, cudaStream_t st) {
+  const long long pairs = (long long)p.total_q * p.h_q;
+  if (pairs == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((pairs + 7) / 8);
+  if (p.dtype == VLF_BF16) split_combine_kernel<DV, true><<<blocks, 256, 0, st>>>(p);
+  else split_combine_kernel<DV, false><<<blocks, 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -692,6 +790,22 @@ bool make_tmap_q3(CUtensorMap *m, const void *base, uint64_t tokens, uint64_t he
   return r == CUDA_SUCCESS;
 }
 
+// The kernel instantiation for a dtype and bias kind (0 none, 1 rows from global memory, 2 TMA
+// tiles: unpacked, unsplit, one tile per CTA only).
+template <int DQK, int DV, int NK, int NV, int NT, bool PACK, bool SPLIT>
+void (*pick_fwd(bool bf, int bias_kind))(const FwdMaps, const Params) {
+  if constexpr (NT == 1 && !PACK && !SPLIT) {
+    if (bias_kind == 2)
+      return bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 2, false, false>
+                : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 2, false, false>;
+  }
+  if (bias_kind != 0)
+    return bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 1, PACK, SPLIT>
+              : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 1, PACK, SPLIT>;
+  return bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 0, PACK, SPLIT>
+            : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 0, PACK, SPLIT>;
+}
+
 template <int DQK, int DV, int NK, int NV, int NT>
 cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   using C = FwdCfg<DQK, DV, NK, NV, NT>;
@@ -714,9 +828,12 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   const unsigned blocks = (unsigned)((p.max_q + rows_per_cta - 1) / rows_per_cta);
   const unsigned heads = pack ? p.h_kv : (pair_heads ? p.h_q / 2 : p.h_q);
   if (blocks == 0) return cudaSuccess;
+  // split-KV parts (NT = 1): grid z enumerates (sequence, part); their bias rows are read with
+  // per-thread loads (the parts keep two CTAs per SM)
+  const bool split = NT == 1 && p.kv_splits > 1;
   // A bias whose rows are 16-byte aligned goes through TMA tiles (one unpacked tile per CTA; the
   // ring takes the room of a second CTA per SM); others are read row by row.
-  const bool bias_tma = NT == 1 && !pack && p.bias != nullptr && p.max_kv % 4 == 0 &&
+  const bool bias_tma = NT == 1 && !pack && !split && p.bias != nullptr && p.max_kv % 4 == 0 &&
                         (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
   if (bias_tma && !make_tmap_bias(&maps.bias, p.bias, p.total_q, (uint64_t)p.bias_heads * p.max_kv, 128, true))
     return cudaErrorInvalidValue;
@@ -724,31 +841,24 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   // a head-broadcast bias: the heads of one row block run together and share its tiles in L2
   Params pl = p;
   pl.heads_fast = p.bias != nullptr && p.bias_heads == 1 && !pack;
-  const dim3 grid = pl.heads_fast ? dim3(heads, blocks, p.num_seqs) : dim3(blocks, heads, p.num_seqs);
+  const unsigned zdim = (unsigned)p.num_seqs * (split ? (unsigned)p.kv_splits : 1u);
+  if (zdim > 65535u) return cudaErrorInvalidValue;
+  const dim3 grid = pl.heads_fast ? dim3(heads, blocks, zdim) : dim3(blocks, heads, zdim);
   using K = void (*)(const FwdMaps, const Params);
   K kern;
   int smem = C::SMEM;
-  if (pack) {
-    if constexpr (NT == 1)
-      kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 1, true>
-                          : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 1, true>)
-                    : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 0, true>
-                          : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 0, true>);
+  const int bias_kind = p.bias ? (bias_tma ? 2 : 1) : 0;
+  if constexpr (NT == 1) {
+    if (split)
+      kern = pack ? pick_fwd<DQK, DV, NK, NV, NT, true, true>(bf, bias_kind)
+                  : pick_fwd<DQK, DV, NK, NV, NT, false, true>(bf, bias_kind);
     else
-      return cudaErrorInvalidValue;
-  } else if (bias_tma) {
-    if constexpr (NT == 1) {
-      kern = bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 2, false>
-                : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 2, false>;
-      smem = FwdCfg<DQK, DV, NK, NV, NT, 2>::SMEM;
-    } else {
-      return cudaErrorInvalidValue;
-    }
+      kern = pack ? pick_fwd<DQK, DV, NK, NV, NT, true, false>(bf, bias_kind)
+                  : pick_fwd<DQK, DV, NK, NV, NT, false, false>(bf, bias_kind);
+    if (bias_tma) smem = FwdCfg<DQK, DV, NK, NV, NT, 2>::SMEM;
   } else {
-    kern = p.bias ? (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 1, false>
-                        : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 1, false>)
-                  : (bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 0, false>
-                        : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 0, false>);
+    if (pack || split || bias_tma) return cudaErrorInvalidValue;
+    kern = pick_fwd<DQK, DV, NK, NV, NT, false, false>(bf, bias_kind);
   }
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
@@ -758,6 +868,58 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   return e;
 }
 }  // namespace
+
+bool tc_forward_splittable(const Params &p) {
+  return tc_forward_supported(p) && p.d_qk == p.d_v && p.d_qk <= 128;  // one query tile per CTA
+}
+
+cudaError_t tc_forward_split(const Params &p, cudaStream_t st) {
+  if (!tc_forward_splittable(p) || p.kv_splits < 2 || !p.o_part || !p.lse_part) return cudaErrorInvalidValue;
+  cudaError_t e = tc_forward(p, st);
+  if (e != cudaSuccess || p.total_q == 0 || p.total_kv == 0) return e;  // (empty: plain path ran)
+  if (p.d_v == 64) return launch_combine<64>(p, st);
+  if (p.d_v == 96) return launch_combine<96>(p, st);
+  return launch_combine<128>(p, st);
+}
+
+// Parts per CTA band: split when the unsplit grid leaves SMs idle (fewer CTAs than two per SM,
+// the residency of one-tile CTAs), into as many parts as keep the grid within one such wave,
+// each part at least four KV tiles long (a part costs a prologue, an fp32 partial write and a
+// read in the combine).  Between one and three waves, a grid whose last wave is partly empty
+// (under 95% wave efficiency) is cut into 2 or 3 parts, whichever fills its waves better (the
+// fewer on a tie), each part at least 16 KV tiles: shorter CTAs shorten the partly occupied
+// tail (measured on decode rows x 8 kv heads against 4096-16384 keys: 5-28% faster).
+int fwd_num_splits(int num_seqs, int max_q, int max_kv, int h_q, int h_kv, int d_qk, int d_v,
+                   int dtype, unsigned flags, int num_sms) {
+  if ((dtype != VLF_F16 && dtype != VLF_BF16) || (flags & VLF_FLAG_FORCE_SIMT)) return 1;
+  if (d_qk != d_v || (d_qk != 64 && d_qk != 96 && d_qk != 128)) return 1;
+  if (num_seqs < 1 || max_q < 1 || max_kv < 1 || h_kv < 1 || h_q % h_kv != 0 || num_sms < 1) return 1;
+  const int group = h_q / h_kv;
+  const bool pack = group >= 2 && 128 % group == 0 && (long long)max_q * group <= 128 &&
+                    !(flags & VLF_FLAG_NO_PACK);
+  const long long rows = pack ? 128 / group : 128;
+  const long long ctas = (max_q + rows - 1) / rows * (pack ? h_kv : h_q) * (long long)num_seqs;
+  const long long slots = 2LL * num_sms;
+  const long long tiles = ((long long)max_kv + kBN - 1) / kBN;
+  if (ctas >= slots) {
+    if (ctas >= 3 * slots) return 1;
+    // wave efficiency of sp parts: ctas * sp / (slots * waves), compared by cross-multiplying
+    auto waves = [&](long long sp) { return (ctas * sp + slots - 1) / slots; };
+    if (ctas * 100 >= 95 * slots * waves(1)) return 1;
+    int best = 1;
+    for (int sp = 2; sp <= 3; ++sp) {
+      if (tiles < 16 * sp || (long long)sp * num_seqs > 65535) break;
+      if (best == 1 || ctas * sp * waves(best) > ctas * best * waves(sp)) best = sp;
+    }
+    return best;
+  }
+  const long long by_grid = slots / ctas;
+  const long long by_len = tiles / 4;
+  long long sp = by_grid < by_len ? by_grid : by_len;
+  if (sp > 64) sp = 64;
+  if (sp * num_seqs > 65535) sp = 65535 / num_seqs;
+  return sp < 2 ? 1 : (int)sp;
+}
 
 cudaError_t tc_forward(const Params &p, cudaStream_t st) {
   if (p.d_qk == 64) return launch_fwd<64, 64, 3, 3, 1>(p, st);

@@ -16,6 +16,10 @@ Workloads (named by what they are; the shapes are the benchmark configurations o
 * ``long49152_fp16_bias_alibi`` / ``long49152_fp16_bias_prefix`` -- one sequence of 49,152
   tokens, H=16, head_dim 128, q/k/v ~ N(0, 0.5^2), fp16, additive fp32 bias: prefix-LM 0/-inf
   plus per-head ALiBi (per-head bias tensor), or the prefix-LM part alone broadcast over heads.
+* ``decode64x8192_bf16_gqa`` / ``decode4x32768_bf16_gqa`` -- one new query row per sequence
+  against a cache of 8192 (64 sequences) or 32,768 tokens (4 sequences), H_q=32, H_kv=8, head
+  dim 128, end-aligned causal, bf16, forward only.
+* ``dense4x4096_bf16_causal_d96`` -- the dense configuration at head width 96.
 
 Draw order: the ragged lengths come from a CPU ``torch.Generator`` seeded with ``seed``; the
 tensors from a generator on the target device seeded with ``seed``, in the order q, k, v, dout,
@@ -118,6 +122,11 @@ def workload(name: str, seed: int = 0) -> Workload:
         # row sees every key), GQA 4, forward only
         return Workload(name, "bf16", [1] * 64, [8192] * 64, 32, 8, 128, 128, causal=True,
                         backward=False)
+    if name == "decode4x32768_bf16_gqa":
+        # a small batch of decode steps against long caches (4 rows x 8 kv heads: too few
+        # CTAs to fill the GPU unless each cache is split), GQA 4, forward only
+        return Workload(name, "bf16", [1] * 4, [32768] * 4, 32, 8, 128, 128, causal=True,
+                        backward=False)
     if name in ("long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix"):
         lens = [49152]
         return Workload(name, "fp16", lens, lens, 16, 16, 128, 128, causal=False, sigma=0.5,
@@ -128,7 +137,7 @@ def workload(name: str, seed: int = 0) -> Workload:
 WORKLOADS = ["varlen64_fp16_full", "varlen64_fp16_causal", "dense4x4096_bf16_causal",
              "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
              "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "decode64x8192_bf16_gqa",
-             "dense4x4096_bf16_causal_d96"]
+             "dense4x4096_bf16_causal_d96", "decode4x32768_bf16_gqa"]
 
 
 def custom(lengths_q, lengths_kv=None, *, dtype="bf16", h_q=4, h_kv=None, d_qk=64, d_v=None,
