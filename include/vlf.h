@@ -87,8 +87,8 @@ typedef enum {
  *   lse          NULL or fp32 [h_q, total_q]: natural-log log-sum-exp of each row's logits,
  *                -inf for a row that sees no key (its out row is 0).  Required by the backward.
  * Supported: dtype F16/BF16 with any 1 <= d_qk, d_v <= 256 (tensor-core kernels for
- * (d_qk, d_v) in {(64,64), (96,96), (128,128), (192,128)}); dtype F32 with d_qk, d_v <= 256
- * (fp32 FMA).
+ * (d_qk, d_v) in {(64,64), (96,96), (128,128), (192,128), (256,256)}); dtype F32 with d_qk,
+ * d_v <= 256 (fp32 FMA).
  */
 int vlf_attn_varlen_fwd(const void *q, const void *k, const void *v,
                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
@@ -122,8 +122,8 @@ int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
  *   workspace    device buffer of at least vlf_attn_varlen_fwd_split_workspace_size(total_q,
  *                h_q, d_v, num_splits) bytes, owned by the caller, clobbered; may be NULL when
  *                the call runs unsplit
- * Shapes that cannot split (dtype F32, (d_qk, d_v) other than (64,64), (96,96), (128,128)) run
- * the unsplit forward.  Returns VLF_ERR_WORKSPACE when a split call's workspace is missing or
+ * Shapes that cannot split (dtype F32, (d_qk, d_v) other than (64,64), (96,96), (128,128),
+ * (256,256)) run the unsplit forward.  Returns VLF_ERR_WORKSPACE when a split call's workspace is missing or
  * too small.
  */
 int vlf_attn_varlen_fwd_split(const void *q, const void *k, const void *v,
@@ -138,7 +138,8 @@ int vlf_attn_varlen_fwd_split(const void *q, const void *k, const void *v,
 
 /*
  * The number of parts vlf_attn_varlen_fwd_split uses for num_splits = 0 (1: no split).  Pure
- * host arithmetic on the launch shape, with two CTAs resident per SM as the "slots" of a wave:
+ * host arithmetic on the launch shape, with the CTAs resident per SM (two; one at width 256)
+ * as the "slots" of a wave:
  * a grid below one wave is split into as many parts as keep it within one wave, each part at
  * least 256 keys (at most 64 parts); a grid of one to three waves whose last wave is under 95%
  * full gets 2 or 3 parts, whichever fills its waves better (the fewer on a tie), each at least

@@ -1,6 +1,6 @@
 """GPU vs fp64 oracle, every element, on small varlen problems that still span several tiles
 and ragged tails: dtypes x {self, cross} x {causal, window, GQA/MQA, bias dim1 in {1, H}} x head
-widths {64, 96, 128, 192/128, odd}, lengths including 0, 1, 15-17, 127-129 and thousands of tiny
+widths {64, 96, 128, 192/128, 256, odd}, lengths including 0, 1, 15-17, 127-129 and thousands of tiny
 windows.  Also: tile skipping is exact (skip on/off give identical bits), bad cu_seqlens are
 reported through the device error word, and the SIMT and tensor-core paths both pass."""
 import numpy as np
@@ -37,6 +37,11 @@ CASES = {
                                     causal=True, window=100),
     "fp16_d96_decode_gqa4": W.custom([1, 1, 3], [200, 1, 700], dtype="fp16", h_q=8, h_kv=2,
                                      d_qk=96, causal=True),
+    # width 256: tensor-core forward (one CTA per SM, 256-column O), SIMT backward
+    "bf16_d256_gqa_causal": W.custom([129, 1, 300, 64], dtype="bf16", h_q=4, h_kv=2, d_qk=256,
+                                     causal=True),
+    "fp16_d256_decode_gqa4_window": W.custom([1, 2, 1], [700, 90, 1500], dtype="fp16", h_q=8,
+                                             h_kv=2, d_qk=256, causal=True, window=600),
     "bf16_empty_seqs": W.custom([0, 5, 0, 130], [3, 5, 0, 130], dtype="bf16", h_q=2, d_qk=64,
                                 causal=False),
     # decode-sized problems (the forward packs a kv head's G query heads into one tile)
@@ -78,7 +83,9 @@ def test_parity_case(name):
     # max_seqlen_kv not a multiple of 4: bias rows are read row by row instead of through TMA
     ("bf16", 4, True, 128, 0, (70, 1, 141)),
     # enough items per CTA that both backward kernels' bias rings wrap several times
-    ("fp16", 4, True, 96, 0, (300, 1, 257)), ("bf16", 1, False, 64, 0, (384, 129, 200))])
+    ("fp16", 4, True, 96, 0, (300, 1, 257)), ("bf16", 1, False, 64, 0, (384, 129, 200)),
+    # width 256: bias rows read by the softmax threads (no room for a bias ring)
+    ("bf16", 4, True, 256, 0, (70, 1, 140))])
 def test_parity_bias(dtype, heads, causal, d, window, lengths):
     """Bias tiles through TMA (D 64/128, rows 16-byte aligned), row by row otherwise, with the
     heads of a row block run together for a head-broadcast bias."""

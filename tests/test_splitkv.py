@@ -38,6 +38,8 @@ def test_num_splits_choice():
     # parts of at least four 64-key tiles
     assert f(1, 1, 300, 8, 8, 128, 128, bf16, num_sms=152) == 1
     assert f(1, 1, 512, 8, 8, 128, 128, bf16, num_sms=152) == 2
+    # width 256: one CTA per SM (152 slots)
+    assert f(4, 1, 32768, 32, 8, 256, 256, bf16, num_sms=152) == 4
     # at most 64 parts
     assert f(1, 1, 1 << 20, 1, 1, 64, 64, bf16, num_sms=152) == 64
     # unpacked tiles: 2 row blocks x 4 heads
@@ -46,7 +48,7 @@ def test_num_splits_choice():
     assert f(1, 1, 65536, 8, 8, 192, 128, bf16, num_sms=152) == 1
     assert f(1, 1, 65536, 8, 8, 128, 128, torch.float32, num_sms=152) == 1
     assert f(1, 1, 65536, 8, 8, 128, 128, bf16, flags=vlf.VLF_FLAG_FORCE_SIMT, num_sms=152) == 1
-    assert f(1, 1, 65536, 8, 8, 256, 256, bf16, num_sms=152) == 1
+    assert f(1, 1, 65536, 8, 8, 256, 128, bf16, num_sms=152) == 1
 
 
 CASES = {
@@ -59,6 +61,9 @@ CASES = {
     # unpacked tiles (no GQA), two row blocks in one sequence, no mask
     "bf16_d96_two_blocks": (W.custom([130, 5], [2000, 130], dtype="bf16", h_q=2, d_qk=96,
                                      causal=False), (3,)),
+    # width 256 (one CTA per SM, 256-column O), packed decode tiles
+    "bf16_d256_decode": (W.custom([1, 1, 2], [2000, 700, 3000], dtype="bf16", h_q=8, h_kv=2,
+                                  d_qk=256, causal=True), (3, 9)),
     # more parts than the band has tiles: empty parts
     "bf16_parts_exceed_tiles": (W.custom([1, 2], [100, 40], dtype="bf16", h_q=4, h_kv=1,
                                          d_qk=128, causal=True), (8, 64)),

@@ -93,15 +93,19 @@ struct FwdCfg {
   // (no alignment slack: the dynamic shared window starts 1024-byte aligned, checked in-kernel)
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr int THREADS = NT == 2 ? 416 : 256;
-  // TMEM: query tile t's two 64-column S buffers at 128 t, its O at O_COL + 128 t
-  static constexpr uint32_t TMEM_COLS = 256 * NT, O_COL = 128 * NT;
+  // TMEM: query tile t's two 64-column S buffers at 128 t, its O at O_COL + 128 t.  WIDE
+  // (width 256, NT = 1): O takes 256 columns and the CTA the whole TMEM -- one CTA per SM, as its
+  // shared memory (a 64 KB Q tile, 32 KB K / V slots) already is.
+  static constexpr bool WIDE = NV_PAD > 128;
+  static constexpr uint32_t TMEM_COLS = WIDE ? 512 : 256 * NT, O_COL = 128 * NT;
+  static constexpr int MIN_BLOCKS = NT == 1 && !WIDE ? 2 : 1;  // CTAs resident per SM
   // The producer issues K(j + LEAD) before V(j).  A K or V tile waits for its ring slot; with
   // one query tile a K load must not queue behind a V slot that frees late, so K leads by one.
   static constexpr int LEAD = NT == 1 ? 1 : 0;
   static_assert(NT == 1 || NT == 2, "query tiles per CTA");
   static_assert(NV >= 2 && NK >= 2, "ring depth");
-  static_assert(DQK % 32 == 0 && DV % 32 == 0 && NV_PAD <= 128, "tile shapes");
-  static_assert(SMEM <= (NT == 2 || NBS > 0 ? 232448 : 115712), "shared memory");  // NT = 1: two per SM
+  static_assert(DQK % 32 == 0 && DV % 32 == 0 && NV_PAD <= (NT == 1 ? 256 : 128), "tile shapes");
+  static_assert(SMEM <= (MIN_BLOCKS == 1 || NBS > 0 ? 232448 : 115712), "shared memory");
 };
 
 // Time-bounded wait that ignores the abort flag (used to drain in-flight work at teardown).
@@ -165,7 +169,7 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
 // p.kv_splits of its KV band and writes fp32 partial results (a separate instantiation, so that
 // the unsplit kernels carry none of its code or registers).
 template <int DQK, int DV, int NK, int NV, int NT, bool BF16, int BIAS, bool PACK, bool SPLIT>
-__global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, NT == 1 ? 2 : 1)
+__global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, FwdCfg<DQK, DV, NK, NV, NT>::MIN_BLOCKS)
 tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
   constexpr int NBS = BIAS == 2 ? 2 : 0;
   static_assert(BIAS != 2 || (NT == 1 && !PACK), "bias tiles through TMA: one unpacked tile");
@@ -768,7 +772,8 @@ bool make_tmap_bias(CUtensorMap *m, const float *base, uint64_t rows, uint64_t c
 bool tc_forward_supported(const Params &p) {
   if (p.dtype != VLF_F16 && p.dtype != VLF_BF16) return false;
   const bool shape = (p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 96 && p.d_v == 96) ||
-                     (p.d_qk == 128 && p.d_v == 128) || (p.d_qk == 192 && p.d_v == 128);
+                     (p.d_qk == 128 && p.d_v == 128) || (p.d_qk == 192 && p.d_v == 128) ||
+                     (p.d_qk == 256 && p.d_v == 256);
   return shape;
 }
 
@@ -794,7 +799,7 @@ bool make_tmap_q3(CUtensorMap *m, const void *base, uint64_t tokens, uint64_t he
 // tiles: unpacked, unsplit, one tile per CTA only).
 template <int DQK, int DV, int NK, int NV, int NT, bool PACK, bool SPLIT>
 void (*pick_fwd(bool bf, int bias_kind))(const FwdMaps, const Params) {
-  if constexpr (NT == 1 && !PACK && !SPLIT) {
+  if constexpr (NT == 1 && !PACK && !SPLIT && DV <= 128) {
     if (bias_kind == 2)
       return bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 2, false, false>
                 : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 2, false, false>;
@@ -833,7 +838,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   const bool split = NT == 1 && p.kv_splits > 1;
   // A bias whose rows are 16-byte aligned goes through TMA tiles (one unpacked tile per CTA; the
   // ring takes the room of a second CTA per SM); others are read row by row.
-  const bool bias_tma = NT == 1 && !pack && !split && p.bias != nullptr && p.max_kv % 4 == 0 &&
+  const bool bias_tma = NT == 1 && DV <= 128 && !pack && !split && p.bias != nullptr && p.max_kv % 4 == 0 &&
                         (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
   if (bias_tma && !make_tmap_bias(&maps.bias, p.bias, p.total_q, (uint64_t)p.bias_heads * p.max_kv, 128, true))
     return cudaErrorInvalidValue;
@@ -855,7 +860,8 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
     else
       kern = pack ? pick_fwd<DQK, DV, NK, NV, NT, true, false>(bf, bias_kind)
                   : pick_fwd<DQK, DV, NK, NV, NT, false, false>(bf, bias_kind);
-    if (bias_tma) smem = FwdCfg<DQK, DV, NK, NV, NT, 2>::SMEM;
+    if constexpr (DV <= 128)
+      if (bias_tma) smem = FwdCfg<DQK, DV, NK, NV, NT, 2>::SMEM;
   } else {
     if (pack || split || bias_tma) return cudaErrorInvalidValue;
     kern = pick_fwd<DQK, DV, NK, NV, NT, false, false>(bf, bias_kind);
@@ -870,7 +876,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
 }  // namespace
 
 bool tc_forward_splittable(const Params &p) {
-  return tc_forward_supported(p) && p.d_qk == p.d_v && p.d_qk <= 128;  // one query tile per CTA
+  return tc_forward_supported(p) && p.d_qk == p.d_v;  // one query tile per CTA
 }
 
 cudaError_t tc_forward_split(const Params &p, cudaStream_t st) {
@@ -879,11 +885,13 @@ cudaError_t tc_forward_split(const Params &p, cudaStream_t st) {
   if (e != cudaSuccess || p.total_q == 0 || p.total_kv == 0) return e;  // (empty: plain path ran)
   if (p.d_v == 64) return launch_combine<64>(p, st);
   if (p.d_v == 96) return launch_combine<96>(p, st);
+  if (p.d_v == 256) return launch_combine<256>(p, st);
   return launch_combine<128>(p, st);
 }
 
-// Parts per CTA band: split when the unsplit grid leaves SMs idle (fewer CTAs than two per SM,
-// the residency of one-tile CTAs), into as many parts as keep the grid within one such wave,
+// Parts per CTA band: split when the unsplit grid leaves SMs idle (fewer CTAs than resident
+// slots: two one-tile CTAs per SM, one at width 256), into as many parts as keep the grid within
+// one such wave,
 // each part at least four KV tiles long (a part costs a prologue, an fp32 partial write and a
 // read in the combine).  Between one and three waves, a grid whose last wave is partly empty
 // (under 95% wave efficiency) is cut into 2 or 3 parts, whichever fills its waves better (the
@@ -892,14 +900,14 @@ cudaError_t tc_forward_split(const Params &p, cudaStream_t st) {
 int fwd_num_splits(int num_seqs, int max_q, int max_kv, int h_q, int h_kv, int d_qk, int d_v,
                    int dtype, unsigned flags, int num_sms) {
   if ((dtype != VLF_F16 && dtype != VLF_BF16) || (flags & VLF_FLAG_FORCE_SIMT)) return 1;
-  if (d_qk != d_v || (d_qk != 64 && d_qk != 96 && d_qk != 128)) return 1;
+  if (d_qk != d_v || (d_qk != 64 && d_qk != 96 && d_qk != 128 && d_qk != 256)) return 1;
   if (num_seqs < 1 || max_q < 1 || max_kv < 1 || h_kv < 1 || h_q % h_kv != 0 || num_sms < 1) return 1;
   const int group = h_q / h_kv;
   const bool pack = group >= 2 && 128 % group == 0 && (long long)max_q * group <= 128 &&
                     !(flags & VLF_FLAG_NO_PACK);
   const long long rows = pack ? 128 / group : 128;
   const long long ctas = (max_q + rows - 1) / rows * (pack ? h_kv : h_q) * (long long)num_seqs;
-  const long long slots = 2LL * num_sms;
+  const long long slots = (d_v == 256 ? 1LL : 2LL) * num_sms;  // CTAs resident per SM
   const long long tiles = ((long long)max_kv + kBN - 1) / kBN;
   if (ctas >= slots) {
     if (ctas >= 3 * slots) return 1;
@@ -925,6 +933,7 @@ cudaError_t tc_forward(const Params &p, cudaStream_t st) {
   if (p.d_qk == 64) return launch_fwd<64, 64, 3, 3, 1>(p, st);
   if (p.d_qk == 96) return launch_fwd<96, 96, 3, 2, 1>(p, st);
   if (p.d_qk == 128) return launch_fwd<128, 128, 3, 2, 1>(p, st);
+  if (p.d_qk == 256) return launch_fwd<256, 256, 3, 2, 1>(p, st);
   return launch_fwd<192, 128, 3, 3, 2>(p, st);
 }
 

@@ -20,6 +20,7 @@ Workloads (named by what they are; the shapes are the benchmark configurations o
   against a cache of 8192 (64 sequences) or 32,768 tokens (4 sequences), H_q=32, H_kv=8, head
   dim 128, end-aligned causal, bf16, forward only.
 * ``dense4x4096_bf16_causal_d96`` -- the dense configuration at head width 96.
+* ``dense4x4096_bf16_causal_d256`` -- the dense configuration at head width 256, forward only.
 
 Draw order: the ragged lengths come from a CPU ``torch.Generator`` seeded with ``seed``; the
 tensors from a generator on the target device seeded with ``seed``, in the order q, k, v, dout,
@@ -109,6 +110,11 @@ def workload(name: str, seed: int = 0) -> Workload:
         # the dense configuration at head width 96 (a width the pages list beside 64/128/256)
         lens = [4096] * 4
         return Workload(name, "bf16", lens, lens, 32, 32, 96, 96, causal=True)
+    if name == "dense4x4096_bf16_causal_d256":
+        # the dense configuration at head width 256, forward only (the backward at this width
+        # runs on the SIMT kernels)
+        lens = [4096] * 4
+        return Workload(name, "bf16", lens, lens, 32, 32, 256, 256, causal=True, backward=False)
     if name == "ragged64_gqa_window_bf16":
         g = torch.Generator("cpu").manual_seed(seed)
         lens = ragged_lengths(64, 128, 8192, g)
@@ -137,7 +143,7 @@ def workload(name: str, seed: int = 0) -> Workload:
 WORKLOADS = ["varlen64_fp16_full", "varlen64_fp16_causal", "dense4x4096_bf16_causal",
              "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
              "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "decode64x8192_bf16_gqa",
-             "dense4x4096_bf16_causal_d96", "decode4x32768_bf16_gqa"]
+             "dense4x4096_bf16_causal_d96", "decode4x32768_bf16_gqa", "dense4x4096_bf16_causal_d256"]
 
 
 def custom(lengths_q, lengths_kv=None, *, dtype="bf16", h_q=4, h_kv=None, d_qk=64, d_v=None,
