@@ -238,11 +238,22 @@ def main():
     fpp = F.flops_per_pair(w.d_qk, w.d_v)
     pairs = F.workload_pairs(w)
     dt = x["q"].dtype
+    # a latent workload with a given rope_heads goes through the split-operand calls (its
+    # operands as produced, the rope key possibly shared); the others through the plain calls
+    latent_api = w.latent_split is not None and w.rope_heads is not None
+    in_names = ("q_nope", "q_rope", "k_nope", "k_rope", "v") if latent_api else ("q", "k", "v")
+    grad_of = dict(zip(("dq_nope", "dq_rope", "dk_nope", "dk_rope", "dv") if latent_api
+                       else ("dq", "dk", "dv"), in_names))
+    if latent_api:
+        del x["q"], x["k"]  # the concatenated operands are not used
     out = torch.empty((w.total_q, w.h_q, w.d_v), dtype=dt, device=dev)
     lse = torch.empty((w.h_q, w.total_q), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
-    ws = torch.empty(vlf.vlf_attn_varlen_bwd_workspace_size(
-        w.total_q, w.total_kv, w.h_q, w.h_kv, w.d_qk, w.d_v, dt), dtype=torch.uint8, device=dev)
+    res0 = {"out": out, "lse": lse, **{g: torch.empty_like(x[n]) for g, n in grad_of.items()}}
+    ws_bytes = (vlf.vlf_attn_varlen_bwd_latent_workspace_size(
+        w.total_q, w.total_kv, w.h_q, w.h_kv, w.rope_heads, dt) if latent_api else
+        vlf.vlf_attn_varlen_bwd_workspace_size(w.total_q, w.total_kv, w.h_q, w.h_kv, w.d_qk,
+                                               w.d_v, dt))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     kw = dict(scale=w.scale, causal=w.causal, window=w.window, bias=x["bias"])
     # small-batch / decode shapes split each CTA's KV band (the library's choice); the parts'
     # workspace is allocated once, outside the timed region
@@ -256,20 +267,34 @@ def main():
     # latency-bound) time the forward alone
     fwd_only = not w.backward
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        vlf.vlf_attn_varlen_fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_kv"],
-                                w.max_seqlen_q, w.max_seqlen_kv, out=out, lse=lse,
-                                workspace=fws[0], **fkw, **kw)
+    def run(d, r, fw, st=None, ev=None):
+        """One step on inputs d into results r through the library's calls (on stream st, the
+        current one when None); ev: per-stage timing events."""
+        ops = [d[n] for n in in_names]
+        cu = (d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv)
+        if latent_api:
+            vlf.vlf_attn_varlen_fwd_latent(*ops, *cu, out=r["out"], lse=r["lse"], stream=st, **kw)
+        else:
+            vlf.vlf_attn_varlen_fwd(*ops, *cu, out=r["out"], lse=r["lse"], stream=st,
+                                    workspace=fw, **fkw, **kw)
         if fwd_only:
             if ev is not None:
                 ev[1].record(stream)
             return
-        vlf.vlf_attn_varlen_bwd(x["dout"], x["q"], x["k"], x["v"], out, lse, x["cu_seqlens_q"],
-                                x["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv, dq=dq, dk=dk,
-                                dv=dv, workspace=ws, stage_events=None if ev is None else ev[1:],
-                                **kw)
+        sev = None if ev is None else ev[1:]
+        if latent_api:
+            vlf.vlf_attn_varlen_bwd_latent(d["dout"], *ops, r["out"], r["lse"], *cu,
+                                           grads=tuple(r[g] for g in grad_of), workspace=ws,
+                                           stream=st, stage_events=sev, **kw)
+        else:
+            vlf.vlf_attn_varlen_bwd(d["dout"], *ops, r["out"], r["lse"], *cu, dq=r["dq"],
+                                    dk=r["dk"], dv=r["dv"], workspace=ws, stream=st,
+                                    stage_events=sev, **kw)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        run(x, res0, fws[0], ev=ev)
 
     for _ in range(args.warmup):
         step()
@@ -295,8 +320,8 @@ def main():
     # their timed steps a buffer twice the L2 size is overwritten (outside each step's events)
     # and the step time is the mean of the per-step event times.
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    in_bytes = sum(t.numel() * t.element_size() for t in (x["q"], x["k"], x["v"], x["dout"],
-                                                          x["bias"]) if t is not None)
+    in_bytes = sum(t.numel() * t.element_size() for t in [x[n] for n in in_names] +
+                   [x["dout"], x["bias"]] if t is not None)
     flush = in_bytes < 2 * l2_bytes
     flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
     t_start.record(stream)
@@ -332,9 +357,11 @@ def main():
     tc = (fwd_path if dom == "fwd" else bwd_path) == 1
     # Algorithmic bytes per kernel launch (the minimum it moves): its tensors read and written
     # once, plus the bias once per pass where there is one.
-    eb = x["q"].element_size()
+    eb = x["v"].element_size()
     nq, nk = w.total_q * w.h_q, w.total_kv * w.h_kv
     q_b, k_b, v_b = nq * w.d_qk * eb, nk * w.d_qk * eb, nk * w.d_v * eb
+    if latent_api:  # K as read: the nope parts and the (possibly shared) rope key
+        k_b = (x["k_nope"].numel() + x["k_rope"].numel()) * eb
     o_b, row_b = nq * w.d_v * eb, 4 * nq                    # O (or dO), one fp32 per row
     bias_b = 0 if x["bias"] is None else x["bias"].numel() * 4
     bytes_of = {"fwd": q_b + k_b + v_b + o_b + row_b + bias_b,
@@ -374,9 +401,8 @@ def main():
         # input pipeline would: step k+1's upload and step k-1's read-back run on the copy
         # engines while step k's kernels run.  (The bias, where a workload has one, stays
         # resident like a weight.)
-        in_keys = ("q", "k", "v", "cu_seqlens_q", "cu_seqlens_kv") + (() if fwd_only else ("dout",))
-        res_like = {"out": out, "lse": lse} if fwd_only else {"out": out, "lse": lse, "dq": dq,
-                                                              "dk": dk, "dv": dv}
+        in_keys = in_names + ("cu_seqlens_q", "cu_seqlens_kv") + (() if fwd_only else ("dout",))
+        res_like = {"out": out, "lse": lse} if fwd_only else res0
         host = {k: x[k].cpu().pin_memory() for k in in_keys}
         dset = [{k: torch.empty_like(x[k]) for k in in_keys} for _ in range(2)]
         rset = [{k: torch.empty_like(t) for k, t in res_like.items()} for _ in range(2)]
@@ -402,14 +428,7 @@ def main():
                 ev_up[i].record(s_up)
             s_cmp.wait_event(ev_up[i])
             s_cmp.wait_event(ev_dn[i])  # the read-back of step - 2 is done with set i
-            vlf.vlf_attn_varlen_fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_kv"],
-                                    w.max_seqlen_q, w.max_seqlen_kv, out=r["out"], lse=r["lse"],
-                                    stream=s_cmp, workspace=fws[i], **fkw, **kw)
-            if not fwd_only:
-                vlf.vlf_attn_varlen_bwd(d["dout"], d["q"], d["k"], d["v"], r["out"], r["lse"],
-                                        d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q,
-                                        w.max_seqlen_kv, dq=r["dq"], dk=r["dk"], dv=r["dv"],
-                                        workspace=ws, stream=s_cmp, **kw)
+            run(d, r, fws[i], st=s_cmp)
             ev_cmp[i].record(s_cmp)
             with torch.cuda.stream(s_dn):
                 s_dn.wait_event(ev_cmp[i])

@@ -206,6 +206,59 @@ int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
                            unsigned flags, void *const *stage_events, int n_stage_events);
 
 /*
+ * Latent attention with split operands (triton-msl part 2, "Latent attention": the score is the
+ * sum of two query-key products over different widths, a 128-wide "nope" part and a 64-wide
+ * "rope" part, so the contraction is 192 wide while the output stays 128 wide).  The parts are
+ * passed as they are produced, without concatenation, and the rope key may be one tensor shared
+ * by every head:
+ *   logit(i, j) = scale * (q_nope_i . k_nope_j + q_rope_i . k_rope_j) + bias,
+ * with head h reading k_nope / v of kv head h / (h_q / h_kv) and k_rope of that kv head, or of
+ * the single rope head when rope_heads = 1.  Results equal vlf_attn_varlen_fwd / _bwd on the
+ * concatenated operands q = [q_nope | q_rope], k = [k_nope | k_rope broadcast over kv heads]
+ * (the same kernels, the same arithmetic).
+ *
+ *   q_nope  [total_q, h_q, 128]   q_rope [total_q, h_q, 64]          dtype
+ *   k_nope  [total_kv, h_kv, 128] k_rope [total_kv, rope_heads, 64]  dtype, rope_heads in {1, h_kv}
+ *   v       [total_kv, h_kv, 128]                                     dtype
+ *   d_nope, d_rope, d_v must be 128, 64, 128 (VLF_ERR_UNSUPPORTED otherwise, and for dtype F32
+ *   or VLF_FLAG_FORCE_SIMT: there is no SIMT kernel for split operands); other arguments and
+ *   outputs as vlf_attn_varlen_fwd / _bwd.  scale <= 0 selects 1/sqrt(192).
+ * Backward outputs (written): dq_nope / dq_rope like q_nope / q_rope, dk_nope like k_nope, dv
+ * like v, dk_rope like k_rope -- for a shared rope key (rope_heads = 1) the sum over every head
+ * of its gradient, accumulated in fp32 in kv-head order (deterministic) and rounded once.  The
+ * workspace (caller-owned, clobbered) holds the row dot products and, for a shared rope key with
+ * h_kv > 1, the per-kv-head fp32 rope gradients [h_kv, total_kv, 64].
+ */
+int vlf_attn_varlen_fwd_latent(const void *q_nope, const void *q_rope, const void *k_nope,
+                               const void *k_rope, const void *v,
+                               const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv,
+                               int num_seqs, int total_q, int total_kv, int max_seqlen_q,
+                               int max_seqlen_kv, int h_q, int h_kv, int rope_heads,
+                               int d_nope, int d_rope, int d_v, int dtype,
+                               float scale, int causal, int window,
+                               const float *bias, int bias_heads,
+                               void *out, float *lse, vlf_stream_t stream, unsigned flags);
+
+/* Bytes of workspace vlf_attn_varlen_bwd_latent needs (pure host arithmetic; 0 for invalid
+ * sizes). */
+size_t vlf_attn_varlen_bwd_latent_workspace_size(int total_q, int total_kv, int h_q, int h_kv,
+                                                 int rope_heads, int dtype);
+
+int vlf_attn_varlen_bwd_latent(const void *q_nope, const void *q_rope, const void *k_nope,
+                               const void *k_rope, const void *v, const void *out,
+                               const float *lse, const void *dout,
+                               const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv,
+                               int num_seqs, int total_q, int total_kv, int max_seqlen_q,
+                               int max_seqlen_kv, int h_q, int h_kv, int rope_heads,
+                               int d_nope, int d_rope, int d_v, int dtype,
+                               float scale, int causal, int window,
+                               const float *bias, int bias_heads,
+                               void *dq_nope, void *dq_rope, void *dk_nope, void *dk_rope,
+                               void *dv, void *workspace, size_t workspace_bytes,
+                               vlf_stream_t stream, unsigned flags,
+                               void *const *stage_events, int n_stage_events);
+
+/*
  * Number of kernels this library has launched in this process (all devices, all streams),
  * counted on the host at each successful launch.  For benchmarks that report their launches.
  */

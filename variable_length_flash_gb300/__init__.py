@@ -42,7 +42,8 @@ EXPORTS = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_fwd_ex", "vlf_attn_varlen_bwd
            "vlf_status_string", "vlf_sched_kv_band", "vlf_sched_q_band", "vlf_version",
            "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path", "vlf_attn_varlen_bwd_noalloc",
            "vlf_noalloc_scratch_bytes", "vlf_attn_varlen_fwd_split", "vlf_fwd_num_splits",
-           "vlf_attn_varlen_fwd_split_workspace_size"]
+           "vlf_attn_varlen_fwd_split_workspace_size", "vlf_attn_varlen_fwd_latent",
+           "vlf_attn_varlen_bwd_latent", "vlf_attn_varlen_bwd_latent_workspace_size"]
 VLF_BWD_STAGES = 3
 BWD_STAGE_NAMES = ["rowdot", "dkdv", "dq"]
 
@@ -89,6 +90,13 @@ def _load():
     lib.vlf_fwd_num_splits.restype = I
     lib.vlf_attn_varlen_fwd_split_workspace_size.argtypes = [I, I, I, I]
     lib.vlf_attn_varlen_fwd_split_workspace_size.restype = Z
+    lib.vlf_attn_varlen_fwd_latent.argtypes = [P] * 7 + [I] * 12 + [F, I, I, P, I, P, P, P, U]
+    lib.vlf_attn_varlen_fwd_latent.restype = I
+    lib.vlf_attn_varlen_bwd_latent_workspace_size.argtypes = [I] * 6
+    lib.vlf_attn_varlen_bwd_latent_workspace_size.restype = Z
+    lib.vlf_attn_varlen_bwd_latent.argtypes = ([P] * 10 + [I] * 12 + [F, I, I, P, I] + [P] * 6 +
+                                               [Z, P, U, P, I])
+    lib.vlf_attn_varlen_bwd_latent.restype = I
     lib.vlf_noalloc_scratch_bytes.argtypes = []
     lib.vlf_noalloc_scratch_bytes.restype = Z
     lib.vlf_launch_count.argtypes = []
@@ -314,6 +322,83 @@ def vlf_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, ma
         _ptr(workspace), workspace.numel(), _stream(stream, q), int(flags), *_events(stage_events))
     _check(st, "vlf_attn_varlen_bwd")
     return dq, dk, dv
+
+
+def _latent_args(q_nope, q_rope, k_nope, k_rope, v):
+    """Shapes of a split-operand latent call: (tq, hq, tk, hkv, rope_heads)."""
+    _req(q_nope, "q_nope")
+    for t, n in ((q_rope, "q_rope"), (k_nope, "k_nope"), (k_rope, "k_rope"), (v, "v")):
+        _req(t, n, q_nope.dtype)
+    if any(t.dim() != 3 for t in (q_nope, q_rope, k_nope, k_rope, v)):
+        raise VlfError(VLF_ERR_INVALID, "latent operands must be [tokens, heads, width]")
+    tq, hq, _ = q_nope.shape
+    tk, hkv, _ = k_nope.shape
+    if tuple(q_rope.shape[:2]) != (tq, hq) or k_rope.shape[0] != tk or tuple(v.shape[:2]) != (tk, hkv):
+        raise VlfError(VLF_ERR_INVALID, "latent operand shapes disagree")
+    return tq, hq, tk, hkv, int(k_rope.shape[1])
+
+
+def vlf_attn_varlen_fwd_latent(q_nope, q_rope, k_nope, k_rope, v, cu_seqlens_q, cu_seqlens_kv,
+                               max_seqlen_q, max_seqlen_kv=None, scale=None, causal=False,
+                               window=0, bias=None, out=None, lse=None, stream=None, flags=0):
+    """Latent attention forward with split operands (q_nope [Tq,H,128], q_rope [Tq,H,64],
+    k_nope [Tkv,Hkv,128], k_rope [Tkv,1 or Hkv,64], v [Tkv,Hkv,128]); equals the forward on the
+    concatenated operands.  Returns out [Tq,H,128] and lse fp32 [H,Tq]."""
+    tq, hq, tk, hkv, rh = _latent_args(q_nope, q_rope, k_nope, k_rope, v)
+    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
+    if max_seqlen_kv is None:
+        max_seqlen_kv = int(bias.shape[2]) if bias is not None else _max_len(cu_seqlens_kv)
+    bias, bh = _bias_args(bias, tq, hq)
+    dv = v.shape[2]
+    if out is None:
+        out = torch.empty((tq, hq, dv), dtype=q_nope.dtype, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty((hq, tq), dtype=torch.float32, device=q_nope.device)
+    st = _lib.vlf_attn_varlen_fwd_latent(
+        _ptr(q_nope), _ptr(q_rope), _ptr(k_nope), _ptr(k_rope), _ptr(v), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_kv), cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q),
+        int(max_seqlen_kv), hq, hkv, rh, q_nope.shape[2], q_rope.shape[2], dv,
+        _DTYPE[q_nope.dtype], float(scale) if scale else 0.0, int(bool(causal)), int(window or 0),
+        _ptr(bias), bh, _ptr(out), _ptr(lse), _stream(stream, q_nope), int(flags))
+    _check(st, "vlf_attn_varlen_fwd_latent")
+    return out, lse
+
+
+def vlf_attn_varlen_bwd_latent_workspace_size(total_q, total_kv, h_q, h_kv, rope_heads, dtype) -> int:
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(_lib.vlf_attn_varlen_bwd_latent_workspace_size(total_q, total_kv, h_q, h_kv,
+                                                              rope_heads, dt))
+
+
+def vlf_attn_varlen_bwd_latent(dout, q_nope, q_rope, k_nope, k_rope, v, out, lse, cu_seqlens_q,
+                               cu_seqlens_kv, max_seqlen_q, max_seqlen_kv=None, scale=None,
+                               causal=False, window=0, bias=None, grads=None, workspace=None,
+                               stream=None, flags=0, stage_events=None):
+    """Latent attention backward with split operands.  Returns (dq_nope, dq_rope, dk_nope,
+    dk_rope, dv); a shared rope key (k_rope with one head) gets the sum of every head's
+    gradient.  ``grads``: optional preallocated 5-tuple in that order."""
+    tq, hq, tk, hkv, rh = _latent_args(q_nope, q_rope, k_nope, k_rope, v)
+    for t, n in ((dout, "dout"), (out, "out")):
+        _req(t, n, q_nope.dtype)
+    _req(lse, "lse", torch.float32)
+    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
+    if max_seqlen_kv is None:
+        max_seqlen_kv = int(bias.shape[2]) if bias is not None else _max_len(cu_seqlens_kv)
+    bias, bh = _bias_args(bias, tq, hq)
+    if grads is None:
+        grads = tuple(torch.empty_like(t) for t in (q_nope, q_rope, k_nope, k_rope, v))
+    need = vlf_attn_varlen_bwd_latent_workspace_size(tq, tk, hq, hkv, rh, q_nope.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_nope.device)
+    st = _lib.vlf_attn_varlen_bwd_latent(
+        _ptr(q_nope), _ptr(q_rope), _ptr(k_nope), _ptr(k_rope), _ptr(v), _ptr(out), _ptr(lse),
+        _ptr(dout), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), cu_seqlens_q.numel() - 1, tq, tk,
+        int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, rh, q_nope.shape[2], q_rope.shape[2],
+        v.shape[2], _DTYPE[q_nope.dtype], float(scale) if scale else 0.0, int(bool(causal)),
+        int(window or 0), _ptr(bias), bh, *[_ptr(g) for g in grads], _ptr(workspace),
+        workspace.numel(), _stream(stream, q_nope), int(flags), *_events(stage_events))
+    _check(st, "vlf_attn_varlen_bwd_latent")
+    return grads
 
 
 def vlf_noalloc_scratch_bytes() -> int:

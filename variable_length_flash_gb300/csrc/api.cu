@@ -72,7 +72,7 @@ int check_common(const void *q, const void *k, const void *v, const int32_t *cu_
   if (dtype != VLF_F16 && dtype != VLF_BF16 && dtype != VLF_F32) return VLF_ERR_INVALID;
   if (num_seqs == 0 && (total_q != 0 || total_kv != 0)) return VLF_ERR_INVALID;
   if (num_seqs > 0 && (!cu_q || !cu_kv)) return VLF_ERR_INVALID;
-  if ((total_q > 0 || total_kv > 0) && (!q || !k || !v)) return VLF_ERR_INVALID;
+  if ((total_q > 0 && !q) || (total_kv > 0 && (!k || !v))) return VLF_ERR_INVALID;
   if (bias && bias_heads != 1 && bias_heads != h_q) return VLF_ERR_INVALID;
   if (d_qk > 256 || d_v > 256) return VLF_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || h_q > 65535) return VLF_ERR_UNSUPPORTED;
@@ -107,6 +107,32 @@ size_t workspace_bytes_for(int total_q, int h_q, int d_qk, int dtype) {
   rowdot = (rowdot + 255) & ~(size_t)255;
   if (dtype == VLF_F32) return rowdot;
   return rowdot + vlf::tc_backward_workspace(total_q, h_q, d_qk);
+}
+
+// Checks shared by the split-operand latent entry points (beyond check_common on the nope
+// tensors): the rope tensors, rope_heads, and the one head shape with a kernel.
+int check_latent(const void *q_rope, const void *k_rope, int total_q, int total_kv, int h_kv,
+                 int rope_heads, int d_nope, int d_rope, int d_v, int dtype, unsigned flags) {
+  if ((total_q > 0 && !q_rope) || (total_kv > 0 && !k_rope)) return VLF_ERR_INVALID;
+  if (rope_heads != 1 && rope_heads != h_kv) return VLF_ERR_INVALID;
+  if (!aligned16(q_rope) || !aligned16(k_rope)) return VLF_ERR_ALIGN;
+  if (d_nope != 128 || d_rope != 64 || d_v != 128) return VLF_ERR_UNSUPPORTED;
+  if ((dtype != VLF_F16 && dtype != VLF_BF16) || (flags & VLF_FLAG_FORCE_SIMT)) return VLF_ERR_UNSUPPORTED;
+  return VLF_OK;
+}
+
+size_t latent_rope_part_bytes(int total_kv, int h_kv, int rope_heads) {
+  if (rope_heads != 1 || h_kv <= 1 || total_kv <= 0) return 0;
+  return ((size_t)h_kv * (size_t)total_kv * 64 * sizeof(float) + 255) & ~(size_t)255;
+}
+
+__global__ void fill_f32_kernel(float *p, size_t n, float v) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = v;
+}
+
+cudaError_t zero16(void *p, size_t elems, cudaStream_t st) {
+  return elems && p ? cudaMemsetAsync(p, 0, elems * 2, st) : cudaSuccess;
 }
 
 }  // namespace
@@ -334,6 +360,117 @@ int vlf_attn_varlen_bwd(const void *q, const void *k, const void *v, const void 
                                 total_q, total_kv, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk,
                                 d_v, dtype, scale, causal, window, bias, bias_heads, dq, dk, dv,
                                 workspace, workspace_bytes, stream, 0u, nullptr, 0);
+}
+
+int vlf_attn_varlen_fwd_latent(const void *q_nope, const void *q_rope, const void *k_nope,
+                               const void *k_rope, const void *v, const int32_t *cu_seqlens_q,
+                               const int32_t *cu_seqlens_kv, int num_seqs, int total_q,
+                               int total_kv, int max_seqlen_q, int max_seqlen_kv, int h_q,
+                               int h_kv, int rope_heads, int d_nope, int d_rope, int d_v,
+                               int dtype, float scale, int causal, int window, const float *bias,
+                               int bias_heads, void *out, float *lse, vlf_stream_t stream,
+                               unsigned flags) {
+  int st = check_common(q_nope, k_nope, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q,
+                        total_kv, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_nope + d_rope, d_v,
+                        dtype, bias, bias_heads);
+  if (st != VLF_OK) return st;
+  st = check_latent(q_rope, k_rope, total_q, total_kv, h_kv, rope_heads, d_nope, d_rope, d_v, dtype, flags);
+  if (st != VLF_OK) return st;
+  if (total_q > 0 && !out) return VLF_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(lse)) return VLF_ERR_ALIGN;
+  if (num_seqs == 0 || max_seqlen_q == 0 || total_q == 0) return VLF_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (total_kv == 0) {  // no keys anywhere: O = 0, LSE = -inf
+    e = zero16(out, (size_t)total_q * h_q * d_v, cs);
+    if (e == cudaSuccess && lse) {
+      const size_t n = (size_t)total_q * h_q;
+      fill_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, cs>>>(lse, n, -INFINITY);
+      e = cudaGetLastError();
+      if (e == cudaSuccess) vlf::count_launch();
+    }
+    return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
+  }
+  vlf::Params p;
+  fill_common(p, q_nope, k_nope, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+              max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_nope + d_rope, d_v, dtype, scale, causal,
+              window, bias, bias_heads, flags);
+  p.latent = 1;
+  p.q_rope = q_rope;
+  p.k_rope = k_rope;
+  p.rope_heads = rope_heads;
+  p.out = out;
+  p.lse = lse;
+  p.err = error_word_ptr();
+  if (!p.err) return VLF_ERR_LAUNCH;
+  e = vlf::tc_forward(p, cs);
+  return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
+}
+
+size_t vlf_attn_varlen_bwd_latent_workspace_size(int total_q, int total_kv, int h_q, int h_kv,
+                                                 int rope_heads, int dtype) {
+  if (total_q < 0 || total_kv < 0 || h_q < 1 || h_kv < 1) return 0;
+  return workspace_bytes_for(total_q, h_q, 192, dtype) +
+         latent_rope_part_bytes(total_kv, h_kv, rope_heads);
+}
+
+int vlf_attn_varlen_bwd_latent(const void *q_nope, const void *q_rope, const void *k_nope,
+                               const void *k_rope, const void *v, const void *out,
+                               const float *lse, const void *dout, const int32_t *cu_seqlens_q,
+                               const int32_t *cu_seqlens_kv, int num_seqs, int total_q,
+                               int total_kv, int max_seqlen_q, int max_seqlen_kv, int h_q,
+                               int h_kv, int rope_heads, int d_nope, int d_rope, int d_v,
+                               int dtype, float scale, int causal, int window, const float *bias,
+                               int bias_heads, void *dq_nope, void *dq_rope, void *dk_nope,
+                               void *dk_rope, void *dv, void *workspace, size_t workspace_bytes,
+                               vlf_stream_t stream, unsigned flags, void *const *stage_events,
+                               int n_stage_events) {
+  if (stage_events && n_stage_events < VLF_BWD_STAGES + 1) return VLF_ERR_INVALID;
+  int st = check_common(q_nope, k_nope, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q,
+                        total_kv, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_nope + d_rope, d_v,
+                        dtype, bias, bias_heads);
+  if (st != VLF_OK) return st;
+  st = check_latent(q_rope, k_rope, total_q, total_kv, h_kv, rope_heads, d_nope, d_rope, d_v, dtype, flags);
+  if (st != VLF_OK) return st;
+  if (total_q > 0 && (!out || !lse || !dout || !dq_nope || !dq_rope)) return VLF_ERR_INVALID;
+  if (total_kv > 0 && (!dk_nope || !dk_rope || !dv)) return VLF_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq_nope) ||
+      !aligned16(dq_rope) || !aligned16(dk_nope) || !aligned16(dk_rope) || !aligned16(dv) ||
+      !aligned16(workspace))
+    return VLF_ERR_ALIGN;
+  const size_t rowdot_bytes = workspace_bytes_for(total_q, h_q, 192, dtype);
+  const size_t need = rowdot_bytes + latent_rope_part_bytes(total_kv, h_kv, rope_heads);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return VLF_ERR_WORKSPACE;
+  if (num_seqs == 0) return VLF_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (total_q == 0 || total_kv == 0) {  // nothing attends: every gradient is zero
+    cudaError_t e = zero16(dq_nope, (size_t)total_q * h_q * d_nope, cs);
+    if (e == cudaSuccess) e = zero16(dq_rope, (size_t)total_q * h_q * d_rope, cs);
+    if (e == cudaSuccess) e = zero16(dk_nope, (size_t)total_kv * h_kv * d_nope, cs);
+    if (e == cudaSuccess) e = zero16(dk_rope, (size_t)total_kv * rope_heads * d_rope, cs);
+    if (e == cudaSuccess) e = zero16(dv, (size_t)total_kv * h_kv * d_v, cs);
+    return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
+  }
+  vlf::Params p;
+  fill_common(p, q_nope, k_nope, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+              max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_nope + d_rope, d_v, dtype, scale, causal,
+              window, bias, bias_heads, flags);
+  p.latent = 1;
+  p.q_rope = q_rope;
+  p.k_rope = k_rope;
+  p.rope_heads = rope_heads;
+  p.out = const_cast<void *>(out);
+  p.lse = const_cast<float *>(lse);
+  p.dout = dout;
+  p.dq = dq_nope; p.dk = dk_nope; p.dv = dv;
+  p.dq_rope = dq_rope; p.dk_rope = dk_rope;
+  p.rowdot = static_cast<float *>(workspace);
+  if (latent_rope_part_bytes(total_kv, h_kv, rope_heads) > 0)
+    p.dk_rope_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + rowdot_bytes);
+  p.err = error_word_ptr();
+  if (!p.err) return VLF_ERR_LAUNCH;
+  cudaError_t e = vlf::tc_backward(p, cs, reinterpret_cast<const cudaEvent_t *>(stage_events));
+  return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
 }
 
 int vlf_check_error(vlf_stream_t stream) {

@@ -40,6 +40,17 @@ struct Params {
   int kv_splits = 1;
   float *o_part = nullptr;    // [kv_splits, total_q, h_q, d_v]
   float *lse_part = nullptr;  // [kv_splits, h_q, total_q]
+  // latent head with split operands (QK width 192 = 128 "nope" + 64 "rope", V width 128): q and
+  // k point to q_nope [total_q, h_q, 128] and k_nope [total_kv, h_kv, 128]; the last 64 columns
+  // of each Q / K tile come from q_rope [total_q, h_q, 64] and k_rope [total_kv, rope_heads, 64]
+  // (rope_heads 1: one rope key shared by every head).  The backward writes dq / dk as their
+  // nope parts and dq_rope / dk_rope; a shared rope key's gradient goes per kv head to
+  // dk_rope_part [h_kv, total_kv, 64] fp32 and is summed over heads afterwards.
+  int latent = 0;
+  const void *q_rope = nullptr, *k_rope = nullptr;
+  int rope_heads = 0;
+  void *dq_rope = nullptr, *dk_rope = nullptr;
+  float *dk_rope_part = nullptr;
 };
 
 // ---------------------------------------------------------------- element access

@@ -32,6 +32,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -55,6 +57,8 @@ constexpr int kDkdv = 0, kDq = 1, kDqS = 2;
 
 struct BwdMaps {
   CUtensorMap outer0, outer1, inner0, inner1, bias;
+  // latent head with split operands: the rope tensors behind outer0 / inner0 (64 columns)
+  CUtensorMap outer0_rope, inner0_rope;
 };
 
 // outer0/outer1: K, V (dK/dV) or Q, dO (dQ), 128 rows.  inner0/inner1: Q, dO (dK/dV) or K, V
@@ -218,6 +222,11 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
+    // a latent head given as split operands (QK width 192 only): blocks 0-1 of each Q / K tile
+    // come from the nope tensors (row width 128 per head), block 2 from the rope tensors
+    const bool lat = DQK == 192 && p.latent;
+    const int qw = lat ? 128 : DQK;
+    const int rh = lat && p.rope_heads == 1 ? 0 : hk;  // the kv head's rope key
     if (n_items > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&maps.outer0);
@@ -225,11 +234,19 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         tma_prefetch_desc(&maps.inner0);
         tma_prefetch_desc(&maps.inner1);
         if (BIAS == 2) tma_prefetch_desc(&maps.bias);
+        if (lat) {
+          tma_prefetch_desc(&maps.outer0_rope);
+          tma_prefetch_desc(&maps.inner0_rope);
+        }
         const int orow = (MODE == kDkdv ? sq.k0 : sq.q0) + tile0;
         const int oh = MODE == kDkdv ? hk : head_outer;  // head index inside the outer tensors
         mbar_expect_tx(bar(C::B_OUT), C::O0_BYTES + C::O1_BYTES);
-        for (int c = 0; c < C::KB0; ++c)
-          tma_load_2d(sO0 + c * C::OBLK, &maps.outer0, oh * DQK + 64 * c, orow, bar(C::B_OUT));
+        for (int c = 0; c < C::KB0; ++c) {
+          if (lat && c == 2)  // the rope block: K's from the (possibly shared) rope key, or Q's
+            tma_load_2d(sO0 + c * C::OBLK, &maps.outer0_rope, (MODE == kDkdv ? rh : oh) * 64, orow, bar(C::B_OUT));
+          else
+            tma_load_2d(sO0 + c * C::OBLK, &maps.outer0, oh * qw + 64 * c, orow, bar(C::B_OUT));
+        }
         for (int c = 0; c < C::KB1; ++c)
           tma_load_2d(sO1 + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
       }
@@ -295,9 +312,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         const int irow = (MODE == kDkdv ? sq.q0 : sq.k0) + item_row(n);
         if (lane == 0) {
           mbar_expect_tx(bar(C::B_IF + st), C::I0_BYTES);
-          for (int c = 0; c < C::KB0; ++c)
-            tma_load_2d(sIn0 + st * C::I0_BYTES + c * C::IBLK, &maps.inner0, ih * DQK + 64 * c, irow,
-                        bar(C::B_IF + st));
+          for (int c = 0; c < C::KB0; ++c) {
+            if (lat && c == 2)
+              tma_load_2d(sIn0 + st * C::I0_BYTES + c * C::IBLK, &maps.inner0_rope,
+                          (MODE == kDkdv ? ih : rh) * 64, irow, bar(C::B_IF + st));
+            else
+              tma_load_2d(sIn0 + st * C::I0_BYTES + c * C::IBLK, &maps.inner0, ih * qw + 64 * c, irow,
+                          bar(C::B_IF + st));
+          }
           ++issued0[st];
         }
         mbar_arrive(bar(C::B_IF + st));
@@ -604,46 +626,68 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       fence_after();
-      // columns [c0, c0 + ncols) of an accumulator (row width `width` in the output) -> dtype
-      auto store_acc = [&](uint32_t tcol, int c0, int ncols, int width, void *dst_base, int heads,
-                           int head, float mul) {
-        uint4 *dst = nullptr;
-        if (orow_ok) {
-          const size_t g = (size_t)((MODE == kDkdv ? sq.k0 : sq.q0) + orow);
-          dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(dst_base) +
-                                          ((g * heads + head) * (size_t)width + c0) * 2);
-        }
+      // TMEM columns [tcol, tcol + ncols) of this thread's row, times mul, to dst_base + off
+      // (elements): 16-bit, or fp32 when f32
+      const size_t g = (size_t)((MODE == kDkdv ? sq.k0 : sq.q0) + (orow_ok ? orow : 0));
+      auto store_acc = [&](uint32_t tcol, int ncols, void *dst_base, size_t off, float mul, bool f32) {
 #pragma unroll 1
         for (int ch = 0; ch < ncols / 32; ++ch) {
           uint32_t v[32];
           if (n_items > 0) {
             __syncwarp();
-            tmem_ld32(lane_addr + tcol + c0 + ch * 32, v);
+            tmem_ld32(lane_addr + tcol + ch * 32, v);
             tmem_ld_wait();
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = 0u;
           }
-          uint32_t o16[16];
+          if (!orow_ok) continue;
+          if (f32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(dst_base) + off + 32 * ch);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            o16[e] = pack2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul, is_bf16);
-          if (dst) {
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(v[4 * q4]) * mul, __uint_as_float(v[4 * q4 + 1]) * mul,
+                                    __uint_as_float(v[4 * q4 + 2]) * mul, __uint_as_float(v[4 * q4 + 3]) * mul);
+          } else {
+            uint32_t o16[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              o16[e] = pack2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul, is_bf16);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dst_base) + off + 32 * ch);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
-              dst[ch * 4 + q4] = make_uint4(o16[4 * q4], o16[4 * q4 + 1], o16[4 * q4 + 2], o16[4 * q4 + 3]);
+              dst[q4] = make_uint4(o16[4 * q4], o16[4 * q4 + 1], o16[4 * q4 + 2], o16[4 * q4 + 3]);
           }
         }
       };
+      // a latent head given as split operands: the nope and rope parts of dK / dQ go to separate
+      // tensors; a rope key shared by the kv heads gets its per-head part in fp32, summed later
+      const bool lat = DQK == 192 && p.latent;
       if (MODE == kDkdv) {
-        if (half == 0) store_acc(C::ACC0, 0, DV, DV, p.dv, p.h_kv, hk, 1.f);
-        else store_acc(C::ACC1, 0, DQK, DQK, p.dk, p.h_kv, hk, p.scale);
+        if (half == 0) {
+          store_acc(C::ACC0, DV, p.dv, (g * p.h_kv + hk) * DV, 1.f, false);
+        } else if (!lat) {
+          store_acc(C::ACC1, DQK, p.dk, (g * p.h_kv + hk) * DQK, p.scale, false);
+        } else {
+          store_acc(C::ACC1, 128, p.dk, (g * p.h_kv + hk) * 128, p.scale, false);
+          if (p.dk_rope_part)
+            store_acc(C::ACC1 + 128, 64, p.dk_rope_part, ((size_t)hk * p.total_kv + g) * 64, p.scale, true);
+          else
+            store_acc(C::ACC1 + 128, 64, p.dk_rope, (g * p.rope_heads + (p.rope_heads == 1 ? 0 : hk)) * 64,
+                      p.scale, false);
+        }
       } else {
-        // the two halves split dQ's 32-column chunks (an odd count: the first takes one more)
-        constexpr int nch = DQK / 32, first = (nch + 1) / 2;
-        if (half == 0) store_acc(C::ACC0, 0, 32 * first, DQK, p.dq, p.h_q, head_outer, p.scale);
-        else if (nch > first)
-          store_acc(C::ACC0, 32 * first, 32 * (nch - first), DQK, p.dq, p.h_q, head_outer, p.scale);
+        const size_t row = g * p.h_q + head_outer;
+        if (lat) {
+          if (half == 0) store_acc(C::ACC0, 128, p.dq, row * 128, p.scale, false);
+          else store_acc(C::ACC0 + 128, 64, p.dq_rope, row * 64, p.scale, false);
+        } else {
+          // the two halves split dQ's 32-column chunks (an odd count: the first takes one more)
+          constexpr int nch = DQK / 32, first = (nch + 1) / 2;
+          if (half == 0) store_acc(C::ACC0, 32 * first, p.dq, row * DQK, p.scale, false);
+          else if (nch > first)
+            store_acc(C::ACC0 + 32 * first, 32 * (nch - first), p.dq, row * DQK + 32 * first, p.scale, false);
+        }
       }
     }
   }
@@ -664,17 +708,30 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   BwdMaps m;
   const uint64_t tq = p.total_q, tk = p.total_kv;
   bool ok;
+  // a latent head with split operands: q / k hold the 128-wide nope parts, q_rope / k_rope the
+  // 64-wide rope parts
+  const bool lat = DQK == 192 && p.latent;
+  const uint64_t qw = lat ? 128 : DQK;
+  const uint64_t qc = (uint64_t)p.h_q * qw, kc = (uint64_t)p.h_kv * qw;
+  const uint64_t qrc = (uint64_t)p.h_q * 64, krc = (uint64_t)(lat ? p.rope_heads : 1) * 64;
   if (MODE == kDkdv) {
-    ok = make_tmap_16bit(&m.outer0, p.k, tk, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, 128, bf) &&
+    ok = make_tmap_16bit(&m.outer0, p.k, tk, kc, kc, 128, bf) &&
          make_tmap_16bit(&m.outer1, p.v, tk, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, 128, bf) &&
-         make_tmap_16bit(&m.inner0, p.q, tq, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, IR, bf) &&
+         make_tmap_16bit(&m.inner0, p.q, tq, qc, qc, IR, bf) &&
          make_tmap_16bit(&m.inner1, p.dout, tq, (uint64_t)p.h_q * DV, (uint64_t)p.h_q * DV, IR, bf);
+    if (lat)
+      ok = ok && make_tmap_16bit(&m.outer0_rope, p.k_rope, tk, krc, krc, 128, bf) &&
+           make_tmap_16bit(&m.inner0_rope, p.q_rope, tq, qrc, qrc, IR, bf);
   } else {
-    ok = make_tmap_16bit(&m.outer0, p.q, tq, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, 128, bf) &&
+    ok = make_tmap_16bit(&m.outer0, p.q, tq, qc, qc, 128, bf) &&
          make_tmap_16bit(&m.outer1, p.dout, tq, (uint64_t)p.h_q * DV, (uint64_t)p.h_q * DV, 128, bf) &&
-         make_tmap_16bit(&m.inner0, p.k, tk, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, IR, bf) &&
+         make_tmap_16bit(&m.inner0, p.k, tk, kc, kc, IR, bf) &&
          make_tmap_16bit(&m.inner1, p.v, tk, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, IR, bf);
+    if (lat)
+      ok = ok && make_tmap_16bit(&m.outer0_rope, p.q_rope, tq, qrc, qrc, 128, bf) &&
+           make_tmap_16bit(&m.inner0_rope, p.k_rope, tk, krc, krc, IR, bf);
   }
+  if (!lat) { m.outer0_rope = m.outer0; m.inner0_rope = m.inner0; }  // (unused)
   if (NBS > 0)
     ok = ok && make_tmap_bias(&m.bias, p.bias, tq, (uint64_t)p.bias_heads * p.max_kv,
                               MODE == kDkdv ? IR : 128, MODE != kDkdv);
@@ -705,6 +762,31 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   return e;
 }
 
+// The gradient of a rope key shared by the kv heads of a split-operand latent head: the dK/dV
+// kernel left each kv head's part in fp32 [h_kv, total_kv, 64]; sum them in head order
+// (deterministic) into dk_rope [total_kv, 1, 64].
+template <bool BF16>
+__global__ void __launch_bounds__(256) rope_grad_sum_kernel(const Params p) {
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  const size_t n = (size_t)p.total_kv * 64;
+  const size_t i = (size_t)blockIdx.x * 256 + threadIdx.x;
+  if (i >= n) return;
+  float acc = 0.f;
+  for (int h = 0; h < p.h_kv; ++h) acc += p.dk_rope_part[(size_t)h * n + i];
+  static_cast<T *>(p.dk_rope)[i] = from_f32<T>(acc);
+}
+
+cudaError_t rope_grad_sum(const Params &p, cudaStream_t st) {
+  const size_t n = (size_t)p.total_kv * 64;
+  if (n == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((n + 255) / 256);
+  if (p.dtype == VLF_BF16) rope_grad_sum_kernel<true><<<blocks, 256, 0, st>>>(p);
+  else rope_grad_sum_kernel<false><<<blocks, 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
 // Per head width: item rows, buffers, ring-0 / ring-1 stages and bias stages of the dK/dV kernel
 // (IR_KV, NBUF_KV, NST_KV, NST1_KV, NBS_KV) and the mode, item rows, buffers, ring stages and
 // bias stages of the dQ kernel (MODE_Q, IR_Q, NBUF_Q, NST_Q, NST1_Q, NBS_Q).  A ring slot is
@@ -718,6 +800,7 @@ cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
   if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV, NST1_KV, NBS_KV>(p, st)) != cudaSuccess) return e;
+  if (DQK == 192 && p.latent && p.dk_rope_part && (e = rope_grad_sum(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
   if ((e = launch_bwd<MODE_Q, DQK, DV, IR_Q, NBUF_Q, NST_Q, NST1_Q, NBS_Q>(p, st)) != cudaSuccess) return e;
   return mark(ev, 3, st);

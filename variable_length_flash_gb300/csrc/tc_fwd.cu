@@ -56,6 +56,7 @@ struct FwdMaps {
   CUtensorMap q, k, v;
   CUtensorMap q3;    // PACK: Q as [tokens][heads][D_qk], box {64, G heads, 128 / G tokens}
   CUtensorMap bias;  // bias through TMA: [total_q][bias_heads x max_kv] fp32, box {32, 128}
+  CUtensorMap q_rope, k_rope;  // latent head with split operands: the rope tensors (64 columns)
 };
 
 // NT: query tiles per CTA.  NT = 2: 416 threads and all 512 TMEM columns, one CTA per SM.
@@ -254,6 +255,16 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
+      // a latent head given as split operands (QK width 192 only): the first two 64-column
+      // blocks of each Q / K tile come from the nope tensors (row width 128 per head), the third
+      // from the rope tensors
+      const bool lat = DQK == 192 && p.latent;
+      const int qw = lat ? 128 : DQK;
+      const int rh = lat && p.rope_heads == 1 ? 0 : hk;  // the kv head's rope key
+      if (lat) {
+        tma_prefetch_desc(&maps.q_rope);
+        tma_prefetch_desc(&maps.k_rope);
+      }
       int nq = 0;
       for (int t = 0; t < 2; ++t) nq += ti.row0[t] < sq.q_len ? 1 : 0;
       mbar_expect_tx(bar(C::B_Q), nq * C::Q_BYTES);
@@ -263,8 +274,11 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           if (PACK)  // rows (token, head of the group): one 3-D box
             tma_load_3d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q3, 64 * c, hk * p.group,
                         sq.q0 + ti.row0[t], bar(C::B_Q));
+          else if (lat && c == 2)
+            tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q_rope, ti.head[t] * 64,
+                        sq.q0 + ti.row0[t], bar(C::B_Q));
           else
-            tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q, ti.head[t] * DQK + 64 * c,
+            tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q, ti.head[t] * qw + 64 * c,
                         sq.q0 + ti.row0[t], bar(C::B_Q));
         }
       }
@@ -290,9 +304,14 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           if (it >= NK) ok = mbar_wait(bar(C::B_KE + ks), ((it / NK) - 1) & 1, abort_flag, p.err);
           if (!ok) break;
           mbar_expect_tx(bar(C::B_KF + ks), C::K_BYTES);
-          for (int c = 0; c < C::KBQ; ++c)
-            tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, &maps.k, hk * DQK + 64 * c,
-                        sq.k0 + kj * kBN, bar(C::B_KF + ks));
+          for (int c = 0; c < C::KBQ; ++c) {
+            if (lat && c == 2)
+              tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, &maps.k_rope, rh * 64,
+                          sq.k0 + kj * kBN, bar(C::B_KF + ks));
+            else
+              tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, &maps.k, hk * qw + 64 * c,
+                          sq.k0 + kj * kBN, bar(C::B_KF + ks));
+          }
           ++k_issued[ks];
         }
         if (vj >= lo) {
@@ -821,13 +840,21 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   // query heads of a kv head into one tile, so each K/V tile is read once for the group.
   const bool pack = NT == 1 && p.group >= 2 && 128 % p.group == 0 && p.max_q * p.group <= 128 &&
                     !(p.flags & VLF_FLAG_NO_PACK);
-  if (!make_tmap_16bit(&maps.q, p.q, p.total_q, (uint64_t)p.h_q * DQK, (uint64_t)p.h_q * DQK, 128, bf) ||
-      !make_tmap_16bit(&maps.k, p.k, p.total_kv, (uint64_t)p.h_kv * DQK, (uint64_t)p.h_kv * DQK, kBN, bf) ||
+  // a latent head with split operands: q / k hold the 128-wide nope parts
+  const bool lat = DQK == 192 && p.latent;
+  const uint64_t qw = lat ? 128 : DQK;
+  if (lat && (!make_tmap_16bit(&maps.q_rope, p.q_rope, p.total_q, (uint64_t)p.h_q * 64, (uint64_t)p.h_q * 64, 128, bf) ||
+              !make_tmap_16bit(&maps.k_rope, p.k_rope, p.total_kv, (uint64_t)p.rope_heads * 64,
+                               (uint64_t)p.rope_heads * 64, kBN, bf)))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_16bit(&maps.q, p.q, p.total_q, (uint64_t)p.h_q * qw, (uint64_t)p.h_q * qw, 128, bf) ||
+      !make_tmap_16bit(&maps.k, p.k, p.total_kv, (uint64_t)p.h_kv * qw, (uint64_t)p.h_kv * qw, kBN, bf) ||
       !make_tmap_16bit(&maps.v, p.v, p.total_kv, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, kBN, bf))
     return cudaErrorInvalidValue;
   if (pack && !make_tmap_q3(&maps.q3, p.q, p.total_q, p.h_q, DQK, p.group, 128 / p.group, bf))
     return cudaErrorInvalidValue;
   if (!pack) maps.q3 = maps.q;
+  if (!lat) { maps.q_rope = maps.q; maps.k_rope = maps.k; }
   const bool pair_heads = NT == 2 && (p.group % 2 == 0);
   const int rows_per_cta = pack ? 128 / p.group : (NT == 1 || pair_heads ? 128 : 256);
   const unsigned blocks = (unsigned)((p.max_q + rows_per_cta - 1) / rows_per_cta);

@@ -21,6 +21,8 @@ Workloads (named by what they are; the shapes are the benchmark configurations o
   dim 128, end-aligned causal, bf16, forward only.
 * ``dense4x4096_bf16_causal_d96`` -- the dense configuration at head width 96.
 * ``dense4x4096_bf16_causal_d256`` -- the dense configuration at head width 256, forward only.
+* ``latent2x8192_bf16_causal_shared_rope`` -- the latent configuration with split operands and
+  one rope key [tokens, 1, 64] shared by all 128 heads.
 
 Draw order: the ragged lengths come from a CPU ``torch.Generator`` seeded with ``seed``; the
 tensors from a generator on the target device seeded with ``seed``, in the order q, k, v, dout,
@@ -58,6 +60,7 @@ class Workload:
     sigma: float = 1.0
     bias: Optional[str] = None            # None | "alibi_prefix" (per head) | "prefix" (broadcast)
     latent_split: Optional[tuple] = None  # (nope, rope) widths of the QK head
+    rope_heads: Optional[int] = None      # latent: heads of the rope key (None: h_kv; 1: shared)
     backward: bool = True
     meta: dict = field(default_factory=dict)
 
@@ -123,6 +126,12 @@ def workload(name: str, seed: int = 0) -> Workload:
         lens = [8192] * 2
         return Workload(name, "bf16", lens, lens, 128, 128, 192, 128, causal=True,
                         scale=1.0 / math.sqrt(192.0), latent_split=(128, 64))
+    if name == "latent2x8192_bf16_causal_shared_rope":
+        # the latent configuration with its operands split as produced and one rope key shared
+        # by every head (the form the split-operand calls take)
+        lens = [8192] * 2
+        return Workload(name, "bf16", lens, lens, 128, 128, 192, 128, causal=True,
+                        scale=1.0 / math.sqrt(192.0), latent_split=(128, 64), rope_heads=1)
     if name == "decode64x8192_bf16_gqa":
         # one new query row per sequence against an 8192-token cache (end-aligned causal: the
         # row sees every key), GQA 4, forward only
@@ -143,15 +152,17 @@ def workload(name: str, seed: int = 0) -> Workload:
 WORKLOADS = ["varlen64_fp16_full", "varlen64_fp16_causal", "dense4x4096_bf16_causal",
              "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
              "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "decode64x8192_bf16_gqa",
-             "dense4x4096_bf16_causal_d96", "decode4x32768_bf16_gqa", "dense4x4096_bf16_causal_d256"]
+             "dense4x4096_bf16_causal_d96", "decode4x32768_bf16_gqa", "dense4x4096_bf16_causal_d256",
+             "latent2x8192_bf16_causal_shared_rope"]
 
 
 def custom(lengths_q, lengths_kv=None, *, dtype="bf16", h_q=4, h_kv=None, d_qk=64, d_v=None,
-           causal=False, window=0, scale=None, sigma=1.0, bias=None, name="custom") -> Workload:
+           causal=False, window=0, scale=None, sigma=1.0, bias=None, latent_split=None,
+           rope_heads=None, name="custom") -> Workload:
     """A small ad-hoc workload for tests (same draw rules as the named ones)."""
     lengths_kv = list(lengths_q) if lengths_kv is None else list(lengths_kv)
     return Workload(name, dtype, list(lengths_q), lengths_kv, h_q, h_kv or h_q, d_qk,
-                    d_v or d_qk, causal, window, scale, sigma, bias)
+                    d_v or d_qk, causal, window, scale, sigma, bias, latent_split, rope_heads)
 
 
 def cu_seqlens(lengths) -> torch.Tensor:
@@ -221,7 +232,9 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", with_dout: Optional[bo
 
     Returns q [Tq,Hq,Dqk], k [Tkv,Hkv,Dqk], v [Tkv,Hkv,Dv] (workload dtype), dout [Tq,Hq,Dv]
     (if the workload has a backward or ``with_dout``), cu_seqlens_q/kv int32 on ``device``,
-    and bias fp32 [Tq, bias_heads, max_kv] or None.
+    and bias fp32 [Tq, bias_heads, max_kv] or None.  A latent workload also returns its parts
+    q_nope, q_rope, k_nope, k_rope (k_rope with ``rope_heads`` heads; q / k are their
+    concatenations, the rope key broadcast over the kv heads).
     """
     dt = DTYPES[w.dtype]
     gen = torch.Generator(device).manual_seed(seed)
@@ -231,13 +244,14 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", with_dout: Optional[bo
         qn = _normal((tq, w.h_q, nope), w.sigma, dt, gen, device)
         qr = _normal((tq, w.h_q, rope), w.sigma, dt, gen, device)
         kn = _normal((tk, w.h_kv, nope), w.sigma, dt, gen, device)
-        kr = _normal((tk, w.h_kv, rope), w.sigma, dt, gen, device)
+        kr = _normal((tk, w.rope_heads or w.h_kv, rope), w.sigma, dt, gen, device)
         q = torch.cat([qn, qr], dim=2).contiguous()
-        k = torch.cat([kn, kr], dim=2).contiguous()
-        del qn, qr, kn, kr
+        k = torch.cat([kn, kr.expand(tk, w.h_kv, rope)], dim=2).contiguous()
+        split = {"q_nope": qn, "q_rope": qr, "k_nope": kn, "k_rope": kr}
     else:
         q = _normal((tq, w.h_q, w.d_qk), w.sigma, dt, gen, device)
         k = _normal((tk, w.h_kv, w.d_qk), w.sigma, dt, gen, device)
+        split = {}
     v = _normal((tk, w.h_kv, w.d_v), w.sigma, dt, gen, device)
     want_dout = w.backward if with_dout is None else with_dout
     dout = _normal((tq, w.h_q, w.d_v), 1.0, dt, gen, device) if want_dout else None
@@ -246,6 +260,7 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", with_dout: Optional[bo
         "cu_seqlens_q": cu_seqlens(w.lengths_q).to(device),
         "cu_seqlens_kv": cu_seqlens(w.lengths_kv).to(device),
         "bias": make_bias(w, device=device) if (with_bias and w.bias is not None) else None,
+        **split,
     }
 
 
