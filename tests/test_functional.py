@@ -129,3 +129,27 @@ def test_bool_mask_equals_additive_bias_and_oracle():
     ref = oracle_run(w, xc)
     gpu = {"out": out, "dq": q.grad, "dk": k.grad, "dv": v.grad}
     assert_within(compare(w, gpu, ref, keys=["out", "dq", "dk", "dv"]), "bool mask")
+
+
+@pytest.mark.gpu
+def test_latent_attention_autograd_equals_direct_calls():
+    """latent_attention: autograd over the split-operand calls (a rope key shared by the heads
+    gets the sum of their gradients)."""
+    w = W.custom([70, 1, 130], dtype="bf16", h_q=4, h_kv=2, d_qk=192, d_v=128, causal=True,
+                 latent_split=(128, 64), rope_heads=1)
+    x = W.make_inputs(w, seed=22, device="cuda", with_dout=True)
+    names = ("q_nope", "q_rope", "k_nope", "k_rope", "v")
+    leaves = [x[n].clone().requires_grad_(True) for n in names]
+    out = vlf.latent_attention(*leaves, x["cu_seqlens_q"], x["cu_seqlens_kv"], w.max_seqlen_q,
+                               w.max_seqlen_kv, causal=True)
+    out.backward(x["dout"])
+    o, lse = vlf.vlf_attn_varlen_fwd_latent(*(x[n] for n in names), x["cu_seqlens_q"],
+                                            x["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv,
+                                            causal=True)
+    grads = vlf.vlf_attn_varlen_bwd_latent(x["dout"], *(x[n] for n in names), o, lse,
+                                           x["cu_seqlens_q"], x["cu_seqlens_kv"], w.max_seqlen_q,
+                                           w.max_seqlen_kv, causal=True)
+    assert vlf.vlf_check_error() == 0
+    assert torch.equal(out.detach(), o)
+    for leaf, g in zip(leaves, grads):
+        assert torch.equal(leaf.grad, g)

@@ -37,11 +37,14 @@ CASES = {
                                     causal=True, window=100),
     "fp16_d96_decode_gqa4": W.custom([1, 1, 3], [200, 1, 700], dtype="fp16", h_q=8, h_kv=2,
                                      d_qk=96, causal=True),
-    # width 256: tensor-core forward (one CTA per SM, 256-column O), SIMT backward
+    # width 256: tensor-core forward (one CTA per SM, 256-column O) and backward (dV and dK
+    # passes, dQ)
     "bf16_d256_gqa_causal": W.custom([129, 1, 300, 64], dtype="bf16", h_q=4, h_kv=2, d_qk=256,
                                      causal=True),
     "fp16_d256_decode_gqa4_window": W.custom([1, 2, 1], [700, 90, 1500], dtype="fp16", h_q=8,
                                              h_kv=2, d_qk=256, causal=True, window=600),
+    "fp16_d256_gqa_window_long": W.custom([700, 300, 129], dtype="fp16", h_q=4, h_kv=2,
+                                          d_qk=256, causal=True, window=200),
     "bf16_empty_seqs": W.custom([0, 5, 0, 130], [3, 5, 0, 130], dtype="bf16", h_q=2, d_qk=64,
                                 causal=False),
     # decode-sized problems (the forward packs a kv head's G query heads into one tile)

@@ -443,7 +443,7 @@ __all__ = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_bwd", "vlf_attn_varlen_bwd_wo
 
 # differentiable entry points (autograd over the two calls above)
 from .functional import (flash_attn_varlen_func, flash_attn_varlen_kvpacked_func,  # noqa: E402
-                         flash_attn_varlen_qkvpacked_func, varlen_attention)
+                         flash_attn_varlen_qkvpacked_func, latent_attention, varlen_attention)
 
-__all__ += ["varlen_attention", "flash_attn_varlen_func", "flash_attn_varlen_qkvpacked_func",
+__all__ += ["varlen_attention", "latent_attention", "flash_attn_varlen_func", "flash_attn_varlen_qkvpacked_func",
             "flash_attn_varlen_kvpacked_func"]

@@ -54,6 +54,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // instead, so the single dP buffer is free as soon as the compute warps have loaded it and the
 // next item's dP can run during this item's elementwise pass (S stays double-buffered).
 constexpr int kDkdv = 0, kDq = 1, kDqS = 2;
+// Width 256: the dK and dV accumulators (256 columns each) fill TMEM, so the key-tile work runs
+// as two kernels -- kDv (S^T, P^T, dV += P^T dO) and kDk (S^T, dP^T, dS^T, dK += dS^T Q) --
+// each with room for its product buffers (one S recompute more than kDkdv).
+constexpr int kDv = 3, kDk = 4;
 
 struct BwdMaps {
   CUtensorMap outer0, outer1, inner0, inner1, bias;
@@ -65,13 +69,18 @@ struct BwdMaps {
 // (dQ), IR rows per item.  NBS: stages of the bias ring (0: no bias through TMA).
 template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS = 0>
 struct BwdCfg {
+  // key-tile CTAs (outer tiles K / V, inner items Q / dO) and which products / accumulations run
+  static constexpr bool KEYS = MODE == kDkdv || MODE == kDv || MODE == kDk;
+  static constexpr bool HAS_DP = MODE != kDv;              // dP (dK/dV: dP^T) product
+  static constexpr bool HAS_DV = MODE == kDkdv || MODE == kDv;  // dV += P^T dO
+  static constexpr bool HAS_LAST = MODE != kDv;            // dK or dQ accumulation
   // 64-col blocks of tensors 0 / 1; a width that is not a multiple of 64 (96) is padded to
   // whole blocks (next head's values or zero fill): products step over the real width along K,
   // accumulations run at the padded N and the extra accumulator columns are never stored
   static constexpr int KB0 = (DQK + 63) / 64, KB1 = (DV + 63) / 64;
   static constexpr int NQ_PAD = KB0 * 64, NV_PAD = KB1 * 64;
   static constexpr int OBLK = 128 * 128, IBLK = IR * 128;  // bytes per 64-col block
-  static constexpr int O0_BYTES = KB0 * OBLK, O1_BYTES = KB1 * OBLK;
+  static constexpr int O0_BYTES = KB0 * OBLK, O1_BYTES = MODE == kDv ? 0 : KB1 * OBLK;  // kDv: no V
   static constexpr int I0_BYTES = KB0 * IBLK, I1_BYTES = KB1 * IBLK;
   // two rings of inner tiles: ring 0 (Q for dK/dV, K for dQ; NSTAGE slots) and ring 1 (dO for
   // dK/dV, V for dQ; NSTAGE1 slots), each slot released as soon as its last reader is done
@@ -79,16 +88,16 @@ struct BwdCfg {
   static constexpr int OFF_IN1 = OFF_IN0 + NSTAGE * I0_BYTES;
   // per ring-0 slot: the item's IR columns as IR/2 pairs {-LSE2_c, -LSE2_c+1, -D_c, -D_c+1}
   // (dK/dV only)
-  static constexpr int PAIRS = MODE == kDkdv ? IR / 2 : 0;
+  static constexpr int PAIRS = KEYS ? IR / 2 : 0;
   static constexpr int OFF_LD = OFF_IN1 + NSTAGE1 * I1_BYTES;
   // bias ring: per item its 128 x IR fp32 tile as 32-column boxes.  dK/dV: 4 boxes {32 keys, IR
   // query rows}, unswizzled (the 32 keys of a warp read one 128-byte row at a time); dQ: IR / 32
   // boxes {32 keys, 128 query rows}, 128-byte swizzled (each thread reads along its own row).
-  static constexpr int BIAS_BOX = MODE == kDkdv ? 32 * IR * 4 : 32 * 128 * 4;
+  static constexpr int BIAS_BOX = KEYS ? 32 * IR * 4 : 32 * 128 * 4;
   static constexpr int BIAS_STAGE = 128 * IR * 4;
   static constexpr int NBS_ = NBS > 0 ? NBS : 1;  // (a nonzero divisor where there is no ring)
   // (swizzled boxes start 1024-byte aligned, unswizzled ones 128-byte aligned)
-  static constexpr int B_ALIGN = MODE == kDkdv ? 128 : 1024;
+  static constexpr int B_ALIGN = KEYS ? 128 : 1024;
   static constexpr int OFF_B = (OFF_LD + NSTAGE * PAIRS * 16 + B_ALIGN - 1) & ~(B_ALIGN - 1);
   static constexpr int OFF_BAR = OFF_B + NBS * BIAS_STAGE;
   // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE] (ring 0), in1_full[NSTAGE1],
@@ -104,17 +113,19 @@ struct BwdCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   // TMEM: accumulators first, then NBUF x (S IR cols, dP IR cols); kDqS: NBUF S buffers, then
-  // one dP buffer
-  static constexpr uint32_t ACC0 = 0;    // dV (dK/dV) or dQ (dQ)
-  static constexpr uint32_t ACC1 = 128;  // dK (dK/dV)
-  static constexpr uint32_t BUF = MODE == kDkdv ? 128 + NQ_PAD : (MODE == kDqS ? NQ_PAD : 256);
+  // one dP buffer.  kDv / kDk: the one accumulator (dV / dK, up to 256 columns) at 0.
+  static constexpr uint32_t ACC0 = 0;                       // dV (dK/dV, kDv) or dQ (dQ)
+  static constexpr uint32_t ACC1 = MODE == kDk ? 0 : 128;   // dK (dK/dV, kDk)
+  static constexpr uint32_t BUF = MODE == kDkdv ? 128 + NQ_PAD
+                                  : (MODE == kDv ? NV_PAD : (MODE == kDk || MODE == kDqS ? NQ_PAD : 256));
   __host__ __device__ static constexpr uint32_t s_col(int b) { return MODE == kDqS ? BUF + IR * b : BUF + 2 * IR * b; }
   __host__ __device__ static constexpr uint32_t dp_col(int b) { return MODE == kDqS ? BUF + NBUF * IR : BUF + 2 * IR * b + IR; }
   static constexpr int HALF = IR / 2;      // columns per compute warpgroup
   static constexpr int CHUNKS = HALF / 32;  // 32-column chunks per compute thread
   static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * 2 * IR) <= 512, "TMEM columns");
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(NV_PAD <= 128 && NQ_PAD <= 256 && DQK % 32 == 0 && DV % 32 == 0, "head widths");
+  static_assert((MODE != kDkdv || NV_PAD <= 128) && NV_PAD <= 256 && NQ_PAD <= 256 && DQK % 32 == 0 &&
+                DV % 32 == 0, "head widths");
   static_assert(IR == 64 || IR == 128, "item rows");
   static_assert(NBUF == 1 || IR == 64 || MODE == kDqS, "double buffering only with 64-row items");
 };
@@ -149,7 +160,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   const int bxr = p.heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
   const int gx = p.heads_fast ? (int)gridDim.y : (int)gridDim.x;
   const int byh = p.heads_fast ? (int)blockIdx.x : (int)blockIdx.y;
-  if (MODE == kDkdv) {
+  if (C::KEYS) {
     tile0 = bxr * 128;  // first key
     hk = byh;
     head_outer = hk;
@@ -195,7 +206,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     for (int i = 0; i < NSTAGE; ++i) { mbar_init(bar(C::B_IF + i), 33); mbar_init(bar(C::B_IE + i), 1); }
     for (int i = 0; i < NSTAGE1; ++i) { mbar_init(bar(C::B_IF1 + i), 1); mbar_init(bar(C::B_IE1 + i), 1); }
     for (int b = 0; b < NBUF; ++b) {
-      mbar_init(bar(C::B_S + b), 2);
+      mbar_init(bar(C::B_S + b), C::HAS_DP ? 2 : 1);  // S and dP issued
       mbar_init(bar(C::B_P + b), 256);
       mbar_init(bar(C::B_D + b), 1);
       mbar_init(bar(C::B_D0 + b), 1);
@@ -217,8 +228,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   constexpr int is_bf16 = BF16 ? 1 : 0;
 
   // item n -> (query head, first inner row) ; inner rows are queries (dK/dV) or keys (dQ)
-  auto item_head = [&](int n) { return MODE == kDkdv ? hk * p.group + n / nq_tiles : head_outer; };
-  auto item_row = [&](int n) { return MODE == kDkdv ? lo + (n % nq_tiles) * IR : lo + n * IR; };
+  auto item_head = [&](int n) { return C::KEYS ? hk * p.group + n / nq_tiles : head_outer; };
+  auto item_row = [&](int n) { return C::KEYS ? lo + (n % nq_tiles) * IR : lo + n * IR; };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -238,16 +249,16 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           tma_prefetch_desc(&maps.outer0_rope);
           tma_prefetch_desc(&maps.inner0_rope);
         }
-        const int orow = (MODE == kDkdv ? sq.k0 : sq.q0) + tile0;
-        const int oh = MODE == kDkdv ? hk : head_outer;  // head index inside the outer tensors
+        const int orow = (C::KEYS ? sq.k0 : sq.q0) + tile0;
+        const int oh = C::KEYS ? hk : head_outer;  // head index inside the outer tensors
         mbar_expect_tx(bar(C::B_OUT), C::O0_BYTES + C::O1_BYTES);
         for (int c = 0; c < C::KB0; ++c) {
           if (lat && c == 2)  // the rope block: K's from the (possibly shared) rope key, or Q's
-            tma_load_2d(sO0 + c * C::OBLK, &maps.outer0_rope, (MODE == kDkdv ? rh : oh) * 64, orow, bar(C::B_OUT));
+            tma_load_2d(sO0 + c * C::OBLK, &maps.outer0_rope, (C::KEYS ? rh : oh) * 64, orow, bar(C::B_OUT));
           else
             tma_load_2d(sO0 + c * C::OBLK, &maps.outer0, oh * qw + 64 * c, orow, bar(C::B_OUT));
         }
-        for (int c = 0; c < C::KB1; ++c)
+        for (int c = 0; c < (C::O1_BYTES > 0 ? C::KB1 : 0); ++c)  // (kDv reads no V)
           tma_load_2d(sO1 + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
       }
       int issued0[NSTAGE] = {0}, issued1[NSTAGE1] = {0}, issuedb[C::NBS_] = {0};
@@ -265,7 +276,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
               // bias columns: bias head * max_seqlen_kv + sequence-local key; rows: global query
               // rows.  Boxes past the tensor are zero-filled; columns past the sequence's keys
               // and rows past its queries are masked by the compute threads.
-              if (MODE == kDkdv) {
+              if (C::KEYS) {
                 const int x = (p.bias_heads == 1 ? 0 : item_head(n)) * p.max_kv + tile0;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -286,7 +297,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           if (lane == 0) w = mbar_wait(bar(C::B_IE + st), ((n / NSTAGE) - 1) & 1, abort_flag, p.err);
           if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
         }
-        if (MODE == kDkdv) {
+        if (C::KEYS) {
           // -LSE (base 2; -inf for rows that see nothing or lie past the sequence, so P = 0) and
           // -D of the item's column pairs lane, lane + 32, ...
           const int h = item_head(n), i0 = item_row(n);
@@ -308,14 +319,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             ldbuf[st * C::PAIRS + lane + 32 * pp] = make_float4(nl[0], nl[1], nd[0], nd[1]);
           }
         }
-        const int ih = MODE == kDkdv ? item_head(n) : hk;  // head inside the inner tensors
-        const int irow = (MODE == kDkdv ? sq.q0 : sq.k0) + item_row(n);
+        const int ih = C::KEYS ? item_head(n) : hk;  // head inside the inner tensors
+        const int irow = (C::KEYS ? sq.q0 : sq.k0) + item_row(n);
         if (lane == 0) {
           mbar_expect_tx(bar(C::B_IF + st), C::I0_BYTES);
           for (int c = 0; c < C::KB0; ++c) {
             if (lat && c == 2)
               tma_load_2d(sIn0 + st * C::I0_BYTES + c * C::IBLK, &maps.inner0_rope,
-                          (MODE == kDkdv ? ih : rh) * 64, irow, bar(C::B_IF + st));
+                          (C::KEYS ? ih : rh) * 64, irow, bar(C::B_IF + st));
             else
               tma_load_2d(sIn0 + st * C::I0_BYTES + c * C::IBLK, &maps.inner0, ih * qw + 64 * c, irow,
                           bar(C::B_IF + st));
@@ -354,11 +365,11 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     // the pipe idle; split, each waits only for what its own products need.  Each runs its
     // loop as a whole converged warp (uniform operands) and elect.sync picks the issuing lane.
     const int role = warp == 1 ? 0 : (warp == 11 ? 1 : 2);  // 0: S, 1: dP, 2: accumulations
-    if (n_items > 0) {
+    if (n_items > 0 && (C::HAS_DP || role != 1)) {  // (kDv: no dP products)
       // S / dP: M = 128 outer rows, N = IR inner rows, both operands K-major
       const uint32_t id_sp = idesc_f16(is_bf16, 128, IR, 0, 0);
       // accumulations: A from TMEM (K = IR inner rows), B = inner tile MN-major
-      const uint32_t id_a0 = idesc_f16(is_bf16, 128, MODE == kDkdv ? C::NV_PAD : C::NQ_PAD, 0, 1);
+      const uint32_t id_a0 = idesc_f16(is_bf16, 128, C::KEYS ? C::NV_PAD : C::NQ_PAD, 0, 1);
       const uint32_t id_a1 = idesc_f16(is_bf16, 128, C::NQ_PAD, 0, 1);
       // descriptors are built once; a K step adds its byte offset / 16 to the start-address
       // field (shared addresses stay far below the field's 2^18-byte range, so nothing carries)
@@ -384,7 +395,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // the 16-bit A operand of K step kk (16 inner rows) sits in the first half of the 32-column
       // chunk its compute thread loaded: column 32 * (kk / 2) + 8 * (kk % 2)
       auto a_col = [](int kk) { return (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1)); };
-      // accumulation 0 (dV += P^T dO) -- dK/dV only
+      // accumulation 0 (dV += P^T dO) -- dK/dV and kDv
       auto issue_acc0 = [&](int n) {
         const uint64_t d_i1 = sdesc_sw128(sIn1 + (n % NSTAGE1) * C::I1_BYTES, C::IBLK, 1024);
 #pragma unroll
@@ -395,8 +406,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // last accumulation: dK += dS^T Q (dK/dV) or dQ += dS K (dQ)
       auto issue_acc1 = [&](int n) {
         const uint64_t d_i0 = sdesc_sw128(sIn0 + (n % NSTAGE) * C::I0_BYTES, C::IBLK, 1024);
-        const uint32_t acc = MODE == kDkdv ? C::ACC1 : C::ACC0;
-        const uint32_t id = MODE == kDkdv ? id_a1 : id_a0;
+        const uint32_t acc = C::KEYS ? C::ACC1 : C::ACC0;
+        const uint32_t id = C::KEYS ? id_a1 : id_a0;
 #pragma unroll
         for (int kk = 0; kk < IR / 16; ++kk)
           mma_ts_w(tmem + acc, (MODE == kDqS ? s_cols(n) : dp_cols(n)) + a_col(kk),
@@ -422,11 +433,12 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             const int n = m - NBUF;  // the item that used these columns before
             const uint32_t par = (n / NBUF) & 1;
             if (role == 0) {
-              // S(m) overwrites the columns accumulation 0 (dK/dV) read P^T from; kDq: they are
-              // free as soon as the compute warps have loaded them; kDqS: once the dQ
+              // S(m) overwrites the columns accumulation 0 (dK/dV, kDv) read P^T from; kDq, kDk:
+              // they are free as soon as the compute warps have loaded them; kDqS: once the dQ
               // accumulation has read the dS written there
-              ok = MODE == kDkdv ? wait_all(C::B_D0 + b, par)
-                                 : (MODE == kDq ? wait_all(C::B_P + b, par) : wait_all(C::B_D + b, par));
+              ok = C::HAS_DV ? wait_all(C::B_D0 + b, par)
+                             : (MODE == kDq || MODE == kDk ? wait_all(C::B_P + b, par)
+                                                           : wait_all(C::B_D + b, par));
             } else {
               // dP(m) overwrites the dS the last accumulation reads
               ok = wait_all(C::B_D + b, par);
@@ -437,8 +449,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           if (role == 0) issue_s(m);
           else issue_dp(m);
           mma_commit_w(bar(C::B_S + b));
-          // dQ: V (ring 1) has no reader after dP
-          if (MODE != kDkdv && role == 1) mma_commit_w(bar(C::B_IE1 + m % NSTAGE1));
+          // dQ, kDk: V / dO (ring 1) has no reader after dP
+          if (!C::HAS_DV && role == 1) mma_commit_w(bar(C::B_IE1 + m % NSTAGE1));
         }
       } else {
         for (int n = 0; n < n_items && ok; ++n) {
@@ -446,13 +458,19 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           ok = wait_all(C::B_P + b, (n / NBUF) & 1);
           if (!ok) break;
           fence_after();
-          if (MODE == kDkdv) {
+          if (C::HAS_DV) {
+            // kDv: no dP product has waited for this item's dO tile; wait for it here
+            if (MODE == kDv) {
+              ok = wait_all(C::B_IF1 + n % NSTAGE1, (n / NSTAGE1) & 1);
+              if (!ok) break;
+              fence_after();
+            }
             issue_acc0(n);
             mma_commit_w(bar(C::B_D0 + b));
             mma_commit_w(bar(C::B_IE1 + n % NSTAGE1));  // dO (ring 1) has no reader after dV
           }
-          issue_acc1(n);
-          mma_commit_w(bar(C::B_D + b));
+          if (C::HAS_LAST) issue_acc1(n);
+          mma_commit_w(bar(C::B_D + b));  // (the item's last accumulation)
           mma_commit_w(bar(C::B_IE + n % NSTAGE));
         }
       }
@@ -468,15 +486,15 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     const float sl2 = p.scale_log2;
     const int orow = tile0 + r;  // this thread's outer row
-    const bool orow_ok = MODE == kDkdv ? orow < sq.kv_len : orow < sq.q_len;
+    const bool orow_ok = C::KEYS ? orow < sq.kv_len : orow < sq.q_len;
     // the columns this row may see form one interval (query rows for dK/dV, keys for dQ)
     int vis_lo, vis_hi;
-    if (MODE == kDkdv) visible_rows(orow, off, sq.q_len, p.causal, p.window, vis_lo, vis_hi);
+    if (C::KEYS) visible_rows(orow, off, sq.q_len, p.causal, p.window, vis_lo, vis_hi);
     else visible_range(orow, off, sq.kv_len, p.causal, p.window, vis_lo, vis_hi);
     if (!orow_ok) vis_hi = vis_lo;
     float row_nl = -INFINITY, row_nd = 0.f;  // dQ: this row's -LSE (base 2) and -D
     const float *brow_dq = nullptr;
-    if (MODE != kDkdv && orow_ok) {
+    if (!C::KEYS && orow_ok) {
       const size_t gi = (size_t)head_outer * p.total_q + sq.q0 + orow;
       const float L = p.lse[gi];
       row_nl = L == -INFINITY ? -INFINITY : -L * kLog2e;
@@ -493,13 +511,13 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       bool w = mbar_wait(bar(C::B_S + b), (n / NBUF) & 1, abort_flag, p.err);
       // the LSE / D pairs were written by the producer lanes before their arrive on in_full:
       // acquire that barrier too before reading them
-      if (MODE == kDkdv && w) w = mbar_wait(bar(C::B_IF + st), (n / NSTAGE) & 1, abort_flag, p.err);
+      if (C::KEYS && w) w = mbar_wait(bar(C::B_IF + st), (n / NSTAGE) & 1, abort_flag, p.err);
       if (BIAS == 2 && w) w = mbar_wait(bar(C::B_BF + n % C::NBS_), (n / C::NBS_) & 1, abort_flag, p.err);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       fence_after();
       const float *brow = brow_dq;
-      if (MODE == kDkdv && BIAS == 1 && orow_ok) {
+      if (C::KEYS && BIAS == 1 && orow_ok) {
         const int bh = p.bias_heads == 1 ? 0 : h;
         brow = p.bias + (size_t)bh * p.max_kv + orow;  // + (q0 + i) * bias_heads * max_kv per column
       }
@@ -511,10 +529,15 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         uint32_t sv[32], dv[32];
         __syncwarp();
         tmem_ld32(s_addr, sv);
-        tmem_ld32(dp_addr, dv);
+        if (C::HAS_DP) {
+          tmem_ld32(dp_addr, dv);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dv[e] = 0u;  // (kDv: no dP; dS is not formed)
+        }
         // is every element of this thread's 32 columns visible (no per-element mask)?
         bool plain;
-        if (MODE == kDkdv) {
+        if (C::KEYS) {
           const int j = orow, ilast = i0 + 31;
           plain = orow_ok && ilast < sq.q_len && (!p.causal || j <= i0 + off) &&
                   (p.window <= 0 || j >= ilast + off - p.window + 1);
@@ -530,7 +553,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         float bq4[32];
         if (BIAS == 2) {
           const uint32_t bstage = sBias + (n % C::NBS_) * C::BIAS_STAGE;
-          if (MODE == kDkdv) {
+          if (C::KEYS) {
             const uint32_t bcol = bstage + quarter * C::BIAS_BOX + lane * 4 + col0 * 128;
 #pragma unroll
             for (int k = 0; k < 32; ++k) bq4[k] = lds_f32(bcol + k * 128);
@@ -556,7 +579,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           for (int e = 0; e < 16; ++e) {
             const int c = 2 * e;
             float4 q4;
-            if (MODE == kDkdv) q4 = lp[e];
+            if (C::KEYS) q4 = lp[e];
             else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
             float xa = fmaf(__uint_as_float(sv[c]), sl2, q4.x);
             float xb = fmaf(__uint_as_float(sv[c + 1]), sl2, q4.y);
@@ -572,7 +595,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         } else {
           // dQ with a bias from global memory: the chunk's 32 bias values of this row, 16 bytes
           // at a time when the row address is 16-byte aligned and the chunk lies inside the row
-          const bool bvec = BIAS == 1 && MODE != kDkdv && brow != nullptr &&
+          const bool bvec = BIAS == 1 && !C::KEYS && brow != nullptr &&
                             (reinterpret_cast<uintptr_t>(brow + i0) & 15u) == 0 && i0 + 32 <= p.max_kv;
           if (bvec) {
 #pragma unroll
@@ -585,7 +608,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           for (int e = 0; e < 16; ++e) {
             const int c = 2 * e;
             float4 q4;
-            if (MODE == kDkdv) q4 = lp[e];
+            if (C::KEYS) q4 = lp[e];
             else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
             float xs[2];
 #pragma unroll
@@ -597,7 +620,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
               } else if (BIAS == 1 && brow) {
                 // element by element unless the chunk was loaded 16 bytes at a time (bq4),
                 // clamped into the sequence so that masked columns read a valid address
-                const float bv = MODE == kDkdv
+                const float bv = C::KEYS
                                      ? __ldg(brow + (size_t)(sq.q0 + min(cc, sq.q_len - 1)) * p.bias_heads * (size_t)p.max_kv)
                                      : (bvec ? bq4[c + u] : __ldg(brow + min(cc, sq.kv_len - 1)));
                 x = fmaf(bv, kLog2e, x);
@@ -612,8 +635,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           }
         }
         __syncwarp();
-        if (MODE == kDkdv) tmem_st16(s_addr, pk);
-        tmem_st16(MODE == kDqS ? s_addr : dp_addr, dk);
+        if (C::KEYS && C::HAS_DV) tmem_st16(s_addr, pk);          // P^T for dV
+        if (C::HAS_DP) tmem_st16(MODE == kDqS ? s_addr : dp_addr, dk);  // dS (dK/dV: dS^T)
       }
       if (BIAS == 2) mbar_arrive(bar(C::B_BE + n % C::NBS_));  // the bias slot may be refilled
       tmem_st_wait();
@@ -628,7 +651,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       fence_after();
       // TMEM columns [tcol, tcol + ncols) of this thread's row, times mul, to dst_base + off
       // (elements): 16-bit, or fp32 when f32
-      const size_t g = (size_t)((MODE == kDkdv ? sq.k0 : sq.q0) + (orow_ok ? orow : 0));
+      const size_t g = (size_t)((C::KEYS ? sq.k0 : sq.q0) + (orow_ok ? orow : 0));
       auto store_acc = [&](uint32_t tcol, int ncols, void *dst_base, size_t off, float mul, bool f32) {
 #pragma unroll 1
         for (int ch = 0; ch < ncols / 32; ++ch) {
@@ -663,7 +686,15 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // a latent head given as split operands: the nope and rope parts of dK / dQ go to separate
       // tensors; a rope key shared by the kv heads gets its per-head part in fp32, summed later
       const bool lat = DQK == 192 && p.latent;
-      if (MODE == kDkdv) {
+      if (MODE == kDv || MODE == kDk) {
+        // the pass's one accumulator, its columns split between the two halves
+        constexpr int W = MODE == kDv ? DV : DQK, first = 32 * ((W / 32 + 1) / 2);
+        void *dst = MODE == kDv ? p.dv : p.dk;
+        const uint32_t acc = MODE == kDv ? C::ACC0 : C::ACC1;
+        const float mul = MODE == kDv ? 1.f : p.scale;
+        if (half == 0) store_acc(acc, first, dst, (g * p.h_kv + hk) * W, mul, false);
+        else if (W > first) store_acc(acc + first, W - first, dst, (g * p.h_kv + hk) * W + first, mul, false);
+      } else if (MODE == kDkdv) {
         if (half == 0) {
           store_acc(C::ACC0, DV, p.dv, (g * p.h_kv + hk) * DV, 1.f, false);
         } else if (!lat) {
@@ -714,7 +745,7 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   const uint64_t qw = lat ? 128 : DQK;
   const uint64_t qc = (uint64_t)p.h_q * qw, kc = (uint64_t)p.h_kv * qw;
   const uint64_t qrc = (uint64_t)p.h_q * 64, krc = (uint64_t)(lat ? p.rope_heads : 1) * 64;
-  if (MODE == kDkdv) {
+  if (C::KEYS) {
     ok = make_tmap_16bit(&m.outer0, p.k, tk, kc, kc, 128, bf) &&
          make_tmap_16bit(&m.outer1, p.v, tk, (uint64_t)p.h_kv * DV, (uint64_t)p.h_kv * DV, 128, bf) &&
          make_tmap_16bit(&m.inner0, p.q, tq, qc, qc, IR, bf) &&
@@ -734,12 +765,12 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   if (!lat) { m.outer0_rope = m.outer0; m.inner0_rope = m.inner0; }  // (unused)
   if (NBS > 0)
     ok = ok && make_tmap_bias(&m.bias, p.bias, tq, (uint64_t)p.bias_heads * p.max_kv,
-                              MODE == kDkdv ? IR : 128, MODE != kDkdv);
+                              C::KEYS ? IR : 128, !C::KEYS);
   else
     m.bias = m.inner0;  // (unused)
   if (!ok) return cudaErrorInvalidValue;
-  const unsigned tiles = MODE == kDkdv ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128;
-  const unsigned heads = MODE == kDkdv ? p.h_kv : p.h_q;
+  const unsigned tiles = C::KEYS ? (p.max_kv + 127) / 128 : (p.max_q + 127) / 128;
+  const unsigned heads = C::KEYS ? p.h_kv : p.h_q;
   if (tiles == 0) return cudaSuccess;
   Params pl = p;
   pl.heads_fast = p.bias != nullptr && p.bias_heads == 1;
@@ -806,12 +837,27 @@ cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   return mark(ev, 3, st);
 }
 
+// Width 256: the row-dot, the dV pass and the dK pass (together the dK/dV stage), then dQ (dS
+// over S, 64-key items).  Rings as deep as shared memory allows: 64 KB outer tiles, 32 KB items.
+cudaError_t bwd_shape256(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
+  cudaError_t e;
+  if ((e = mark(ev, 0, st)) != cudaSuccess) return e;
+  if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
+  if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDv, 256, 256, 64, 2, 2, 2, 0>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDk, 256, 256, 64, 2, 2, 1, 0>(p, st)) != cudaSuccess) return e;
+  if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDqS, 256, 256, 64, 2, 2, 1, 0>(p, st)) != cudaSuccess) return e;
+  return mark(ev, 3, st);
+}
+
 }  // namespace
 
 bool tc_backward_supported(const Params &p) {
   if (p.dtype != VLF_F16 && p.dtype != VLF_BF16) return false;
   return (p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 96 && p.d_v == 96) ||
-         (p.d_qk == 128 && p.d_v == 128) || (p.d_qk == 192 && p.d_v == 128);
+         (p.d_qk == 128 && p.d_v == 128) || (p.d_qk == 192 && p.d_v == 128) ||
+         (p.d_qk == 256 && p.d_v == 256);
 }
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
@@ -829,6 +875,7 @@ cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev)
   if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 6, 6, 0, kDqS, 128, 2, 3, 3, 0>(p, st, ev);
   if (p.d_qk == 96) return bwd_shape<96, 96, 64, 2, 5, 4, 0, kDqS, 128, 2, 3, 2, 0>(p, st, ev);
   if (p.d_qk == 128) return bwd_shape<128, 128, 64, 2, 5, 4, 0, kDqS, 128, 2, 3, 2, 0>(p, st, ev);
+  if (p.d_qk == 256) return bwd_shape256(p, st, ev);
   return bwd_shape<192, 128, 64, 1, 3, 3, 0, kDq, 64, 2, 3, 3, 0>(p, st, ev);
 }
 

@@ -5,7 +5,7 @@ max_seqlen_q, scale=None, causal=False)`` with a sliding ``window`` and an addit
 ``attn_bias`` (a bool mask becomes a 0 / -inf bias; a bias that requires grad is refused), and
 differentiable flash_attn-compatible wrappers ``flash_attn_varlen_qkvpacked_func(qkv,
 cu_seqlens, max_seqlen)`` and ``flash_attn_varlen_kvpacked_func(q, kv, cu_q, cu_k, max_q,
-max_k)``.  Everything here is argument marshalling and autograd plumbing: the forward and the
+max_k)``; and ``latent_attention`` on split nope / rope operands.  Everything here is argument marshalling and autograd plumbing: the forward and the
 backward are the library's kernels (``vlf_attn_varlen_fwd`` / ``vlf_attn_varlen_bwd``).
 
 flash_attn's ``window_size=(left, right)`` counts keys on each side of the diagonal; the window
@@ -19,7 +19,7 @@ from __future__ import annotations
 import torch
 
 from . import (VLF_ERR_INVALID, VLF_ERR_UNSUPPORTED, VlfError, vlf_attn_varlen_bwd,
-               vlf_attn_varlen_fwd)
+               vlf_attn_varlen_bwd_latent, vlf_attn_varlen_fwd, vlf_attn_varlen_fwd_latent)
 
 
 def mask_to_bias(mask: torch.Tensor) -> torch.Tensor:
@@ -83,6 +83,53 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_seq
         max_seqlen_kv = int((cu_seqlens_kv[1:] - cu_seqlens_kv[:-1]).max().item()) \
             if cu_seqlens_kv.numel() > 1 else 0
     return _VarlenAttention.apply(q.contiguous(), k.contiguous(), v.contiguous(), cu_seqlens_q,
+                                  cu_seqlens_kv, int(max_seqlen_q), int(max_seqlen_kv), scale,
+                                  bool(causal), int(window or 0), bias)
+
+
+class _LatentAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q_nope, q_rope, k_nope, k_rope, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q,
+                max_seqlen_kv, scale, causal, window, bias):
+        out, lse = vlf_attn_varlen_fwd_latent(q_nope, q_rope, k_nope, k_rope, v, cu_seqlens_q,
+                                              cu_seqlens_kv, max_seqlen_q, max_seqlen_kv,
+                                              scale=scale, causal=causal, window=window, bias=bias)
+        ctx.save_for_backward(q_nope, q_rope, k_nope, k_rope, v, out, lse, cu_seqlens_q,
+                              cu_seqlens_kv)
+        ctx.bias = bias
+        ctx.args = (max_seqlen_q, max_seqlen_kv, scale, causal, window)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q_nope, q_rope, k_nope, k_rope, v, out, lse, cu_q, cu_kv = ctx.saved_tensors
+        max_q, max_kv, scale, causal, window = ctx.args
+        grads = vlf_attn_varlen_bwd_latent(dout.contiguous(), q_nope, q_rope, k_nope, k_rope, v,
+                                           out, lse, cu_q, cu_kv, max_q, max_kv, scale=scale,
+                                           causal=causal, window=window, bias=ctx.bias)
+        return (*grads, None, None, None, None, None, None, None, None)
+
+
+def latent_attention(q_nope, q_rope, k_nope, k_rope, v, cu_seqlens_q, cu_seqlens_kv,
+                     max_seqlen_q, max_seqlen_kv=None, scale=None, causal=False, window=0,
+                     attn_bias=None):
+    """Latent attention with split operands (triton-msl part 2, "Latent attention"),
+    differentiable in all five: score = q_nope . k_nope + q_rope . k_rope (contraction 192 =
+    128 + 64), output width 128.  k_rope [total_kv, 1 or H_kv, 64]: one rope key may serve every
+    head (its gradient is then summed over heads).  ``attn_bias`` as in varlen_attention."""
+    bias = None
+    if attn_bias is not None:
+        if attn_bias.requires_grad:
+            raise VlfError(VLF_ERR_UNSUPPORTED, "the bias is treated as a constant; a bias that "
+                           "requires grad is refused")
+        bias = mask_to_bias(attn_bias).contiguous()
+        if max_seqlen_kv is None:
+            max_seqlen_kv = int(bias.shape[2])
+    if max_seqlen_kv is None:
+        max_seqlen_kv = int((cu_seqlens_kv[1:] - cu_seqlens_kv[:-1]).max().item()) \
+            if cu_seqlens_kv.numel() > 1 else 0
+    return _LatentAttention.apply(q_nope.contiguous(), q_rope.contiguous(), k_nope.contiguous(),
+                                  k_rope.contiguous(), v.contiguous(), cu_seqlens_q,
                                   cu_seqlens_kv, int(max_seqlen_q), int(max_seqlen_kv), scale,
                                   bool(causal), int(window or 0), bias)
 

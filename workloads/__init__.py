@@ -20,7 +20,7 @@ Workloads (named by what they are; the shapes are the benchmark configurations o
   against a cache of 8192 (64 sequences) or 32,768 tokens (4 sequences), H_q=32, H_kv=8, head
   dim 128, end-aligned causal, bf16, forward only.
 * ``dense4x4096_bf16_causal_d96`` -- the dense configuration at head width 96.
-* ``dense4x4096_bf16_causal_d256`` -- the dense configuration at head width 256, forward only.
+* ``dense4x4096_bf16_causal_d256`` -- the dense configuration at head width 256.
 * ``latent2x8192_bf16_causal_shared_rope`` -- the latent configuration with split operands and
   one rope key [tokens, 1, 64] shared by all 128 heads.
 
@@ -114,10 +114,9 @@ def workload(name: str, seed: int = 0) -> Workload:
         lens = [4096] * 4
         return Workload(name, "bf16", lens, lens, 32, 32, 96, 96, causal=True)
     if name == "dense4x4096_bf16_causal_d256":
-        # the dense configuration at head width 256, forward only (the backward at this width
-        # runs on the SIMT kernels)
+        # the dense configuration at head width 256
         lens = [4096] * 4
-        return Workload(name, "bf16", lens, lens, 32, 32, 256, 256, causal=True, backward=False)
+        return Workload(name, "bf16", lens, lens, 32, 32, 256, 256, causal=True)
     if name == "ragged64_gqa_window_bf16":
         g = torch.Generator("cpu").manual_seed(seed)
         lens = ragged_lengths(64, 128, 8192, g)
