@@ -454,10 +454,10 @@ cudaError_t simt_forward(const Params &p, cudaStream_t st) {
 cudaError_t rowdot_forward(const Params &p, cudaStream_t st) {
   if (p.total_q == 0) return cudaSuccess;
   const long long pairs = (long long)p.total_q * p.h_q;
-  if (p.dtype != VLF_F32 && (p.d_v == 64 || p.d_v == 96 || p.d_v == 128)) {
+  if (p.dtype != VLF_F32 && (p.d_v == 64 || p.d_v == 96 || p.d_v == 128 || p.d_v == 256)) {
     // (16-byte loads: the API requires 16-byte aligned tensors, and every segment starts at a
     // multiple of d_v elements, itself a multiple of 8)
-    const int g = p.d_v == 96 ? 4 : p.d_v / 8;
+    const int g = p.d_v == 96 ? 4 : (p.d_v == 256 ? 16 : p.d_v / 8);
     const unsigned blocks = (unsigned)((pairs * g + 255) / 256);
     const bool f16 = p.dtype == VLF_F16;
     if (p.d_v == 64) {
@@ -466,6 +466,9 @@ cudaError_t rowdot_forward(const Params &p, cudaStream_t st) {
     } else if (p.d_v == 96) {
       if (f16) rowdot16_kernel<__half, 4, 3><<<blocks, 256, 0, st>>>(p);
       else rowdot16_kernel<__nv_bfloat16, 4, 3><<<blocks, 256, 0, st>>>(p);
+    } else if (p.d_v == 256) {
+      if (f16) rowdot16_kernel<__half, 16, 2><<<blocks, 256, 0, st>>>(p);
+      else rowdot16_kernel<__nv_bfloat16, 16, 2><<<blocks, 256, 0, st>>>(p);
     } else {
       if (f16) rowdot16_kernel<__half, 16, 1><<<blocks, 256, 0, st>>>(p);
       else rowdot16_kernel<__nv_bfloat16, 16, 1><<<blocks, 256, 0, st>>>(p);

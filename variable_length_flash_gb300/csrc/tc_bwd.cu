@@ -63,6 +63,8 @@ struct BwdMaps {
   CUtensorMap outer0, outer1, inner0, inner1, bias;
   // latent head with split operands: the rope tensors behind outer0 / inner0 (64 columns)
   CUtensorMap outer0_rope, inner0_rope;
+  // outputs stored by TMA boxes {64 columns, 128 rows}: dV, dK (dK/dV); dV (kDv); dK (kDk); dQ
+  CUtensorMap out0, out1;
 };
 
 // outer0/outer1: K, V (dK/dV) or Q, dO (dQ), 128 rows.  inner0/inner1: Q, dO (dK/dV) or K, V
@@ -647,8 +649,53 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     if (ok && n_items > 0)
       ok = mbar_wait(bar(C::B_D + (n_items - 1) % NBUF), ((n_items - 1) / NBUF) & 1, abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
+    // Outputs of a full 128-row tile whose widths are whole 64-column blocks leave through TMA:
+    // each thread writes its row into the idle outer-tile shared memory in the 128-byte-swizzled
+    // box layout and one thread stores whole boxes (per-thread row stores land 32 rows of
+    // another head apart and cost a store transaction per 16 bytes).  Other tiles store rows.
+    const bool lat_out = DQK == 192 && p.latent;
+    const bool tma_out =
+        !lat_out && (C::KEYS ? sq.kv_len : sq.q_len) - tile0 >= 128 &&
+        (MODE == kDkdv ? DV % 64 == 0 && DQK % 64 == 0 : (MODE == kDv ? DV % 64 == 0 : DQK % 64 == 0));
     if (ok) {
       fence_after();
+      // TMEM columns [tcol, tcol + ncols) of this row, times mul, into the staging boxes from
+      // output column col0 on (64 columns per box, 16 KB each, at the outer tiles' offset)
+      auto stage_acc = [&](uint32_t tcol, int ncols, int col0, float mul) {
+#pragma unroll 1
+        for (int ch = 0; ch < ncols / 32; ++ch) {
+          uint32_t v[32];
+          if (n_items > 0) {
+            __syncwarp();
+            tmem_ld32(lane_addr + tcol + ch * 32, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          uint32_t o16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            o16[e] = pack2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul, is_bf16);
+          const int col = col0 + 32 * ch, c16 = (col % 64) / 8;
+          const uint32_t rowa = base + C::OFF_O0 + (col / 64) * C::OBLK + r * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            sts_v4(rowa + (((c16 + q) ^ (r & 7)) << 4), o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
+        }
+      };
+      if (tma_out) {
+        if (MODE == kDkdv) {
+          if (half == 0) stage_acc(C::ACC0, DV, 0, 1.f);                 // dV: boxes 0 .. KB1-1
+          else stage_acc(C::ACC1, DQK, C::KB1 * 64, p.scale);            // dK: the boxes after
+        } else {
+          constexpr int W = MODE == kDv ? DV : DQK, first = 32 * ((W / 32 + 1) / 2);
+          const uint32_t acc = MODE == kDv ? C::ACC0 : (MODE == kDk ? C::ACC1 : C::ACC0);
+          const float mul = MODE == kDv ? 1.f : p.scale;
+          if (half == 0) stage_acc(acc, first, 0, mul);
+          else if (W > first) stage_acc(acc + first, W - first, first, mul);
+        }
+      }
       // TMEM columns [tcol, tcol + ncols) of this thread's row, times mul, to dst_base + off
       // (elements): 16-bit, or fp32 when f32
       const size_t g = (size_t)((C::KEYS ? sq.k0 : sq.q0) + (orow_ok ? orow : 0));
@@ -685,8 +732,10 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       };
       // a latent head given as split operands: the nope and rope parts of dK / dQ go to separate
       // tensors; a rope key shared by the kv heads gets its per-head part in fp32, summed later
-      const bool lat = DQK == 192 && p.latent;
-      if (MODE == kDv || MODE == kDk) {
+      const bool lat = lat_out;
+      if (tma_out) {
+        // (staged above)
+      } else if (MODE == kDv || MODE == kDk) {
         // the pass's one accumulator, its columns split between the two halves
         constexpr int W = MODE == kDv ? DV : DQK, first = 32 * ((W / 32 + 1) / 2);
         void *dst = MODE == kDv ? p.dv : p.dk;
@@ -719,6 +768,29 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           else if (nch > first)
             store_acc(C::ACC0 + 32 * first, 32 * (nch - first), p.dq, row * DQK + 32 * first, p.scale, false);
         }
+      }
+    }
+    if (tma_out) {
+      // every compute thread has staged its rows (a warp that aborted staged nothing; the error
+      // word reports that): make the writes visible to TMA, then one thread stores the boxes and
+      // waits until they have been read out of shared memory
+      fence_proxy_async_smem();
+      named_sync(1, 256);
+      if (warp == 2 && lane == 0 && ok) {
+        const int y = (C::KEYS ? sq.k0 : sq.q0) + tile0;
+        const uint32_t stage0 = base + C::OFF_O0;
+        if (MODE == kDkdv) {
+          for (int j = 0; j < C::KB1; ++j) tma_store_2d(&maps.out0, stage0 + j * C::OBLK, hk * DV + 64 * j, y);
+          for (int j = 0; j < C::KB0; ++j)
+            tma_store_2d(&maps.out1, stage0 + (C::KB1 + j) * C::OBLK, hk * DQK + 64 * j, y);
+        } else if (MODE == kDv) {
+          for (int j = 0; j < C::KB1; ++j) tma_store_2d(&maps.out0, stage0 + j * C::OBLK, hk * DV + 64 * j, y);
+        } else {
+          const int oh = MODE == kDk ? hk : head_outer;
+          for (int j = 0; j < C::KB0; ++j) tma_store_2d(&maps.out0, stage0 + j * C::OBLK, oh * DQK + 64 * j, y);
+        }
+        bulk_commit();
+        bulk_wait_read();
       }
     }
   }
@@ -763,6 +835,19 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
            make_tmap_16bit(&m.inner0_rope, p.k_rope, tk, krc, krc, IR, bf);
   }
   if (!lat) { m.outer0_rope = m.outer0; m.inner0_rope = m.inner0; }  // (unused)
+  // the outputs, for the TMA epilogue of full tiles (dk / dq row widths as the nope parts' for a
+  // split latent head, which stores rows instead)
+  const uint64_t dvc = (uint64_t)p.h_kv * DV;
+  if (MODE == kDkdv)
+    ok = ok && make_tmap_16bit(&m.out0, p.dv, tk, dvc, dvc, 128, bf) &&
+         make_tmap_16bit(&m.out1, p.dk, tk, kc, kc, 128, bf);
+  else if (MODE == kDv)
+    ok = ok && make_tmap_16bit(&m.out0, p.dv, tk, dvc, dvc, 128, bf);
+  else if (MODE == kDk)
+    ok = ok && make_tmap_16bit(&m.out0, p.dk, tk, kc, kc, 128, bf);
+  else
+    ok = ok && make_tmap_16bit(&m.out0, p.dq, tq, qc, qc, 128, bf);
+  if (MODE != kDkdv) m.out1 = m.out0;  // (unused)
   if (NBS > 0)
     ok = ok && make_tmap_bias(&m.bias, p.bias, tq, (uint64_t)p.bias_heads * p.max_kv,
                               C::KEYS ? IR : 128, !C::KEYS);

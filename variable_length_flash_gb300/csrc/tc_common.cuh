@@ -91,6 +91,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x
       : "memory");
 }
 
+// 2-D tiled store of a box from shared memory at (x, y), x and y >= 0 (16-byte rule on x as
+// above), in the calling thread's bulk group; rows past the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// until every committed bulk store of this thread has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// shared-memory writes of the generic proxy made visible to the async proxy (TMA)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+// named barrier over `count` threads (a multiple of 32) of the CTA
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // 3-D tiled load of box {x: 64 elements, y, z} at (x, y, z) (16-byte rule on x as above).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int x, int y, int z,
                                             uint32_t bar) {
