@@ -78,9 +78,9 @@ struct Seq {
 };
 
 // Reads and validates sequence s; on bad cu_seqlens records VLF_ERR_BAD_SEQLENS and returns false.
-__device__ __forceinline__ bool load_seq(const Params &p, int s, Seq &sq) {
-  int a = __ldg(p.cu_q + s), b = __ldg(p.cu_q + s + 1);
-  int c = __ldg(p.cu_kv + s), d = __ldg(p.cu_kv + s + 1);
+// (seq_from: the same from the four values cu_q[s], cu_q[s+1], cu_kv[s], cu_kv[s+1] already
+// loaded, so that a kernel can issue the loads first and overlap their latency with its setup)
+__device__ __forceinline__ bool seq_from(const Params &p, int a, int b, int c, int d, Seq &sq) {
   bool ok = (a >= 0) && (a <= b) && (b <= p.total_q) && (c >= 0) && (c <= d) &&
             (d <= p.total_kv) && (b - a <= p.max_q) && (d - c <= p.max_kv);
   if (!ok) {
@@ -92,6 +92,11 @@ __device__ __forceinline__ bool load_seq(const Params &p, int s, Seq &sq) {
   sq.k0 = c;
   sq.kv_len = d - c;
   return true;
+}
+
+__device__ __forceinline__ bool load_seq(const Params &p, int s, Seq &sq) {
+  return seq_from(p, __ldg(p.cu_q + s), __ldg(p.cu_q + s + 1), __ldg(p.cu_kv + s),
+                  __ldg(p.cu_kv + s + 1), sq);
 }
 
 // ---------------------------------------------------------------- tile scheduler (band math)

@@ -264,6 +264,30 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           tma_load_2d(sO1 + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
       }
       int issued0[NSTAGE] = {0}, issued1[NSTAGE1] = {0}, issuedb[C::NBS_] = {0};
+      // dK/dV: -LSE (base 2; -inf for rows that see nothing or lie past the sequence, so P = 0)
+      // and -D of item n's column pairs lane, lane + 32, ..., loaded one item ahead into
+      // registers so that their global-load latency is off the producer's per-item path
+      // (the raw values are kept: no instruction uses them, so nothing waits, until the write)
+      constexpr int PPL = C::PAIRS > 0 ? C::PAIRS / 32 : 1;
+      float rl[PPL][2], rd[PPL][2];
+      auto load_pairs = [&](int n) {
+        const int h = item_head(n), i0 = item_row(n);
+#pragma unroll
+        for (int pp = 0; pp < PPL; ++pp) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qi = i0 + 2 * (lane + 32 * pp) + u;
+            rl[pp][u] = -INFINITY;
+            rd[pp][u] = 0.f;
+            if (qi < sq.q_len) {
+              const size_t gi = (size_t)h * p.total_q + sq.q0 + qi;
+              rl[pp][u] = __ldg(p.lse + gi);
+              rd[pp][u] = __ldg(p.rowdot + gi);
+            }
+          }
+        }
+      };
+      if (C::KEYS) load_pairs(0);
       for (int n = 0; n < n_items; ++n) {
         const int st = n % NSTAGE, st1 = n % NSTAGE1;
         if (BIAS == 2) {
@@ -300,26 +324,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
         }
         if (C::KEYS) {
-          // -LSE (base 2; -inf for rows that see nothing or lie past the sequence, so P = 0) and
-          // -D of the item's column pairs lane, lane + 32, ...
-          const int h = item_head(n), i0 = item_row(n);
 #pragma unroll
-          for (int pp = 0; pp < C::PAIRS / 32; ++pp) {
-            float nl[2], nd[2];
+          for (int pp = 0; pp < PPL; ++pp) {
+            float nl[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int qi = i0 + 2 * (lane + 32 * pp) + u;
-              nl[u] = -INFINITY;
-              nd[u] = 0.f;
-              if (qi < sq.q_len) {
-                const size_t gi = (size_t)h * p.total_q + sq.q0 + qi;
-                const float L = p.lse[gi];
-                nl[u] = L == -INFINITY ? -INFINITY : -L * kLog2e;
-                nd[u] = -p.rowdot[gi];
-              }
-            }
-            ldbuf[st * C::PAIRS + lane + 32 * pp] = make_float4(nl[0], nl[1], nd[0], nd[1]);
+            for (int u = 0; u < 2; ++u) nl[u] = rl[pp][u] == -INFINITY ? -INFINITY : -rl[pp][u] * kLog2e;
+            ldbuf[st * C::PAIRS + lane + 32 * pp] = make_float4(nl[0], nl[1], -rd[pp][0], -rd[pp][1]);
           }
+          if (n + 1 < n_items) load_pairs(n + 1);  // (consumed next iteration)
         }
         const int ih = C::KEYS ? item_head(n) : hk;  // head inside the inner tensors
         const int irow = (C::KEYS ? sq.q0 : sq.k0) + item_row(n);
