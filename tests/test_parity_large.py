@@ -23,7 +23,7 @@ from tests.parity import LSE_TOL, TOL, gpu_run, max_err
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 LARGE = ["dense4x4096_bf16_causal", "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
-         "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix"]
+         "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "dense4x4096_bf16_causal_d256"]
 
 
 def _np(t):
@@ -157,3 +157,32 @@ def test_decode_full_size_packing_exact(name):
             o_err = max(o_err, max_err(_np(out[cq[s]:cq[s + 1], h]), o_ref))
             l_err = max(l_err, max_err(_np(lse[h, cq[s]:cq[s + 1]]), l_ref))
     assert o_err <= TOL["bf16"] and l_err <= LSE_TOL["bf16"], (o_err, l_err)
+
+
+def test_latent_shared_rope_full_size_equals_plain_calls():
+    """latent2x8192_bf16_causal_shared_rope at full size through the split-operand calls (as
+    bench.py times it) against the plain calls on the concatenated operands (checked against the
+    oracle at full size on the latent workload): identical bits for every output; the shared rope
+    key's gradient against the fp32 sum over the 128 heads of the plain call's rope gradients
+    (each rounded to bf16 there, so the two differ by that rounding only)."""
+    import variable_length_flash_gb300 as vlf
+    torch.cuda.empty_cache()
+    w = W.workload("latent2x8192_bf16_causal_shared_rope")
+    x = W.make_inputs(w, seed=0, device="cuda", with_dout=True)
+    ops = [x[n] for n in ("q_nope", "q_rope", "k_nope", "k_rope", "v")]
+    cu = (x["cu_seqlens_q"], x["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv)
+    out, lse = vlf.vlf_attn_varlen_fwd_latent(*ops, *cu, scale=w.scale, causal=True)
+    grads = vlf.vlf_attn_varlen_bwd_latent(x["dout"], *ops, out, lse, *cu, scale=w.scale,
+                                           causal=True)
+    out_c, lse_c = vlf.vlf_attn_varlen_fwd(x["q"], x["k"], x["v"], *cu, scale=w.scale, causal=True)
+    dq, dk, dv = vlf.vlf_attn_varlen_bwd(x["dout"], x["q"], x["k"], x["v"], out_c, lse_c, *cu,
+                                         scale=w.scale, causal=True)
+    assert vlf.vlf_check_error() == 0
+    assert torch.equal(out, out_c) and torch.equal(lse, lse_c)
+    assert torch.equal(grads[0], dq[..., :128]) and torch.equal(grads[1], dq[..., 128:])
+    assert torch.equal(grads[2], dk[..., :128]) and torch.equal(grads[4], dv)
+    ref = dk[..., 128:].float().sum(dim=1, keepdim=True)
+    err = (grads[3].float() - ref).abs().max().item()
+    assert err <= 1e-2 * ref.abs().max().item(), (err, ref.abs().max().item())
+    del x, grads, dq, dk, dv
+    torch.cuda.empty_cache()
