@@ -65,6 +65,11 @@ typedef enum {
 #define VLF_FLAG_FORCE_SIMT 2u /* use the SIMT fp32-FMA kernels even where a tensor-core one exists */
 #define VLF_FLAG_NO_PACK 4u    /* forward: never pack a kv head's query heads into one tile (the
                                   decode-size layout); results are identical either way */
+#define VLF_FLAG_TEST_TIMEOUT 8u /* testing the failure path: the tensor-core forward's producer
+                                    never loads the query tile, so every CTA's pipeline waits run
+                                    out after their time limit (2 s); the kernel records
+                                    VLF_ERR_TIMEOUT, drains, frees its TMEM and returns, and the
+                                    device stays usable (out is not written) */
 
 /*
  * Forward.  mtlattn 0.3.0, section "Use" (varlen_attention with scale, causal, window, attn_bias).

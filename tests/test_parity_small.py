@@ -195,6 +195,29 @@ def test_bad_cu_seqlens_reported_and_device_stays_usable():
     assert_within(compare(w, gpu, ref), "after error")
 
 
+def test_wait_timeout_reported_and_device_stays_usable():
+    """The failure path without a fault: with VLF_FLAG_TEST_TIMEOUT the forward's producer never
+    loads the query tile, the CTA's bounded waits run out (2 s), the kernel records
+    VLF_ERR_TIMEOUT, drains and returns; the next call on the same context is correct."""
+    import time
+    import variable_length_flash_gb300 as vlf
+    w = W.custom([64], dtype="bf16", h_q=1, d_qk=128)  # one CTA
+    x = W.make_inputs(w, seed=2)
+    dev = {k: (t.cuda() if isinstance(t, torch.Tensor) else t) for k, t in x.items()}
+    assert vlf.vlf_check_error() == 0
+    t0 = time.time()
+    vlf.vlf_attn_varlen_fwd(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"],
+                            dev["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv,
+                            flags=vlf.VLF_FLAG_TEST_TIMEOUT, num_splits=1)
+    status = vlf.vlf_check_error()
+    elapsed = time.time() - t0
+    assert status == vlf.VLF_ERR_TIMEOUT, vlf.vlf_status_string(status)
+    assert 1.5 < elapsed < 60, elapsed  # the 2 s limit ran out, once
+    gpu = gpu_run(w, x, backward=False)
+    ref = oracle_run(w, x, backward=False)
+    assert_within(compare(w, gpu, ref), "after a timeout")
+
+
 def test_refuses_grad_requiring_bias():
     import variable_length_flash_gb300 as vlf
     w = W.custom([8], dtype="bf16", h_q=2, d_qk=64)

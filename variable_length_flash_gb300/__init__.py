@@ -34,6 +34,7 @@ VLF_ERR_TIMEOUT, VLF_ERR_BAD_SEQLENS, VLF_ERR_WORKSPACE = -5, -6, -7
 VLF_FLAG_NO_SKIP = 1
 VLF_FLAG_FORCE_SIMT = 2
 VLF_FLAG_NO_PACK = 4
+VLF_FLAG_TEST_TIMEOUT = 8  # testing: the forward's pipeline waits run out (VLF_ERR_TIMEOUT)
 
 _DTYPE = {torch.float16: VLF_F16, torch.bfloat16: VLF_BF16, torch.float32: VLF_F32}
 

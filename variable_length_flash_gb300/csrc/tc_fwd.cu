@@ -267,8 +267,10 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       }
       int nq = 0;
       for (int t = 0; t < 2; ++t) nq += ti.row0[t] < sq.q_len ? 1 : 0;
-      mbar_expect_tx(bar(C::B_Q), nq * C::Q_BYTES);
-      for (int t = 0; t < 2; ++t) {
+      // (VLF_FLAG_TEST_TIMEOUT: no query tile, so that the waits on it run out)
+      const bool drop_q = (p.flags & VLF_FLAG_TEST_TIMEOUT) != 0;
+      if (!drop_q) mbar_expect_tx(bar(C::B_Q), nq * C::Q_BYTES);
+      for (int t = 0; t < 2 && !drop_q; ++t) {
         if (ti.row0[t] >= sq.q_len) continue;
         for (int c = 0; c < C::KBQ; ++c) {
           if (PACK)  // rows (token, head of the group): one 3-D box
