@@ -23,7 +23,8 @@ from tests.parity import LSE_TOL, TOL, gpu_run, max_err
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 LARGE = ["dense4x4096_bf16_causal", "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
-         "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "dense4x4096_bf16_causal_d256"]
+         "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "dense4x4096_bf16_causal_d96",
+         "dense4x4096_bf16_causal_d256"]
 
 
 def _np(t):
