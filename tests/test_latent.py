@@ -4,8 +4,6 @@ shared by all heads.  CPU: workspace arithmetic and the refusals the C ABI makes
 a device.  GPU: the split-operand calls against the fp64 oracle on the concatenated operands
 (the shared rope key's gradient is the sum over heads of each head's), and bit-identity with
 the concatenated-operand calls where the arithmetic is the same."""
-import ctypes
-
 import numpy as np
 import pytest
 import torch
@@ -86,22 +84,44 @@ def _expected(w, ref):
     return [dq[..., :128], dq[..., 128:], dk[..., :128], dk_rope, ref["dv"]]
 
 
-@pytest.mark.gpu
-@pytest.mark.parametrize("name", list(CASES))
-def test_latent_split_matches_oracle(name):
-    w = CASES[name]
-    x = W.make_inputs(w, seed=41, with_dout=True)
+def _check_against_oracle(w, x, label):
     g = {k: (t.cuda() if isinstance(t, torch.Tensor) else t) for k, t in x.items()}
     out, lse, grads = _latent_run(w, g)
     ref = oracle_run(w, x)
     tol = TOL[w.dtype]
-    assert max_err(to_np(out), ref["out"]) <= tol
-    assert max_err(to_np(lse), ref["lse"]) <= LSE_TOL[w.dtype]
+    assert max_err(to_np(out), ref["out"]) <= tol, label
+    assert max_err(to_np(lse), ref["lse"]) <= LSE_TOL[w.dtype], label
     names = ["dq_nope", "dq_rope", "dk_nope", "dk_rope", "dv"]
     for n, got, exp in zip(names, grads, _expected(w, ref)):
         # a shared rope key sums h_kv heads' gradients (their errors add)
         lim = 3 * tol * (w.h_kv if n == "dk_rope" and w.rope_heads == 1 else 1)
-        assert max_err(to_np(got), exp) <= lim, (name, n, max_err(to_np(got), exp), lim)
+        assert max_err(to_np(got), exp) <= lim, (label, n, max_err(to_np(got), exp), lim)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", list(CASES))
+def test_latent_split_matches_oracle(name):
+    w = CASES[name]
+    _check_against_oracle(w, W.make_inputs(w, seed=41, with_dout=True), name)
+
+
+@pytest.mark.gpu
+def test_latent_split_fuzz():
+    """Random lengths (empty sequences included), GQA, rope key shared or per kv head, causal,
+    window, dtype: every call matches the oracle."""
+    rng = np.random.default_rng(77)
+    for trial in range(8):
+        n = int(rng.integers(1, 4))
+        lq = [int(v) for v in rng.integers(0, 180, n)]
+        lk = lq if rng.random() < 0.6 else [int(v) for v in rng.integers(0, 180, n)]
+        if sum(lq) == 0 or sum(lk) == 0:
+            continue
+        hkv = int(rng.choice([1, 2, 4]))
+        hq = hkv * int(rng.choice([1, 2]))
+        w = W.custom(lq, lk, dtype=str(rng.choice(["fp16", "bf16"])), h_q=hq, h_kv=hkv, d_qk=192,
+                     d_v=128, causal=bool(rng.random() < 0.6), window=int(rng.choice([0, 0, 9, 64])),
+                     latent_split=(128, 64), rope_heads=1 if rng.random() < 0.6 else hkv)
+        _check_against_oracle(w, W.make_inputs(w, seed=200 + trial, with_dout=True), f"fuzz {trial} {w}")
 
 
 @pytest.mark.gpu

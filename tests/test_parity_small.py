@@ -233,16 +233,21 @@ def test_fuzz_correct_or_refuse():
     """Random shapes and flags: every call either matches the oracle or is refused loudly."""
     import variable_length_flash_gb300 as vlf
     rng = np.random.default_rng(1234)
-    for trial in range(12):
+    widths = [(64, 64), (128, 128), (192, 128), (32, 32), (80, 48), (96, 96), (256, 256)]
+    for trial in range(20):
         n = int(rng.integers(1, 5))
-        lq = [int(x) for x in rng.integers(0, 200, n)]
-        cross = rng.random() < 0.3
-        lk = [int(x) for x in rng.integers(0, 200, n)] if cross else lq
+        if rng.random() < 0.25:  # decode-like: a few query rows against longer caches (split-KV)
+            lq = [int(x) for x in rng.integers(1, 5, n)]
+            lk = [int(x) for x in rng.integers(300, 2000, n)]
+        else:
+            lq = [int(x) for x in rng.integers(0, 200, n)]
+            cross = rng.random() < 0.3
+            lk = [int(x) for x in rng.integers(0, 200, n)] if cross else lq
         if sum(lq) == 0 or sum(lk) == 0:
             continue
         hkv = int(rng.choice([1, 2]))
         hq = hkv * int(rng.choice([1, 2, 4]))
-        d, dv = [(64, 64), (128, 128), (192, 128), (32, 32), (80, 48)][int(rng.integers(0, 5))]
+        d, dv = widths[int(rng.integers(0, len(widths)))]
         dtype = str(rng.choice(["fp16", "bf16", "fp32"]))
         causal = bool(rng.random() < 0.6)
         window = int(rng.choice([0, 0, 1, 7, 64]))
