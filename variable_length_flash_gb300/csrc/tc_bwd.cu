@@ -49,7 +49,6 @@ namespace {
 
 using namespace tc;
 
-constexpr float kLog2e = 1.4426950408889634f;
 // kDq keeps dS in the dP columns and double-buffers S and dP; kDqS writes dS over the S columns
 // instead, so the single dP buffer is free as soon as the compute warps have loaded it and the
 // next item's dP can run during this item's elementwise pass (S stays double-buffered).
@@ -132,12 +131,6 @@ struct BwdCfg {
   static_assert(NBUF == 1 || IR == 64 || MODE == kDqS, "double buffering only with 64-row items");
 };
 
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > 200000000ull) break;
-  }
-}
 
 // BF16: element type of the 16-bit tensors (bf16, else fp16), fixed at compile time so the
 // per-element conversions carry no runtime branch.

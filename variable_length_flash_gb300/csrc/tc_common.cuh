@@ -14,6 +14,9 @@ namespace tc {
 // A wait longer than this is a bug (a healthy wait lasts microseconds): the kernel records
 // VLF_ERR_TIMEOUT in the error word, flags the CTA to abort and every role returns.
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+// a teardown drain gives up after this long (the CTA is leaving after an abort)
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -65,6 +68,14 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
         return false;
       }
     }
+  }
+}
+
+// Time-bounded wait that ignores the abort flag: drains in-flight copies and MMAs at teardown.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kDrainTimeoutNs) break;
   }
 }
 

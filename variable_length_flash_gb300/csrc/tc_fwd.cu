@@ -47,7 +47,6 @@ namespace {
 
 using namespace tc;
 
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kBN = 64;                    // keys per KV tile
@@ -109,13 +108,6 @@ struct FwdCfg {
   static_assert(SMEM <= (MIN_BLOCKS == 1 || NBS > 0 ? 232448 : 115712), "shared memory");
 };
 
-// Time-bounded wait that ignores the abort flag (used to drain in-flight work at teardown).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > 200000000ull) break;
-  }
-}
 
 struct TileInfo {
   // row0: first sequence-local query row; head: query head (PACK: the kv head)
