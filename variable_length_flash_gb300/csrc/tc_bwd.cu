@@ -582,22 +582,25 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         uint32_t pk[16], dk[16];
         if (plain) {
           // every pair visible: P = 2^(S log2e scale - LSE2 [+ bias log2e]), dS = P (dP - D)
+          // (packed f32x2 arithmetic: the same per-lane rounding as the scalar forms)
+          const uint64_t sl22 = f2pack(sl2, sl2), lg22 = f2pack(kLog2e, kLog2e);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = 2 * e;
             float4 q4;
             if (C::KEYS) q4 = lp[e];
             else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
-            float xa = fmaf(__uint_as_float(sv[c]), sl2, q4.x);
-            float xb = fmaf(__uint_as_float(sv[c + 1]), sl2, q4.y);
-            if (BIAS == 2) {
-              xa = fmaf(bq4[c], kLog2e, xa);
-              xb = fmaf(bq4[c + 1], kLog2e, xb);
-            }
-            const float pa = ex2(xa), pb = ex2(xb);
-            const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
+            uint64_t x2 = fma2(f2pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl22,
+                               f2pack(q4.x, q4.y));
+            if (BIAS == 2) x2 = fma2(f2pack(bq4[c], bq4[c + 1]), lg22, x2);
+            const float2 x = f2unpack(x2);
+            const float pa = ex2(x.x), pb = ex2(x.y);
+            const uint64_t p2 = f2pack(pa, pb);
+            const uint64_t t2 = add2(f2pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                                     f2pack(q4.z, q4.w));
+            const float2 d = f2unpack(mul2(p2, t2));
             pk[e] = pack2(pa, pb, is_bf16);
-            dk[e] = pack2(pa * ta, pb * tb, is_bf16);
+            dk[e] = pack2(d.x, d.y, is_bf16);
           }
         } else {
           // dQ with a bias from global memory: the chunk's 32 bias values of this row, 16 bytes
@@ -635,10 +638,13 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
               xs[u] = (cc >= vis_lo && cc < vis_hi) ? x : -INFINITY;
             }
             // masked logits (-inf) and rows without keys (-LSE2 = -inf) give P = 0
-            const float pa = ex2(xs[0] + q4.x), pb = ex2(xs[1] + q4.y);
-            const float ta = __uint_as_float(dv[c]) + q4.z, tb = __uint_as_float(dv[c + 1]) + q4.w;
+            const float2 x = f2unpack(add2(f2pack(xs[0], xs[1]), f2pack(q4.x, q4.y)));
+            const float pa = ex2(x.x), pb = ex2(x.y);
+            const uint64_t t2 = add2(f2pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                                     f2pack(q4.z, q4.w));
+            const float2 d = f2unpack(mul2(f2pack(pa, pb), t2));
             pk[e] = pack2(pa, pb, is_bf16);
-            dk[e] = pack2(pa * ta, pb * tb, is_bf16);
+            dk[e] = pack2(d.x, d.y, is_bf16);
           }
         }
         __syncwarp();
