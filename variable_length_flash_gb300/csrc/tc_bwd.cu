@@ -109,7 +109,8 @@ struct BwdCfg {
   static constexpr int B_IE1 = B_IF1 + NSTAGE1, B_S = B_IE1 + NSTAGE1;
   static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + NBUF, B_DRAIN = B_D + NBUF;
   static constexpr int B_PF = B_DRAIN + 3;  // kDqS: the compute warps have loaded dP
-  static constexpr int B_BF = B_PF + 1, B_BE = B_BF + NBS;  // bias full / empty
+  static constexpr int B_QT = B_PF + 1;     // QT: the outer Q / dO rows are in TMEM
+  static constexpr int B_BF = B_QT + 1, B_BE = B_BF + NBS;  // bias full / empty
   static constexpr int NBAR = B_BE + NBS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
@@ -121,6 +122,14 @@ struct BwdCfg {
                                   : (MODE == kDv ? NV_PAD : (MODE == kDk || MODE == kDqS ? NQ_PAD : 256));
   __host__ __device__ static constexpr uint32_t s_col(int b) { return MODE == kDqS ? BUF + IR * b : BUF + 2 * IR * b; }
   __host__ __device__ static constexpr uint32_t dp_col(int b) { return MODE == kDqS ? BUF + NBUF * IR : BUF + 2 * IR * b + IR; }
+  // QT (kDq, widths up to 128): the outer Q and dO tiles are copied once into the TMEM columns
+  // between the accumulator and the S / dP buffers, 16-bit pairs along the row, and are the A
+  // operands of S and dP from there: those products then read only their inner K / V tile from
+  // shared memory (with both operands in shared memory a 64-key product is bound by its reads).
+  // kDqS has no free columns for them.
+  static constexpr bool QT = MODE == kDq && NQ_PAD <= 128 && NV_PAD <= 128;
+  static constexpr uint32_t QA = 128, DOA = 128 + NQ_PAD / 2;
+  static_assert(!QT || (DOA + NV_PAD / 2 <= BUF), "TMEM columns of the A operands");
   static constexpr int HALF = IR / 2;      // columns per compute warpgroup
   static constexpr int CHUNKS = HALF / 32;  // 32-column chunks per compute thread
   static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * 2 * IR) <= 512, "TMEM columns");
@@ -208,6 +217,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     }
     for (int i = 0; i < 3; ++i) mbar_init(bar(C::B_DRAIN + i), 1);
     mbar_init(bar(C::B_PF), 256);
+    mbar_init(bar(C::B_QT), 256);
     for (int i = 0; i < NBS; ++i) { mbar_init(bar(C::B_BF + i), 1); mbar_init(bar(C::B_BE + i), 256); }
     *abort_flag = 0;
     mbar_init_fence();
@@ -388,7 +398,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss_w(s_cols(n), d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
+          if (C::QT) mma_ts_w(s_cols(n), tmem + C::QA + 8 * kk, d_i0 + (ia >> 4), id_sp, kk > 0);
+          else mma_ss_w(s_cols(n), d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
         }
       };
       auto issue_dp = [&](int n) {  // dP (dK/dV: dP^T) of item n
@@ -396,7 +407,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          mma_ss_w(dp_cols(n), d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
+          if (C::QT) mma_ts_w(dp_cols(n), tmem + C::DOA + 8 * kk, d_i1 + (ia >> 4), id_sp, kk > 0);
+          else mma_ss_w(dp_cols(n), d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
         }
       };
       // the 16-bit A operand of K step kk (16 inner rows) sits in the first half of the 32-column
@@ -426,7 +438,8 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       bool ok = true;
       if (role < 2) {
         // products of item m, once its inner tile has landed and its TMEM columns are free
-        ok = wait_all(C::B_OUT, 0);
+        // (QT: once the compute warps have copied the outer rows into TMEM)
+        ok = wait_all(C::QT ? C::B_QT : C::B_OUT, 0);
         for (int m = 0; m < n_items && ok; ++m) {
           const int b = m % NBUF;
           // S reads ring 0 (Q or K), dP reads ring 1 (dO or V)
@@ -512,7 +525,29 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       }
     }
     bool ok = true;
-    for (int n = 0; n < n_items; ++n) {
+    if (C::QT && n_items > 0) {
+      // this thread's row of the outer Q (first half of the compute warps) or dO tile (second
+      // half), 16 bytes at a time from its 128-byte-swizzled blocks, into the A-operand columns
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_OUT), 0, abort_flag, p.err));
+      if (ok) {
+        const uint32_t src = (half == 0 ? sO0 : sO1) + r * 128;
+        const uint32_t dst = lane_addr + (half == 0 ? C::QA : C::DOA);
+        const int nb = half == 0 ? C::KB0 : C::KB1;
+#pragma unroll 1
+        for (int c = 0; c < nb; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            lds_v4(src + c * C::OBLK + ((q ^ (r & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          __syncwarp();
+          tmem_st32(dst + 32 * c, v);
+        }
+        tmem_st_wait();
+      }
+      fence_before();
+      mbar_arrive(bar(C::B_QT));
+    }
+    for (int n = 0; n < n_items && ok; ++n) {
       const int b = n % NBUF, st = n % NSTAGE;
       const int h = item_head(n);
       bool w = mbar_wait(bar(C::B_S + b), (n / NBUF) & 1, abort_flag, p.err);

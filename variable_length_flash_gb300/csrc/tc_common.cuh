@@ -122,6 +122,10 @@ __device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint3
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
                : "memory");
 }
+__device__ __forceinline__ void lds_v4(uint32_t a, uint32_t &x, uint32_t &y, uint32_t &z, uint32_t &w) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x), "=r"(y), "=r"(z), "=r"(w) : "r"(a)
+               : "memory");
+}
 // named barrier over `count` threads (a multiple of 32) of the CTA
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
