@@ -109,7 +109,7 @@ struct BwdCfg {
   static constexpr int B_IE1 = B_IF1 + NSTAGE1, B_S = B_IE1 + NSTAGE1;
   static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + NBUF, B_DRAIN = B_D + NBUF;
   static constexpr int B_PF = B_DRAIN + 3;  // kDqS: the compute warps have loaded dP
-  static constexpr int B_QT = B_PF + 1;     // QT: the outer Q / dO rows are in TMEM
+  static constexpr int B_QT = B_PF + 1;     // QT: the outer Q / dO rows are in TMEM (kDq)
   static constexpr int B_BF = B_QT + 1, B_BE = B_BF + NBS;  // bias full / empty
   static constexpr int NBAR = B_BE + NBS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -122,14 +122,17 @@ struct BwdCfg {
                                   : (MODE == kDv ? NV_PAD : (MODE == kDk || MODE == kDqS ? NQ_PAD : 256));
   __host__ __device__ static constexpr uint32_t s_col(int b) { return MODE == kDqS ? BUF + IR * b : BUF + 2 * IR * b; }
   __host__ __device__ static constexpr uint32_t dp_col(int b) { return MODE == kDqS ? BUF + NBUF * IR : BUF + 2 * IR * b + IR; }
-  // QT (kDq, widths up to 128): the outer Q and dO tiles are copied once into the TMEM columns
-  // between the accumulator and the S / dP buffers, 16-bit pairs along the row, and are the A
-  // operands of S and dP from there: those products then read only their inner K / V tile from
-  // shared memory (with both operands in shared memory a 64-key product is bound by its reads).
-  // kDqS has no free columns for them.
-  static constexpr bool QT = MODE == kDq && NQ_PAD <= 128 && NV_PAD <= 128;
-  static constexpr uint32_t QA = 128, DOA = 128 + NQ_PAD / 2;
-  static_assert(!QT || (DOA + NV_PAD / 2 <= BUF), "TMEM columns of the A operands");
+  // kDq: the outer Q (QT_Q, widths up to 128) and dO (QT_DO) tiles are copied once into the
+  // TMEM columns between the accumulator and the S / dP buffers, 16-bit pairs along the row, and
+  // are the A operands of S and dP from there: those products then read only their inner K / V
+  // tile from shared memory (with both operands in shared memory a 64-key product is bound by
+  // its reads).  QK width 192: the 192-column accumulator leaves room for dO only.  kDqS has no
+  // free columns.
+  static constexpr bool QT_Q = MODE == kDq && NQ_PAD <= 128 && NV_PAD <= 128;
+  static constexpr uint32_t QA = 128, DOA = QT_Q ? 128 + NQ_PAD / 2 : NQ_PAD;
+  static constexpr bool QT_DO = MODE == kDq && NV_PAD <= 128 && DOA + NV_PAD / 2 <= BUF;
+  static constexpr bool QT = QT_Q || QT_DO;
+  static_assert(!QT_Q || QT_DO, "TMEM columns of the A operands");
   static constexpr int HALF = IR / 2;      // columns per compute warpgroup
   static constexpr int CHUNKS = HALF / 32;  // 32-column chunks per compute thread
   static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * 2 * IR) <= 512, "TMEM columns");
@@ -398,7 +401,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          if (C::QT) mma_ts_w(s_cols(n), tmem + C::QA + 8 * kk, d_i0 + (ia >> 4), id_sp, kk > 0);
+          if (C::QT_Q) mma_ts_w(s_cols(n), tmem + C::QA + 8 * kk, d_i0 + (ia >> 4), id_sp, kk > 0);
           else mma_ss_w(s_cols(n), d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
         }
       };
@@ -407,7 +410,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          if (C::QT) mma_ts_w(dp_cols(n), tmem + C::DOA + 8 * kk, d_i1 + (ia >> 4), id_sp, kk > 0);
+          if (C::QT_DO) mma_ts_w(dp_cols(n), tmem + C::DOA + 8 * kk, d_i1 + (ia >> 4), id_sp, kk > 0);
           else mma_ss_w(dp_cols(n), d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
         }
       };
@@ -529,7 +532,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // this thread's row of the outer Q (first half of the compute warps) or dO tile (second
       // half), 16 bytes at a time from its 128-byte-swizzled blocks, into the A-operand columns
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_OUT), 0, abort_flag, p.err));
-      if (ok) {
+      if (ok && (half == 0 ? C::QT_Q : C::QT_DO)) {
         const uint32_t src = (half == 0 ? sO0 : sO1) + r * 128;
         const uint32_t dst = lane_addr + (half == 0 ? C::QA : C::DOA);
         const int nb = half == 0 ? C::KB0 : C::KB1;
