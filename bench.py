@@ -1,26 +1,35 @@
 """Benchmark: varlen flash attention forward + backward on one GB300 (or N replicas).
 
 One step = one pass of the whole hot path over one batch: forward (out, lse) then backward
-(row-dot pre-pass, dK/dV, dQ), on the dense causal workload B=4 x L=4096, H=32, head_dim 128,
-bf16, packed as 4 cu_seqlens segments (inputs are synthetic, seeded, resident in HBM; each of
-q/k/v/out/dout is 134 MB, larger than the 129 MB L2, so no flush is needed between steps).
+(row-dot pre-pass, dK/dV, dQ).  The headline workload is the dense causal configuration B=4 x
+L=4096, H=32, head_dim 128, bf16, packed as 4 cu_seqlens segments (inputs synthetic, seeded,
+resident in HBM; each of q/k/v/out/dout is 134 MB, larger than the 129 MB L2, so no flush is
+needed between steps).
 
 Prints ONE JSON line (rank 0):
   value        fwd+bwd TFLOP/s over unmasked pairs (whole job, all ranks), CUDA-event timed
   fwd_tflops   forward-only TFLOP/s from the same timed region
   e2e          same metric through the C ABI with pinned host buffers, H2D/D2H inside the timing
-  roofline     dominant kernel: algorithmic FLOPs per launch / its average event-timed duration
+  roofline     dominant kernel: algorithmic FLOPs (or bytes) per launch / its mean event time
   cpu_baseline the fp64 oracle (test infrastructure) on a bounded sample, host cores
-  clocks       nvidia-smi samples taken during the timed region
+  clocks       nvidia-smi samples taken during the timed region (and the sustained run before it)
+  sustained    the same step repeated for >= 1 s right before the timed steps (clock evidence)
+  configs      the other benchmark configurations, each timed the same way on its own inputs:
+               the 436-token forward (latency per call), the ragged GQA + window batch, the
+               latent head, the 49,152-token sequence with a per-head and a head-broadcast bias,
+               and the widened rows (decode shapes, head widths 96 / 256, shared rope key)
 
-``--impl reference`` times the fp64 CPU oracle on the same workload instead (rank 0 only).
-Multi-GPU (torchrun): every rank runs its own replica of the workload (weak scaling; the
-ranks exchange nothing in the data path; a barrier and a max-reduce of the timing only).
+``--impl reference`` times the fp64 CPU oracle on the same workload instead (rank 0 only); that
+arm never loads the compiled library.  Multi-GPU (torchrun): every rank runs its own replica of
+the headline workload (weak scaling; the ranks exchange nothing in the data path; a barrier and
+a max-reduce of the timing only); the other configurations run at N = 1 only.
 """
 from __future__ import annotations
 
 import argparse
+import importlib.util
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -35,9 +44,35 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 import workloads as W  # noqa: E402
-from variable_length_flash_gb300 import flops as F  # noqa: E402
+
+
+def _load_flops():
+    """The pair / FLOP counting module, loaded by its path: importing the package would load the
+    compiled library, which the reference arm must not touch."""
+    path = os.path.join(ROOT, "variable_length_flash_gb300", "flops.py")
+    spec = importlib.util.spec_from_file_location("vlf_flops", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+F = _load_flops()
 
 WORKLOAD = "dense4x4096_bf16_causal"
+# (workload, timed steps, warm-up steps) of the other configurations in the line's "configs"
+CONFIGS = [
+    ("ragged64_gqa_window_bf16", 10, 3),
+    ("latent2x8192_bf16_causal", 10, 3),
+    ("long49152_fp16_bias_alibi", 3, 3),
+    ("long49152_fp16_bias_prefix", 3, 3),
+    ("latent2x8192_bf16_causal_shared_rope", 10, 3),
+    ("dense4x4096_bf16_causal_d96", 20, 5),
+    ("dense4x4096_bf16_causal_d256", 20, 5),
+    ("decode64x8192_bf16_gqa", 50, 5),
+    ("decode4x32768_bf16_gqa", 50, 5),
+]
+LATENCY_CONFIGS = ["varlen64_fp16_full", "varlen64_fp16_causal"]
+SUSTAIN_S = 1.2  # length of the sustained run before the timed steps
 
 
 # ------------------------------------------------------------------------------ helpers
@@ -88,20 +123,60 @@ def ncu_traffic(role: str, workload: str):
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
-    k = rec.get("kernels", {}).get(role)
-    if k is None or rec.get("workload") != workload:
-        return None
-    h = hashlib.sha256()
-    for f in k["source_files"]:
-        fp = os.path.join(ROOT, "variable_length_flash_gb300", "csrc", f)
-        if not os.path.exists(fp):
+    for entry in rec.get("captures", [rec]):
+        k = entry.get("kernels", {}).get(role)
+        if k is None or entry.get("workload") != workload:
+            continue
+        h = hashlib.sha256()
+        for f in k["source_files"]:
+            fp = os.path.join(ROOT, "variable_length_flash_gb300", "csrc", f)
+            if not os.path.exists(fp):
+                return None
+            h.update(open(fp, "rb").read())
+        if h.hexdigest() != k["source_sha256"]:
             return None
-        h.update(open(fp, "rb").read())
-    return k["dram_bytes_per_launch"] if h.hexdigest() == k["source_sha256"] else None
+        return k["dram_bytes_per_launch"] * k.get("scale_to_workload", 1.0)
+    return None
+
+
+def l2_bytes_of(dev=None) -> int:
+    if not torch.cuda.is_available():
+        return 0
+    return int(torch.cuda.get_device_properties(dev if dev is not None else 0).L2_cache_size)
+
+
+def input_bytes(w) -> int:
+    """Bytes of a step's inputs (q, k, v, dout, bias), from the workload's shape alone."""
+    eb = {"fp16": 2, "bf16": 2, "fp32": 4}[w.dtype]
+    if w.latent_split is not None and w.rope_heads is not None:
+        nope, rope = w.latent_split
+        qk = (w.total_q * w.h_q + w.total_kv * w.h_kv) * nope + (w.total_q * w.h_q + w.total_kv * w.rope_heads) * rope
+    else:
+        qk = (w.total_q * w.h_q + w.total_kv * w.h_kv) * w.d_qk
+    n = qk + w.total_kv * w.h_kv * w.d_v + (w.total_q * w.h_q * w.d_v if w.backward else 0)
+    bias = w.total_q * w.bias_heads * w.max_seqlen_kv * 4 if w.bias is not None else 0
+    return n * eb + bias
+
+
+def config_of(w, world: int, l2: int) -> dict:
+    """The line's ``config``: the workload and how it is timed (shared by both arms)."""
+    ib = input_bytes(w)
+    flush = ib < 2 * l2
+    return {"workload": w.name, "lengths": sorted(set(w.lengths_q)),
+            "lengths_kv": sorted(set(w.lengths_kv)), "num_seqs": w.num_seqs, "h_q": w.h_q,
+            "h_kv": w.h_kv, "d_qk": w.d_qk, "d_v": w.d_v, "causal": w.causal,
+            "window": w.window, "bias": w.bias, "unmasked_pairs": F.workload_pairs(w),
+            "step": "fwd+bwd" if w.backward else "fwd",
+            "parallelism": f"replicas x{world}",
+            "l2": (f"inputs {ib / 1e6:.1f} MB < 2 x L2: L2 flushed between timed steps (a "
+                   f"{2 * l2 / 1e6:.0f} MB write), per-step events" if flush else
+                   f"inputs {ib / 1e6:.0f} MB > 2 x L2 ({l2 / 1e6:.0f} MB): streamed from HBM, "
+                   "no flush")}
 
 
 class ClockSampler:
-    """nvidia-smi SM clock / throttle-reason samples every 200 ms while running."""
+    """nvidia-smi SM clock / throttle-reason samples every 100 ms while running, each stamped
+    with the host time it arrived; ``summary(t0, t1)`` keeps those taken between t0 and t1."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -113,7 +188,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -125,12 +200,12 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 8:
-                self.rows.append(parts)
+                self.rows.append((time.time(), parts))
 
     def stop(self):
         if self.proc is None:
-            return None
-        time.sleep(0.25)
+            return
+        time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -138,13 +213,37 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "", 1).isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "", 1).isdigit()]
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        rows = [r for t, r in self.rows if t0 <= t <= t1]
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [x for x in (num(r[0]) for r in rows) if x is not None]
+        mx = [x for x in (num(r[1]) for r in rows) if x is not None]
+        pw = [x for x in (num(r[2]) for r in rows) if x is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v == "Active"})
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.rows)}
+                "samples": len(rows), "power_w_max": max(pw) if pw else None,
+                "window_s": round(t1 - t0, 3)}
+
+
+def peak_for(clocks, peaks):
+    """The tensor roof for a kernel timed inside this run: the burst figure while the SM clock
+    held its maximum with no power cap, the sustained (power-capped) figure otherwise."""
+    if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz") and \
+            clocks["sm_mhz"] >= 0.97 * clocks["sm_max_mhz"] and "sw_power_cap" not in clocks["reasons"]:
+        return peaks["bf16_tflops"], "burst"
+    if clocks and clocks.get("sm_mhz"):
+        return peaks["bf16_tflops_sustained"], "sustained"
+    return peaks["bf16_tflops"], "burst (no clock samples)"
 
 
 # ------------------------------------------------------------------------------ CPU oracle
@@ -175,8 +274,8 @@ def oracle_sample(w, x_cpu, units: int):
     return time.perf_counter() - t0, pairs
 
 
-def cpu_inputs(w, units):
-    """Host copies of the sequences the CPU sample touches (drawn on the host generator)."""
+def cpu_inputs(w):
+    """Host copies of the workload's inputs (drawn on the host generator)."""
     return W.make_inputs(w, seed=0, device="cpu")
 
 
@@ -186,7 +285,7 @@ def run_reference(args, rank, world):
     w = W.workload(args.workload)
     fpp = F.flops_per_pair(w.d_qk, w.d_v)["fwd_bwd" if w.backward else "fwd"]
     what = "fwd+bwd" if w.backward else "fwd"
-    x = cpu_inputs(w, 1)
+    x = cpu_inputs(w)
     for _ in range(args.warmup):
         oracle_sample(w, x, 1)
     times, pairs = [], 0
@@ -203,7 +302,7 @@ def run_reference(args, rank, world):
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name},
+            "data": "synthetic (seeded N(0,1))", "config": config_of(w, world, l2_bytes_of()),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -212,6 +311,320 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------------------ GPU arm
+class Problem:
+    """One workload's device inputs, results and the calls of one step through the library."""
+
+    def __init__(self, vlf, w, dev, seed):
+        self.vlf, self.w, self.dev = vlf, w, dev
+        x = W.make_inputs(w, seed=seed, device=dev, with_dout=True)
+        self.latent_api = w.latent_split is not None and w.rope_heads is not None
+        self.in_names = (("q_nope", "q_rope", "k_nope", "k_rope", "v") if self.latent_api
+                         else ("q", "k", "v"))
+        self.grad_of = dict(zip(("dq_nope", "dq_rope", "dk_nope", "dk_rope", "dv") if self.latent_api
+                                else ("dq", "dk", "dv"), self.in_names))
+        if self.latent_api:
+            del x["q"], x["k"]  # the concatenated operands are not used
+        self.x = x
+        dt = x["v"].dtype
+        self.dt = dt
+        out = torch.empty((w.total_q, w.h_q, w.d_v), dtype=dt, device=dev)
+        lse = torch.empty((w.h_q, w.total_q), dtype=torch.float32, device=dev)
+        self.res = {"out": out, "lse": lse}
+        if w.backward:
+            self.res.update({g: torch.empty_like(x[n]) for g, n in self.grad_of.items()})
+        ws_bytes = (vlf.vlf_attn_varlen_bwd_latent_workspace_size(
+            w.total_q, w.total_kv, w.h_q, w.h_kv, w.rope_heads, dt) if self.latent_api else
+            vlf.vlf_attn_varlen_bwd_workspace_size(w.total_q, w.total_kv, w.h_q, w.h_kv, w.d_qk,
+                                                   w.d_v, dt))
+        self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.kw = dict(scale=w.scale, causal=w.causal, window=w.window, bias=x["bias"])
+        # small-batch / decode shapes split each CTA's KV band (the library's choice); the parts'
+        # workspace is allocated once, outside the timed region
+        self.n_split = vlf.vlf_fwd_num_splits(w.num_seqs, w.max_seqlen_q, w.max_seqlen_kv, w.h_q,
+                                              w.h_kv, w.d_qk, w.d_v, dt)
+        self.fws = [torch.empty(max(1, vlf.vlf_attn_varlen_fwd_split_workspace_size(
+            w.total_q, w.h_q, w.d_v, self.n_split)), dtype=torch.uint8, device=dev)
+            for _ in range(2)]
+
+    def run(self, d=None, r=None, fw=None, st=None, ev=None, stream=None):
+        """One step on inputs d into results r (the problem's own when None) on stream st (the
+        current one when None); ev: per-stage timing events recorded on ``stream``."""
+        vlf, w = self.vlf, self.w
+        d = self.x if d is None else d
+        r = self.res if r is None else r
+        fw = self.fws[0] if fw is None else fw
+        ops = [d[n] for n in self.in_names]
+        cu = (d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv)
+        kw = dict(self.kw, bias=d["bias"] if "bias" in d else self.kw["bias"])
+        if self.latent_api:
+            vlf.vlf_attn_varlen_fwd_latent(*ops, *cu, out=r["out"], lse=r["lse"], stream=st, **kw)
+        else:
+            vlf.vlf_attn_varlen_fwd(*ops, *cu, out=r["out"], lse=r["lse"], stream=st,
+                                    workspace=fw, num_splits=self.n_split, **kw)
+        if not w.backward:
+            if ev is not None:
+                ev[1].record(stream)
+            return
+        sev = None if ev is None else ev[1:]
+        if self.latent_api:
+            vlf.vlf_attn_varlen_bwd_latent(d["dout"], *ops, r["out"], r["lse"], *cu,
+                                           grads=tuple(r[g] for g in self.grad_of),
+                                           workspace=self.ws, stream=st, stage_events=sev, **kw)
+        else:
+            vlf.vlf_attn_varlen_bwd(d["dout"], *ops, r["out"], r["lse"], *cu, dq=r["dq"],
+                                    dk=r["dk"], dv=r["dv"], workspace=self.ws, stream=st,
+                                    stage_events=sev, **kw)
+
+    def algorithmic(self):
+        """Per-kernel algorithmic FLOPs and bytes (the minimum each kernel moves: its tensors
+        read and written once, plus the bias once per pass)."""
+        w, x = self.w, self.x
+        pairs = F.workload_pairs(w)
+        fpp = F.flops_per_pair(w.d_qk, w.d_v)
+        eb = x["v"].element_size()
+        nq, nk = w.total_q * w.h_q, w.total_kv * w.h_kv
+        q_b, k_b, v_b = nq * w.d_qk * eb, nk * w.d_qk * eb, nk * w.d_v * eb
+        if self.latent_api:  # K as read: the nope parts and the (possibly shared) rope key
+            k_b = (x["k_nope"].numel() + x["k_rope"].numel()) * eb
+        o_b, row_b = nq * w.d_v * eb, 4 * nq                    # O (or dO), one fp32 per row
+        bias_b = 0 if x["bias"] is None else x["bias"].numel() * 4
+        flops = {"fwd": pairs * fpp["fwd"], "dkdv": pairs * fpp["dkdv"], "dq": pairs * fpp["dq"]}
+        bytes_ = {"fwd": q_b + k_b + v_b + o_b + row_b + bias_b,
+                  "rowdot": 2 * o_b + row_b,
+                  "dkdv": q_b + k_b + v_b + o_b + 2 * row_b + k_b + v_b + bias_b,
+                  "dq": q_b + k_b + v_b + o_b + 2 * row_b + q_b + bias_b}
+        return flops, bytes_
+
+
+def roofline(prob, stage_ms, peaks, tensor_peak, dev):
+    """The dominant stage's roofline: achieved algorithmic FLOP/s (or bytes/s) of its mean
+    event-timed launch against the roof it is closer to."""
+    vlf, w = prob.vlf, prob.w
+    fwd_path = vlf.vlf_fwd_path(w.h_q, w.h_kv, w.d_qk, w.d_v, prob.dt)
+    bwd_path = vlf.vlf_bwd_path(w.h_q, w.h_kv, w.d_qk, w.d_v, prob.dt)
+    dom = max(stage_ms, key=stage_ms.get)
+    flops_of, bytes_of = prob.algorithmic()
+    tc = (fwd_path if dom == "fwd" else bwd_path) == 1
+    sec = stage_ms[dom] * 1e-3
+    hbm_frac = bytes_of[dom] / sec / 1e9 / peaks["hbm_gbs"]
+    ten_frac = flops_of.get(dom, 0) / sec / 1e12 / tensor_peak
+    if dom == "rowdot" or (tc and hbm_frac > ten_frac):
+        roof = {"bound": "hbm", "achieved": bytes_of[dom] / sec / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "algorithmic_bytes": bytes_of[dom]}
+    elif tc:
+        roof = {"bound": "tensor", "achieved": flops_of[dom] / sec / 1e12, "peak": tensor_peak,
+                "unit": "TFLOP/s", "algorithmic_flops": flops_of[dom]}
+    else:
+        props = torch.cuda.get_device_properties(dev)
+        alu_peak = props.multi_processor_count * 128 * 2 * 2070.0 * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": flops_of[dom] / sec / 1e12, "peak": alu_peak,
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    tr = ncu_traffic(dom, w.name) if tc or roof["bound"] == "hbm" else None
+    roof["traffic"] = tr
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz)"
+                                             if roof["bound"] == "alu" else "")
+    return roof, {"fwd": "tcgen05" if fwd_path == 1 else "simt",
+                  "bwd": "tcgen05" if bwd_path == 1 else "simt"}
+
+
+def time_steps(prob, steps, stream, dev, world, flush_l2):
+    """Time exactly ``steps`` steps (barrier + synchronize on both sides).  Returns the step
+    time in ms (max over ranks), the per-stage mean times and the library launches counted."""
+    vlf = prob.vlf
+    n_ev = 2 if not prob.w.backward else 2 + vlf.VLF_BWD_STAGES
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    for row in evs:  # torch creates the CUDA event at its first record()
+        for e in row:
+            e.record(stream)
+    flush_buf = torch.empty(2 * l2_bytes_of(dev), dtype=torch.uint8, device=dev) if flush_l2 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = vlf.vlf_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        if flush_l2:
+            flush_buf.zero_()  # (outside the step's own events)
+        evs[i][0].record(stream)
+        prob.run(ev=evs[i], stream=stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = vlf.vlf_launch_count() - n0
+    barrier(world)
+    st = vlf.vlf_check_error()
+    assert st == 0, vlf.vlf_status_string(st)
+    if flush_l2:
+        ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[-1]) for e in evs), world)
+    else:
+        ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / steps
+    names = ["fwd"] + ([] if not prob.w.backward else list(vlf.BWD_STAGE_NAMES))
+    stage_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, n in enumerate(names)}
+    return ms_step, stage_ms, launches
+
+
+def measure(vlf, w, dev, world, steps, warmup, sampler, peaks, tensor_peak=None, seed=0,
+            sustain_s=0.0):
+    """Times ``steps`` steps of workload ``w`` after ``warmup`` (and, with sustain_s > 0, a
+    sustained run of that many seconds right before the timed steps).  Returns the result
+    record and the Problem (kept alive by the caller while it needs the buffers)."""
+    stream = torch.cuda.current_stream()
+    prob = Problem(vlf, w, dev, seed)
+    for _ in range(warmup):
+        prob.run()
+    torch.cuda.synchronize()
+    st = vlf.vlf_check_error()
+    assert st == 0, vlf.vlf_status_string(st)
+    flush = input_bytes(w) < 2 * l2_bytes_of(dev)
+    t0 = time.time()
+    sustained = None
+    if sustain_s > 0:
+        # the same step back to back for >= sustain_s seconds: the clocks it runs at are those
+        # of a GPU under this load (the samples cover it and the timed steps after it)
+        ms_guess, _, _ = time_steps(prob, 3, stream, dev, world, flush)
+        n = max(3, int(math.ceil(sustain_s * 1e3 / ms_guess)))
+        ms_s, _, _ = time_steps(prob, n, stream, dev, world, flush)
+        sustained = {"steps": n, "ms_per_step": ms_s, "seconds": n * ms_s / 1e3}
+    ms_step, stage_ms, launches = time_steps(prob, steps, stream, dev, world, flush)
+    t1 = time.time()
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if tensor_peak is None:
+        tensor_peak, kind = peak_for(clocks, peaks)
+    else:
+        kind = "as the headline"
+    pairs = F.workload_pairs(w)
+    fpp = F.flops_per_pair(w.d_qk, w.d_v)
+    step_flops = fpp["fwd_bwd"] if w.backward else fpp["fwd"]
+    value = world * pairs * step_flops / (ms_step * 1e-3) / 1e12
+    fwd_tflops = pairs * fpp["fwd"] / (stage_ms["fwd"] * 1e-3) / 1e12
+    roof, paths = roofline(prob, stage_ms, peaks, tensor_peak, dev)
+    rec = {"workload": w.name, "step": "fwd+bwd" if w.backward else "fwd",
+           "value": value, "unit": "TFLOP/s", "steps": steps, "warmup": warmup,
+           "ms_per_step": ms_step, "fwd_tflops": fwd_tflops,
+           "fwd_frac_of_peak": fwd_tflops / tensor_peak,
+           "value_frac_of_peak": value / world / tensor_peak,
+           "tensor_peak": tensor_peak, "tensor_peak_kind": kind,
+           "stage_ms": stage_ms, "roofline": roof, "paths": paths, "kv_splits": prob.n_split,
+           "clocks": clocks, "gpu_launches": launches,
+           "l2": config_of(w, world, l2_bytes_of(dev))["l2"]}
+    if sustained is not None:
+        sustained["value"] = world * pairs * step_flops / (sustained["ms_per_step"] * 1e-3) / 1e12
+        rec["sustained"] = sustained
+    return rec, prob
+
+
+def latency(vlf, w, dev, calls=300, warmup=30):
+    """Per-call latency of a tiny forward through the Python binding and the C ABI.
+    device_us: event-timed call on an L2-flushed device (the flush keeps the GPU busy while
+    the host enqueues the call, so only device time is seen); host_us: host time of the call
+    (argument marshalling, the C ABI's checks and the launch, returning before the kernel
+    ends); us_per_call: back-to-back calls, wall clock (host and device overlap)."""
+    stream = torch.cuda.current_stream()
+    prob = Problem(vlf, w, dev, seed=0)
+    for _ in range(warmup):
+        prob.run()
+    torch.cuda.synchronize()
+    # back-to-back calls, inputs L2-resident
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        prob.run()
+    t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    t2 = time.perf_counter()
+    host_us = (t1 - t0) / calls * 1e6
+    per_call = (t2 - t0) / calls * 1e6
+    # device time per call, L2 flushed before each
+    flush_buf = torch.empty(2 * l2_bytes_of(dev), dtype=torch.uint8, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(calls)]
+    n0 = vlf.vlf_launch_count()
+    for a, b in ev:
+        flush_buf.zero_()
+        a.record(stream)
+        prob.run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    launches = (vlf.vlf_launch_count() - n0) / calls
+    st = vlf.vlf_check_error()
+    assert st == 0, vlf.vlf_status_string(st)
+    dev_us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    pairs = F.workload_pairs(w)
+    fl = pairs * F.flops_per_pair(w.d_qk, w.d_v)["fwd"]
+    return {"workload": w.name, "step": "fwd", "us_per_call": per_call, "host_us": host_us,
+            "device_us": dev_us, "launches_per_call": launches,
+            "value": fl / (per_call * 1e-6) / 1e12, "device_tflops": fl / (dev_us * 1e-6) / 1e12,
+            "unit": "TFLOP/s", "calls": calls, "warmup": warmup, "unmasked_pairs": pairs,
+            "l2": "us_per_call / host_us: back-to-back calls, inputs L2-resident (0.9 MB); "
+                  "device_us: L2 flushed before each call",
+            "status": "latency-bound: far below the 60% forward target (a few microseconds of "
+                      "work per call)"}
+
+
+def e2e_measure(prob, steps, warmup, world, pairs, step_flops):
+    """End to end through the public API with pinned host buffers: every step uploads its
+    inputs and reads back all of its results (out, lse, dq, dk, dv) inside the timed region.
+    Two device / host buffer sets and three streams pipeline the steps the way an input
+    pipeline would: step k+1's upload and step k-1's read-back run on the copy engines while
+    step k's kernels run.  (A bias, where a workload has one, stays resident like a weight.)"""
+    x, w = prob.x, prob.w
+    in_keys = prob.in_names + ("cu_seqlens_q", "cu_seqlens_kv") + (("dout",) if w.backward else ())
+    res_like = prob.res
+    host = {k: x[k].cpu().pin_memory() for k in in_keys}
+    dset = [{k: torch.empty_like(x[k]) for k in in_keys} for _ in range(2)]
+    rset = [{k: torch.empty_like(t) for k, t in res_like.items()} for _ in range(2)]
+    hres = [{k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+             for k, t in res_like.items()} for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in hres[0].values())
+    s_up, s_cmp, s_dn = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_dn = [torch.cuda.Event() for _ in range(2)]
+    cur = torch.cuda.current_stream()
+    for e in ev_cmp + ev_dn:
+        e.record(cur)  # both sets start free
+    torch.cuda.synchronize()
+
+    def e2e_step(step):
+        i = step % 2
+        d, r, h = dset[i], rset[i], hres[i]
+        with torch.cuda.stream(s_up):
+            s_up.wait_event(ev_cmp[i])  # the kernels of step - 2 are done with set i
+            for k in in_keys:
+                d[k].copy_(host[k], non_blocking=True)
+            ev_up[i].record(s_up)
+        s_cmp.wait_event(ev_up[i])
+        s_cmp.wait_event(ev_dn[i])  # the read-back of step - 2 is done with set i
+        prob.run(d=d, r=r, fw=prob.fws[i], st=s_cmp)
+        ev_cmp[i].record(s_cmp)
+        with torch.cuda.stream(s_dn):
+            s_dn.wait_event(ev_cmp[i])
+            for k in res_like:
+                h[k].copy_(r[k], non_blocking=True)
+            ev_dn[i].record(s_dn)
+
+    for it in range(warmup):
+        e2e_step(it)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_up)
+    for it in range(steps):
+        e2e_step(it)
+    b.record(s_dn)  # after the last read-back, which follows every other stream's work
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world) / steps
+    return {"value": world * pairs * step_flops / (e2e_ms * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": e2e_ms, "pipelined": "upload / kernels / read-back of consecutive "
+                                                "steps overlap (3 streams, 2 buffer sets)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -220,6 +633,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="headline workload only (skip the other configurations)")
+    ap.add_argument("--configs", default=None,
+                    help="comma-separated subset of the other configurations to time")
     ap.add_argument("--cpu-units", type=int, default=20,
                     help="(sequence, head) units of the workload for the CPU oracle baseline")
     args = ap.parse_args()
@@ -232,259 +649,62 @@ def main():
     import variable_length_flash_gb300 as vlf
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
     w = W.workload(args.workload)
-    x = W.make_inputs(w, seed=rank, device=dev, with_dout=True)
-    fpp = F.flops_per_pair(w.d_qk, w.d_v)
-    pairs = F.workload_pairs(w)
-    dt = x["q"].dtype
-    # a latent workload with a given rope_heads goes through the split-operand calls (its
-    # operands as produced, the rope key possibly shared); the others through the plain calls
-    latent_api = w.latent_split is not None and w.rope_heads is not None
-    in_names = ("q_nope", "q_rope", "k_nope", "k_rope", "v") if latent_api else ("q", "k", "v")
-    grad_of = dict(zip(("dq_nope", "dq_rope", "dk_nope", "dk_rope", "dv") if latent_api
-                       else ("dq", "dk", "dv"), in_names))
-    if latent_api:
-        del x["q"], x["k"]  # the concatenated operands are not used
-    out = torch.empty((w.total_q, w.h_q, w.d_v), dtype=dt, device=dev)
-    lse = torch.empty((w.h_q, w.total_q), dtype=torch.float32, device=dev)
-    res0 = {"out": out, "lse": lse, **{g: torch.empty_like(x[n]) for g, n in grad_of.items()}}
-    ws_bytes = (vlf.vlf_attn_varlen_bwd_latent_workspace_size(
-        w.total_q, w.total_kv, w.h_q, w.h_kv, w.rope_heads, dt) if latent_api else
-        vlf.vlf_attn_varlen_bwd_workspace_size(w.total_q, w.total_kv, w.h_q, w.h_kv, w.d_qk,
-                                               w.d_v, dt))
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    kw = dict(scale=w.scale, causal=w.causal, window=w.window, bias=x["bias"])
-    # small-batch / decode shapes split each CTA's KV band (the library's choice); the parts'
-    # workspace is allocated once, outside the timed region
-    n_split = vlf.vlf_fwd_num_splits(w.num_seqs, w.max_seqlen_q, w.max_seqlen_kv, w.h_q, w.h_kv,
-                                     w.d_qk, w.d_v, dt)
-    fws = [torch.empty(max(1, vlf.vlf_attn_varlen_fwd_split_workspace_size(
-        w.total_q, w.h_q, w.d_v, n_split)), dtype=torch.uint8, device=dev) for _ in range(2)]
-    fkw = dict(num_splits=n_split)
-
-    # a step is the forward and the backward; workloads without a backward (decode-sized,
-    # latency-bound) time the forward alone
-    fwd_only = not w.backward
-
-    def run(d, r, fw, st=None, ev=None):
-        """One step on inputs d into results r through the library's calls (on stream st, the
-        current one when None); ev: per-stage timing events."""
-        ops = [d[n] for n in in_names]
-        cu = (d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv)
-        if latent_api:
-            vlf.vlf_attn_varlen_fwd_latent(*ops, *cu, out=r["out"], lse=r["lse"], stream=st, **kw)
-        else:
-            vlf.vlf_attn_varlen_fwd(*ops, *cu, out=r["out"], lse=r["lse"], stream=st,
-                                    workspace=fw, **fkw, **kw)
-        if fwd_only:
-            if ev is not None:
-                ev[1].record(stream)
-            return
-        sev = None if ev is None else ev[1:]
-        if latent_api:
-            vlf.vlf_attn_varlen_bwd_latent(d["dout"], *ops, r["out"], r["lse"], *cu,
-                                           grads=tuple(r[g] for g in grad_of), workspace=ws,
-                                           stream=st, stage_events=sev, **kw)
-        else:
-            vlf.vlf_attn_varlen_bwd(d["dout"], *ops, r["out"], r["lse"], *cu, dq=r["dq"],
-                                    dk=r["dk"], dv=r["dv"], workspace=ws, stream=st,
-                                    stage_events=sev, **kw)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        run(x, res0, fws[0], ev=ev)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st = vlf.vlf_check_error()
-    assert st == 0, vlf.vlf_status_string(st)
-
-    # events: per step [fwd start, bwd start(=fwd end), after rowdot, after dkdv, after dq]
-    n_ev = 2 if fwd_only else 2 + vlf.VLF_BWD_STAGES
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    for row in evs:  # torch creates the CUDA event at its first record()
-        for e in row:
-            e.record(stream)
+    peaks = load_peaks()
     sampler = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
-    n0 = vlf.vlf_launch_count()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    # Inputs larger than L2 stream from HBM every step; smaller ones would stay in L2, so between
-    # their timed steps a buffer twice the L2 size is overwritten (outside each step's events)
-    # and the step time is the mean of the per-step event times.
-    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    in_bytes = sum(t.numel() * t.element_size() for t in [x[n] for n in in_names] +
-                   [x["dout"], x["bias"]] if t is not None)
-    flush = in_bytes < 2 * l2_bytes
-    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
-    t_start.record(stream)
-    for i in range(args.steps):
-        if flush:
-            flush_buf.zero_()
-        step(evs[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    launches = vlf.vlf_launch_count() - n0
-    barrier(world)
-    clocks = sampler.stop()
-    st = vlf.vlf_check_error()
-    assert st == 0, vlf.vlf_status_string(st)
-    if flush:
-        ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[-1]) for e in evs), world)
-    else:
-        ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / args.steps
-    stage_names = ["fwd"] + ([] if fwd_only else list(vlf.BWD_STAGE_NAMES))
-    stage_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
-                for i, n in enumerate(stage_names)}
-    fwd_ms = stage_ms["fwd"]
-    step_flops = fpp["fwd"] if fwd_only else fpp["fwd_bwd"]
-    value = world * pairs * step_flops / (ms_step * 1e-3) / 1e12
-    fwd_tflops = pairs * fpp["fwd"] / (fwd_ms * 1e-3) / 1e12
 
-    # roofline of the dominant kernel (one launch per stage per step)
-    peaks = load_peaks()
-    fwd_path = vlf.vlf_fwd_path(w.h_q, w.h_kv, w.d_qk, w.d_v, dt)
-    bwd_path = vlf.vlf_bwd_path(w.h_q, w.h_kv, w.d_qk, w.d_v, dt)
-    dom = max(stage_ms, key=stage_ms.get)
-    flops_of = {"fwd": pairs * fpp["fwd"], "dkdv": pairs * fpp["dkdv"], "dq": pairs * fpp["dq"]}
-    tc = (fwd_path if dom == "fwd" else bwd_path) == 1
-    # Algorithmic bytes per kernel launch (the minimum it moves): its tensors read and written
-    # once, plus the bias once per pass where there is one.
-    eb = x["v"].element_size()
-    nq, nk = w.total_q * w.h_q, w.total_kv * w.h_kv
-    q_b, k_b, v_b = nq * w.d_qk * eb, nk * w.d_qk * eb, nk * w.d_v * eb
-    if latent_api:  # K as read: the nope parts and the (possibly shared) rope key
-        k_b = (x["k_nope"].numel() + x["k_rope"].numel()) * eb
-    o_b, row_b = nq * w.d_v * eb, 4 * nq                    # O (or dO), one fp32 per row
-    bias_b = 0 if x["bias"] is None else x["bias"].numel() * 4
-    bytes_of = {"fwd": q_b + k_b + v_b + o_b + row_b + bias_b,
-                "rowdot": 2 * o_b + row_b,
-                "dkdv": q_b + k_b + v_b + o_b + 2 * row_b + k_b + v_b + bias_b,
-                "dq": q_b + k_b + v_b + o_b + 2 * row_b + q_b + bias_b}
-    # the bound is the roof the kernel is closer to: HBM for the row-dot, decode-sized forwards
-    # and bias streaming, the tensor cores for the rest
-    hbm_frac = bytes_of[dom] / (stage_ms[dom] * 1e-3) / 1e9 / peaks["hbm_gbs"]
-    ten_frac = flops_of.get(dom, 0) / (stage_ms[dom] * 1e-3) / 1e12 / peaks["bf16_tflops"]
-    if dom == "rowdot" or (tc and hbm_frac > ten_frac):
-        achieved = bytes_of[dom] / (stage_ms[dom] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "algorithmic_bytes": bytes_of[dom]}
-    elif tc:
-        achieved = flops_of[dom] / (stage_ms[dom] * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
-    else:
-        props = torch.cuda.get_device_properties(dev)
-        sm_max = (clocks or {}).get("sm_max_mhz") or 2070.0
-        alu_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12
-        achieved = flops_of[dom] / (stage_ms[dom] * 1e-3) / 1e12
-        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(dom, w.name) if tc or roof["bound"] == "hbm" else None
-    roof["kernel"] = dom
-    roof["peak_source"] = peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x max SM clock)"
-                                             if roof["bound"] == "alu" else "")
+    head, prob = measure(vlf, w, dev, world, args.steps, args.warmup, sampler, peaks,
+                         sustain_s=SUSTAIN_S)
+    pairs = F.workload_pairs(w)
+    fpp = F.flops_per_pair(w.d_qk, w.d_v)
+    step_flops = fpp["fwd_bwd"] if w.backward else fpp["fwd"]
+    e2e = None if args.no_e2e else e2e_measure(prob, args.steps, args.warmup, world, pairs,
+                                               step_flops)
+    del prob
+    torch.cuda.empty_cache()
 
-    # end to end through the C ABI with pinned host buffers
-    e2e = None
-    if not args.no_e2e:
-        # End to end through the public API with pinned host buffers: every step uploads its
-        # inputs and reads back all of its results (out, lse, dq, dk, dv) inside the timed
-        # region.  Two device / host buffer sets and three streams pipeline the steps the way an
-        # input pipeline would: step k+1's upload and step k-1's read-back run on the copy
-        # engines while step k's kernels run.  (The bias, where a workload has one, stays
-        # resident like a weight.)
-        in_keys = in_names + ("cu_seqlens_q", "cu_seqlens_kv") + (() if fwd_only else ("dout",))
-        res_like = {"out": out, "lse": lse} if fwd_only else res0
-        host = {k: x[k].cpu().pin_memory() for k in in_keys}
-        dset = [{k: torch.empty_like(x[k]) for k in in_keys} for _ in range(2)]
-        rset = [{k: torch.empty_like(t) for k, t in res_like.items()} for _ in range(2)]
-        hres = [{k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                 for k, t in res_like.items()} for _ in range(2)]
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = sum(t.numel() * t.element_size() for t in hres[0].values())
-        s_up, s_cmp, s_dn = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        ev_up = [torch.cuda.Event() for _ in range(2)]
-        ev_cmp = [torch.cuda.Event() for _ in range(2)]
-        ev_dn = [torch.cuda.Event() for _ in range(2)]
-        for e in ev_cmp + ev_dn:
-            e.record(stream)  # both sets start free
-        torch.cuda.synchronize()
-
-        def e2e_step(step):
-            i = step % 2
-            d, r, h = dset[i], rset[i], hres[i]
-            with torch.cuda.stream(s_up):
-                s_up.wait_event(ev_cmp[i])  # the kernels of step - 2 are done with set i
-                for k in in_keys:
-                    d[k].copy_(host[k], non_blocking=True)
-                ev_up[i].record(s_up)
-            s_cmp.wait_event(ev_up[i])
-            s_cmp.wait_event(ev_dn[i])  # the read-back of step - 2 is done with set i
-            run(d, r, fws[i], st=s_cmp)
-            ev_cmp[i].record(s_cmp)
-            with torch.cuda.stream(s_dn):
-                s_dn.wait_event(ev_cmp[i])
-                for k in res_like:
-                    h[k].copy_(r[k], non_blocking=True)
-                ev_dn[i].record(s_dn)
-
-        for it in range(args.warmup):
-            e2e_step(it)
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s_up)
-        for it in range(args.steps):
-            e2e_step(it)
-        b.record(s_dn)  # after the last read-back, which follows every other stream's work
-        torch.cuda.synchronize()
-        barrier(world)
-        e2e_ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
-        e2e = {"value": world * pairs * step_flops / (e2e_ms * 1e-3) / 1e12,
-               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms, "pipelined": "upload / kernels / read-back of consecutive "
-                                                   "steps overlap (3 streams, 2 buffer sets)"}
+    configs = {}
+    if world == 1 and not args.no_configs:
+        names = [c[0] for c in CONFIGS] + LATENCY_CONFIGS
+        want = set(args.configs.split(",")) if args.configs else set(names)
+        for name in LATENCY_CONFIGS:
+            if name in want and name != w.name:
+                configs[name] = latency(vlf, W.workload(name), dev)
+        for name, steps, warm in CONFIGS:
+            if name not in want or name == w.name:
+                continue
+            rec, p = measure(vlf, W.workload(name), dev, world, steps, warm, sampler, peaks,
+                             tensor_peak=head["tensor_peak"])
+            del p
+            torch.cuda.empty_cache()
+            configs[name] = rec
+    sampler.stop()
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_units > 0:
-        xc = cpu_inputs(w, args.cpu_units)
+        xc = cpu_inputs(w)
         secs, p = oracle_sample(w, xc, args.cpu_units)
         cpu = {"value": p * step_flops / secs / 1e12, "unit": "TFLOP/s",
                "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{args.cpu_units} (sequence, head) units of {w.name}, "
-                         f"{'fwd' if fwd_only else 'fwd+bwd'}, fp64 numpy, {secs:.1f} s"}
+                         f"{'fwd' if not w.backward else 'fwd+bwd'}, fp64 numpy, {secs:.1f} s"}
 
     if rank == 0:
         line = {
-            "metric": "attention TFLOP/s " + ("fwd" if fwd_only else "fwd+bwd") + " (unmasked pairs)",
-            "value": value,
-            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1))",
-            "config": {"workload": w.name, "lengths": sorted(set(w.lengths_q)),
-                       "num_seqs": w.num_seqs, "h_q": w.h_q, "h_kv": w.h_kv, "d_qk": w.d_qk,
-                       "d_v": w.d_v, "causal": w.causal, "window": w.window,
-                       "unmasked_pairs": pairs, "parallelism": f"replicas x{world}",
-                       "l2": (f"inputs {in_bytes / 1e6:.1f} MB < 2 x L2: L2 flushed between "
-                              f"timed steps (a {2 * l2_bytes / 1e6:.0f} MB write), per-step events"
-                              if flush else f"inputs {in_bytes / 1e6:.0f} MB > 2 x L2 "
-                              f"({l2_bytes / 1e6:.0f} MB): streamed from HBM, no flush"),
-                       "fwd_path": "tcgen05" if fwd_path == 1 else "simt",
-                       "kv_splits": n_split,
-                       "bwd_path": "tcgen05" if bwd_path == 1 else "simt"},
-            "fwd_tflops": fwd_tflops, "fwd_frac_of_peak": fwd_tflops / peaks["bf16_tflops"],
-            "fwd_bwd_frac_of_peak": value / world / peaks["bf16_tflops"],
-            "stage_ms": stage_ms, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clocks, "gpu_launches": launches,
+            "metric": "attention TFLOP/s " + ("fwd+bwd" if w.backward else "fwd") + " (unmasked pairs)",
+            "value": head["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded N(0,1))", "config": config_of(w, world, l2_bytes_of(dev)),
+            "paths": dict(head["paths"], kv_splits=head["kv_splits"]),
+            "fwd_tflops": head["fwd_tflops"], "fwd_frac_of_peak": head["fwd_frac_of_peak"],
+            "fwd_bwd_frac_of_peak": head["value_frac_of_peak"],
+            "tensor_peak": head["tensor_peak"], "tensor_peak_kind": head["tensor_peak_kind"],
+            "stage_ms": head["stage_ms"], "roofline": head["roofline"], "cpu_baseline": cpu,
+            "e2e": e2e, "clocks": head["clocks"], "sustained": head.get("sustained"),
+            "gpu_launches": head["gpu_launches"], "configs": configs,
         }
         print(json.dumps(line))
     if world > 1:

@@ -314,7 +314,9 @@ int vlf_sched_q_band(int j0, int j1, int q_len, int kv_len, int causal, int wind
  *     needs to start at zero).  Calls whose work overlaps on the GPU race on it: order them on
  *     one stream, or with events.
  *   - The first call on each device looks up the array's device address; make that first call
- *     before any stream capture begins.
+ *     before any stream capture begins.  The address is kept for the life of the process and is
+ *     not valid after a cudaDeviceReset of that device: do not call this entry point on a
+ *     device after resetting it.
  *   - No cudaMalloc, cudaFree or other allocating routine is called.
  */
 int vlf_attn_varlen_bwd_noalloc(const void *q, const void *k, const void *v, const void *out,

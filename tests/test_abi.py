@@ -101,3 +101,17 @@ def test_scheduler_rejects_bad_ranges():
         vlf.vlf_sched_kv_band(5, 5, 10, 10, True, 0)
     with pytest.raises(vlf.VlfError):
         vlf.vlf_sched_q_band(0, 11, 10, 10, True, 0)
+
+
+def test_noalloc_array_holds_a_problem_at_its_limit():
+    """A backward whose row-dot workspace is exactly the no-allocation entry point's array is
+    within its limit (h_q * total_q = 8,388,608 fp32 values); one more row is beyond it."""
+    limit_floats = vlf.vlf_noalloc_scratch_bytes() // 4
+    assert limit_floats == 8 << 20
+    for dtype in (vlf.VLF_F16, vlf.VLF_BF16, vlf.VLF_F32):
+        at = vlf.vlf_attn_varlen_bwd_workspace_size(limit_floats // 8, limit_floats // 8, 8, 8,
+                                                    128, 128, dtype)
+        assert at == vlf.vlf_noalloc_scratch_bytes(), dtype
+        past = vlf.vlf_attn_varlen_bwd_workspace_size(limit_floats // 8 + 1, 1, 8, 8, 128, 128,
+                                                      dtype)
+        assert past > vlf.vlf_noalloc_scratch_bytes(), dtype

@@ -9,7 +9,9 @@
 #include "kernels.h"
 
 // One error word per device (module-scope __device__ variable; each device that loads the
-// library holds its own copy).  Kernels get its address through Params::err.
+// library holds its own copy).  Kernels get its address through Params::err.  The address is
+// looked up once per device and kept for the life of the process; it is not valid after a
+// cudaDeviceReset of that device.
 __device__ int g_vlf_error_word = 0;
 
 namespace vlf {

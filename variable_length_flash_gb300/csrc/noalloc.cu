@@ -19,6 +19,9 @@
 //     them) race on the array and give wrong gradients; order them on one stream or with events.
 //   * The first call on each device looks up the array's device address (cudaGetSymbolAddress
 //     with that device current); make that first call before any stream capture begins.
+//   * That address is kept for the life of the process.  It is not valid after the device is
+//     reset (cudaDeviceReset): a process that resets a device must not call this entry point on
+//     it afterwards.
 #include <mutex>
 
 #include "common.cuh"

@@ -133,6 +133,9 @@ struct BwdCfg {
   static constexpr bool QT_DO = MODE == kDq && NV_PAD <= 128 && DOA + NV_PAD / 2 <= BUF;
   static constexpr bool QT = QT_Q || QT_DO;
   static_assert(!QT_Q || QT_DO, "TMEM columns of the A operands");
+  // the A operands sit past the accumulator, [0, NQ_PAD), and end before the S / dP buffers
+  static_assert(!QT_Q || (QA >= NQ_PAD && QA + NQ_PAD / 2 <= DOA), "TMEM columns of the Q operand");
+  static_assert(!QT_DO || (DOA >= NQ_PAD && DOA + NV_PAD / 2 <= BUF), "TMEM columns of the dO operand");
   static constexpr int HALF = IR / 2;      // columns per compute warpgroup
   static constexpr int CHUNKS = HALF / 32;  // 32-column chunks per compute thread
   static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * 2 * IR) <= 512, "TMEM columns");
