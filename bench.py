@@ -70,6 +70,7 @@ CONFIGS = [
     ("dense4x4096_bf16_causal_d256", 20, 5),
     ("decode64x8192_bf16_gqa", 50, 5),
     ("decode4x32768_bf16_gqa", 50, 5),
+    ("dense4x4096_fp32_causal_d64", 5, 3),
 ]
 LATENCY_CONFIGS = ["varlen64_fp16_full", "varlen64_fp16_causal"]
 SUSTAIN_S = 1.2  # length of the sustained run before the timed steps
@@ -314,8 +315,8 @@ def run_reference(args, rank, world):
 class Problem:
     """One workload's device inputs, results and the calls of one step through the library."""
 
-    def __init__(self, vlf, w, dev, seed):
-        self.vlf, self.w, self.dev = vlf, w, dev
+    def __init__(self, vlf, w, dev, seed, flags=0):
+        self.vlf, self.w, self.dev, self.flags = vlf, w, dev, flags
         x = W.make_inputs(w, seed=seed, device=dev, with_dout=True)
         self.latent_api = w.latent_split is not None and w.rope_heads is not None
         self.in_names = (("q_nope", "q_rope", "k_nope", "k_rope", "v") if self.latent_api
@@ -355,7 +356,7 @@ class Problem:
         fw = self.fws[0] if fw is None else fw
         ops = [d[n] for n in self.in_names]
         cu = (d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv)
-        kw = dict(self.kw, bias=d["bias"] if "bias" in d else self.kw["bias"])
+        kw = dict(self.kw, bias=d["bias"] if "bias" in d else self.kw["bias"], flags=self.flags)
         if self.latent_api:
             vlf.vlf_attn_varlen_fwd_latent(*ops, *cu, out=r["out"], lse=r["lse"], stream=st, **kw)
         else:
@@ -420,6 +421,8 @@ def roofline(prob, stage_ms, peaks, tensor_peak, dev):
         roof = {"bound": "alu", "achieved": flops_of[dom] / sec / 1e12, "peak": alu_peak,
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    if roof["bound"] == "tensor":
+        roof["frac_of_burst"] = roof["achieved"] / peaks["bf16_tflops"]
     tr = ncu_traffic(dom, w.name) if tc or roof["bound"] == "hbm" else None
     roof["traffic"] = tr
     roof["kernel"] = dom
@@ -501,15 +504,25 @@ def measure(vlf, w, dev, world, steps, warmup, sampler, peaks, tensor_peak=None,
     value = world * pairs * step_flops / (ms_step * 1e-3) / 1e12
     fwd_tflops = pairs * fpp["fwd"] / (stage_ms["fwd"] * 1e-3) / 1e12
     roof, paths = roofline(prob, stage_ms, peaks, tensor_peak, dev)
+    if w.dtype == "fp32":
+        # the same forward on the SIMT fp32-FMA kernels, for comparison with the tf32 passes
+        prob.flags = vlf.VLF_FLAG_FORCE_SIMT
+        _, st_simt, _ = time_steps(prob, max(2, steps // 2), stream, dev, world, flush)
+        prob.flags = 0
     rec = {"workload": w.name, "step": "fwd+bwd" if w.backward else "fwd",
            "value": value, "unit": "TFLOP/s", "steps": steps, "warmup": warmup,
            "ms_per_step": ms_step, "fwd_tflops": fwd_tflops,
            "fwd_frac_of_peak": fwd_tflops / tensor_peak,
            "value_frac_of_peak": value / world / tensor_peak,
            "tensor_peak": tensor_peak, "tensor_peak_kind": kind,
+           "fwd_frac_of_burst": fwd_tflops / peaks["bf16_tflops"],
+           "value_frac_of_burst": value / world / peaks["bf16_tflops"],
            "stage_ms": stage_ms, "roofline": roof, "paths": paths, "kv_splits": prob.n_split,
            "clocks": clocks, "gpu_launches": launches,
            "l2": config_of(w, world, l2_bytes_of(dev))["l2"]}
+    if w.dtype == "fp32":
+        rec["fwd_tflops_simt"] = pairs * fpp["fwd"] / (st_simt["fwd"] * 1e-3) / 1e12
+        rec["stage_ms_simt"] = st_simt
     if sustained is not None:
         sustained["value"] = world * pairs * step_flops / (sustained["ms_per_step"] * 1e-3) / 1e12
         rec["sustained"] = sustained
@@ -702,6 +715,8 @@ def main():
             "fwd_tflops": head["fwd_tflops"], "fwd_frac_of_peak": head["fwd_frac_of_peak"],
             "fwd_bwd_frac_of_peak": head["value_frac_of_peak"],
             "tensor_peak": head["tensor_peak"], "tensor_peak_kind": head["tensor_peak_kind"],
+            "fwd_frac_of_burst": head["fwd_frac_of_burst"],
+            "fwd_bwd_frac_of_burst": head["value_frac_of_burst"],
             "stage_ms": head["stage_ms"], "roofline": head["roofline"], "cpu_baseline": cpu,
             "e2e": e2e, "clocks": head["clocks"], "sustained": head.get("sustained"),
             "gpu_launches": head["gpu_launches"], "configs": configs,

@@ -33,6 +33,14 @@ CASES = {
     "fp32_d64_causal": W.custom([17, 64, 100], dtype="fp32", h_q=2, d_qk=64, causal=True),
     "fp32_d40_window": W.custom([50, 90], dtype="fp32", h_q=2, h_kv=1, d_qk=40, d_v=24,
                                 causal=True, window=7),
+    # fp32 on the tensor cores (products in three tf32 passes): widths 64 and 32, ragged tails,
+    # GQA, windows, cross attention
+    "fp32_d64_odd_gqa": W.custom(ODD, dtype="fp32", h_q=4, h_kv=2, d_qk=64, causal=True),
+    "fp32_d32_window_cross": W.custom([5, 100, 300], [70, 130, 300], dtype="fp32", h_q=2,
+                                      d_qk=32, causal=True, window=50),
+    "fp32_d64_full_long": W.custom([700, 129], dtype="fp32", h_q=2, h_kv=1, d_qk=64),
+    "fp32_d32_decode_mqa": W.custom([1, 3, 1], [200, 64, 1000], dtype="fp32", h_q=4, h_kv=1,
+                                    d_qk=32, causal=True),
     "fp16_d96": W.custom([70, 129], dtype="fp16", h_q=2, d_qk=96, causal=True),
     "bf16_d96_gqa_window": W.custom([300, 1, 129, 64], dtype="bf16", h_q=6, h_kv=2, d_qk=96,
                                     causal=True, window=100),
@@ -170,7 +178,8 @@ def test_outlier_channels(dtype):
 
 
 @pytest.mark.parametrize("name", ["bf16_d128_gqa_causal_odd", "fp16_d128_window16",
-                                  "varlen64_fp16_causal", "bf16_latent_192_128"])
+                                  "varlen64_fp16_causal", "bf16_latent_192_128",
+                                  "fp32_d32_window_cross"])
 @pytest.mark.parametrize("simt", [False, True])
 def test_tile_skipping_is_exact(name, simt):
     """Skipping fully masked KV tiles changes no bit of any output."""
@@ -182,6 +191,21 @@ def test_tile_skipping_is_exact(name, simt):
     b = gpu_run(w, x, flags=base | vlf.VLF_FLAG_NO_SKIP)
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+def test_fp32_tensor_core_forward_is_taken_and_matches_simt():
+    """fp32 at widths 32 / 64 runs the three-pass tf32 forward; it and the SIMT fp32-FMA forward
+    both meet the fp32 gate against the oracle."""
+    import variable_length_flash_gb300 as vlf
+    for d in (32, 64):
+        assert vlf.vlf_fwd_path(4, 2, d, d, vlf.VLF_F32) == 1
+        assert vlf.vlf_fwd_path(4, 2, d, d, vlf.VLF_F32, flags=vlf.VLF_FLAG_FORCE_SIMT) == 0
+    w = CASES["fp32_d64_odd_gqa"]
+    x = W.make_inputs(w, seed=31, with_dout=False)
+    ref = oracle_run(w, x, backward=False)
+    for flags in (0, vlf.VLF_FLAG_FORCE_SIMT):
+        gpu = gpu_run(w, x, flags=flags, backward=False)
+        assert_within(compare(w, gpu, ref), f"fp32 forward flags={flags}")
 
 
 @pytest.mark.parametrize("name", ["bf16_d128_gqa_causal_odd", "bf16_latent_192_128",

@@ -133,6 +133,16 @@ __global__ void fill_f32_kernel(float *p, size_t n, float v) {
   if (i < n) p[i] = v;
 }
 
+// The unsplit forward: the 16-bit tensor-core kernels, the fp32 three-pass tf32 kernel, or the
+// SIMT fp32-FMA kernels (forced by VLF_FLAG_FORCE_SIMT, and for shapes without a tensor-core one).
+cudaError_t forward_dispatch(const vlf::Params &p, cudaStream_t cs) {
+  if (!(p.flags & VLF_FLAG_FORCE_SIMT)) {
+    if (vlf::tc_forward_supported(p)) return vlf::tc_forward(p, cs);
+    if (vlf::tc_forward32_supported(p)) return vlf::tc_forward32(p, cs);
+  }
+  return vlf::simt_forward(p, cs);
+}
+
 cudaError_t zero16(void *p, size_t elems, cudaStream_t st) {
   return elems && p ? cudaMemsetAsync(p, 0, elems * 2, st) : cudaSuccess;
 }
@@ -160,7 +170,8 @@ int vlf_fwd_path(int h_q, int h_kv, int d_qk, int d_v, int dtype, int bias_heads
     return VLF_ERR_INVALID;
   if (d_qk > 256 || d_v > 256) return VLF_ERR_UNSUPPORTED;
   vlf::Params p = shape_params(h_q, h_kv, d_qk, d_v, dtype, bias_heads, flags);
-  return (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_forward_supported(p)) ? 1 : 0;
+  return (!(flags & VLF_FLAG_FORCE_SIMT) &&
+          (vlf::tc_forward_supported(p) || vlf::tc_forward32_supported(p))) ? 1 : 0;
 }
 
 int vlf_bwd_path(int h_q, int h_kv, int d_qk, int d_v, int dtype, int bias_heads, unsigned flags) {
@@ -220,11 +231,7 @@ int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
   p.err = error_word_ptr();
   if (!p.err) return VLF_ERR_LAUNCH;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_forward_supported(p))
-    e = vlf::tc_forward(p, cs);
-  else
-    e = vlf::simt_forward(p, cs);
+  const cudaError_t e = forward_dispatch(p, cs);
   return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
 }
 
@@ -295,10 +302,8 @@ int vlf_attn_varlen_fwd_split(const void *q, const void *k, const void *v,
     p.lse_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                            ((rows * (size_t)d_v * sizeof(float) + 255) & ~(size_t)255));
     e = vlf::tc_forward_split(p, cs);
-  } else if (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_forward_supported(p)) {
-    e = vlf::tc_forward(p, cs);
   } else {
-    e = vlf::simt_forward(p, cs);
+    e = forward_dispatch(p, cs);
   }
   return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
 }

@@ -25,6 +25,10 @@ cudaError_t tc_forward_split(const Params &p, cudaStream_t st);
 // problem's launch shape and the device's SM count.
 int fwd_num_splits(int num_seqs, int max_q, int max_kv, int h_q, int h_kv, int d_qk, int d_v,
                    int dtype, unsigned flags, int num_sms);
+// fp32 inputs on the tensor cores, products in three tf32 passes (tc_fwd32.cu): head widths 32
+// and 64.
+bool tc_forward32_supported(const Params &p);
+cudaError_t tc_forward32(const Params &p, cudaStream_t st);
 bool tc_backward_supported(const Params &p);
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev);
 size_t tc_backward_workspace(int total_q, int h_q, int d_qk);

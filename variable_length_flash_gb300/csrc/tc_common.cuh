@@ -302,6 +302,45 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_type, uint32_t m, u
          | ((m >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor of kind::tf32 (A and B read as tf32 from 32-bit data) with fp32
+// accumulation; both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t m, uint32_t n) {
+  return (1u << 4)            // D format: f32
+         | (2u << 7)          // A format: tf32
+         | (2u << 10)         // B format: tf32
+         | ((n >> 3) << 17)   // N / 8
+         | ((m >> 4) << 24);  // M / 16
+}
+// D[tmem] (+)= A[smem] * B[smem]^T and A[tmem] * B[smem]^T in tf32 (K = 8 per instruction),
+// warp-converged forms as above.
+__device__ __forceinline__ void mma_ss_tf32_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_tf32_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The tf32 value nearest to x (round to nearest, ties to even, on the 13 low mantissa bits
+// that tf32 drops), as an fp32 bit pattern whose low 13 bits are zero; infinities and NaNs are
+// returned unchanged.  x - tf32_round(x) is exact in fp32 (the two share an exponent or x is
+// within a factor of two of the rounded value).
+__device__ __forceinline__ float tf32_round(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7f800000u) == 0x7f800000u) return x;
+  u += 0xfffu + ((u >> 13) & 1u);
+  return __uint_as_float(u & 0xffffe000u);
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
   if (is_bf16) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -764,6 +764,22 @@ bool make_tmap_16bit(CUtensorMap *m, const void *base, uint64_t rows, uint64_t c
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over a [rows, cols] row-major fp32 matrix with row pitch `pitch_elems`; box of 32
+// columns (128 bytes) x box_rows rows, 128-byte swizzle (the K-major tf32 operand layout).
+bool make_tmap_f32(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+                   uint64_t pitch_elems, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_elems * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D map over the bias as [total_q][bias_heads x max_kv] fp32: box {32 columns, box_rows rows}
 // (128-byte rows), optionally 128-byte swizzled (threads that read along a row then take chunk
 // c at c ^ (row mod 8)).

@@ -21,6 +21,7 @@ Workloads (named by what they are; the shapes are the benchmark configurations o
   dim 128, end-aligned causal, bf16, forward only.
 * ``dense4x4096_bf16_causal_d96`` -- the dense configuration at head width 96.
 * ``dense4x4096_bf16_causal_d256`` -- the dense configuration at head width 256.
+* ``dense4x4096_fp32_causal_d64`` -- the dense configuration with fp32 data at head width 64.
 * ``latent2x8192_bf16_causal_shared_rope`` -- the latent configuration with split operands and
   one rope key [tokens, 1, 64] shared by all 128 heads.
 
@@ -113,6 +114,10 @@ def workload(name: str, seed: int = 0) -> Workload:
         # the dense configuration at head width 96 (a width the pages list beside 64/128/256)
         lens = [4096] * 4
         return Workload(name, "bf16", lens, lens, 32, 32, 96, 96, causal=True)
+    if name == "dense4x4096_fp32_causal_d64":
+        # the dense configuration with fp32 inputs at head width 64 (fp32 is supported data)
+        lens = [4096] * 4
+        return Workload(name, "fp32", lens, lens, 32, 32, 64, 64, causal=True)
     if name == "dense4x4096_bf16_causal_d256":
         # the dense configuration at head width 256
         lens = [4096] * 4
@@ -152,7 +157,7 @@ WORKLOADS = ["varlen64_fp16_full", "varlen64_fp16_causal", "dense4x4096_bf16_cau
              "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
              "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "decode64x8192_bf16_gqa",
              "dense4x4096_bf16_causal_d96", "decode4x32768_bf16_gqa", "dense4x4096_bf16_causal_d256",
-             "latent2x8192_bf16_causal_shared_rope"]
+             "latent2x8192_bf16_causal_shared_rope", "dense4x4096_fp32_causal_d64"]
 
 
 def custom(lengths_q, lengths_kv=None, *, dtype="bf16", h_q=4, h_kv=None, d_qk=64, d_v=None,
