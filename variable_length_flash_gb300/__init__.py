@@ -236,6 +236,16 @@ def _bias_args(bias, total_q, h_q):
     return bias, int(bias.shape[1])
 
 
+def _fwd_checks(q, k, v, cu_seqlens_q, cu_seqlens_kv):
+    """The forward's argument checks with a message for each failure (the slow path)."""
+    _req(q, "q"), _req(k, "k", q.dtype), _req(v, "v", q.dtype)
+    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
+    if q.dtype not in _DTYPE:
+        raise VlfError(VLF_ERR_INVALID, f"unsupported dtype {q.dtype}")
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise VlfError(VLF_ERR_INVALID, "q, k, v must be [tokens, heads, head_dim]")
+
+
 def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_seqlen_kv=None,
                         scale=None, causal=False, window=0, bias=None, out=None, lse=None,
                         stream=None, flags=0, num_splits=None, workspace=None):
@@ -246,26 +256,40 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
     decide whether to split each CTA's KV band (small-batch / decode shapes; the parts' fp32
     results go to ``workspace``, allocated here when not given), 1 never splits, k > 1 splits
     into k parts."""
-    _req(q, "q"), _req(k, "k", q.dtype), _req(v, "v", q.dtype)
-    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
-    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
-        raise VlfError(VLF_ERR_INVALID, "q, k, v must be [tokens, heads, head_dim]")
+    # the common case's conditions in one pass (each tensor attribute costs ~0.1 us of host
+    # time, which small problems pay per call); any failure takes the detailed checks
+    dtype = q.dtype
+    if not (dtype in _DTYPE and k.dtype is dtype and v.dtype is dtype and q.is_cuda and k.is_cuda
+            and v.is_cuda and q.is_contiguous() and k.is_contiguous() and v.is_contiguous()
+            and q.dim() == 3 and k.dim() == 3 and v.dim() == 3
+            and cu_seqlens_q.dtype is torch.int32 and cu_seqlens_kv.dtype is torch.int32
+            and cu_seqlens_q.is_cuda and cu_seqlens_kv.is_cuda
+            and cu_seqlens_q.is_contiguous() and cu_seqlens_kv.is_contiguous()):
+        _fwd_checks(q, k, v, cu_seqlens_q, cu_seqlens_kv)
     tq, hq, dqk = q.shape
     tk, hkv, dv = v.shape
-    if k.shape[0] != tk or k.shape[1] != hkv or k.shape[2] != dqk:
+    if k.shape != (tk, hkv, dqk):
         raise VlfError(VLF_ERR_INVALID, "k shape")
     if max_seqlen_kv is None:
         max_seqlen_kv = int(bias.shape[2]) if bias is not None else _max_len(cu_seqlens_kv)
-    if bias is not None and bias.shape[2] != max_seqlen_kv:
-        raise VlfError(VLF_ERR_INVALID, "bias last dim must be max_seqlen_kv")
-    bias, bh = _bias_args(bias, tq, hq)
+    if bias is not None:
+        if bias.shape[2] != max_seqlen_kv:
+            raise VlfError(VLF_ERR_INVALID, "bias last dim must be max_seqlen_kv")
+        bias, bh = _bias_args(bias, tq, hq)
+        bias_p = bias.data_ptr()
+    else:
+        bias_p, bh = None, 0
     if out is None:
-        out = torch.empty((tq, hq, dv), dtype=q.dtype, device=q.device)
+        out = torch.empty((tq, hq, dv), dtype=dtype, device=q.device)
+    elif not (out.dtype is dtype and out.is_cuda and out.is_contiguous()):
+        _req(out, "out", dtype)
     if lse is None:
         lse = torch.empty((hq, tq), dtype=torch.float32, device=q.device)
-    _req(out, "out", q.dtype), _req(lse, "lse", torch.float32)
+    elif not (lse.dtype is torch.float32 and lse.is_cuda and lse.is_contiguous()):
+        _req(lse, "lse", torch.float32)
     nseq = cu_seqlens_q.numel() - 1
-    dt = _DTYPE[q.dtype]
+    dt = _DTYPE[dtype]
+    st_h = stream.cuda_stream if stream is not None else _stream(None, q)
     if num_splits is None:
         num_splits = _lib.vlf_fwd_num_splits(nseq, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
                                              dqk, dv, dt, int(flags), 0)
@@ -275,19 +299,21 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
         _req(workspace, "workspace")
         st = _lib.vlf_attn_varlen_fwd_split(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), nseq, tq, tk,
-            int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv, dt,
-            float(scale) if scale else 0.0, int(bool(causal)), int(window or 0), _ptr(bias), bh,
-            _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), _stream(stream, q), int(flags))
-        _check(st, "vlf_attn_varlen_fwd_split")
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(),
+            cu_seqlens_kv.data_ptr(), nseq, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
+            dqk, dv, dt, float(scale) if scale else 0.0, int(bool(causal)), int(window or 0), bias_p,
+            bh, out.data_ptr(), lse.data_ptr(), int(num_splits), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), st_h, int(flags))
+        if st != VLF_OK:
+            _check(st, "vlf_attn_varlen_fwd_split")
         return out, lse
     st = _lib.vlf_attn_varlen_fwd_ex(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
-        cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv,
-        _DTYPE[q.dtype], float(scale) if scale else 0.0, int(bool(causal)), int(window or 0),
-        _ptr(bias), bh, _ptr(out), _ptr(lse), _stream(stream, q), int(flags))
-    _check(st, "vlf_attn_varlen_fwd")
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_kv.data_ptr(),
+        nseq, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv, dt,
+        float(scale) if scale else 0.0, int(bool(causal)), int(window or 0), bias_p, bh,
+        out.data_ptr(), lse.data_ptr(), st_h, int(flags))
+    if st != VLF_OK:
+        _check(st, "vlf_attn_varlen_fwd")
     return out, lse
 
 

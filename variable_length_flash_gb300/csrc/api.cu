@@ -23,13 +23,13 @@ cudaError_t set_smem_once(const void *kern, int bytes) {
     const void *kern;
     int dev, bytes;
   };
-  static Entry table[256];
-  static int n_entries = 0;
-  static std::mutex mu;
+  // per host thread (no lock on the launch path): a thread that has not set a kernel's limit
+  // itself sets it once more, which is harmless
+  thread_local Entry table[256];
+  thread_local int n_entries = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_entries; ++i)
     if (table[i].kern == kern && table[i].dev == dev) {
       if (bytes <= table[i].bytes) return cudaSuccess;
@@ -52,13 +52,19 @@ int *g_err_ptr[kMaxDevices] = {nullptr};
 int *error_word_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  // the last device's address, per host thread, skips the lock on repeated calls
+  thread_local int t_dev = -1;
+  thread_local int *t_ptr = nullptr;
+  if (dev == t_dev) return t_ptr;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_err_ptr[dev]) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_vlf_error_word) != cudaSuccess) return nullptr;
     g_err_ptr[dev] = static_cast<int *>(ptr);
   }
-  return g_err_ptr[dev];
+  t_dev = dev;
+  t_ptr = g_err_ptr[dev];
+  return t_ptr;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

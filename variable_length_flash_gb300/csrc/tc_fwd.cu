@@ -35,6 +35,7 @@
 //    drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <string.h>
 
 #include <type_traits>
 
@@ -732,7 +733,7 @@ cudaError_t launch_combine(const Params &p, cudaStream_t st) {
   return e;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 driver_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -744,6 +745,59 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   }();
   return fn;
 }
+
+// Every argument of one encode, zero-padded so that two keys compare with memcmp.
+struct TmapKey {
+  void *base;
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], es[3];
+  uint32_t dtype, rank, interleave, swizzle, l2, oob;
+};
+struct TmapEntry {
+  CUtensorMap map;
+  TmapKey key;
+  bool valid;
+};
+// Encoded maps of recent calls, per host thread (no locking): a call that repeats a tensor's
+// address, shape and box -- every training or decode step -- copies its map instead of encoding
+// it again (host time per call matters for small problems, whose kernels take microseconds).
+thread_local TmapEntry t_tmap_cache[64];
+
+CUresult CUDAAPI cached_encode(CUtensorMap *m, CUtensorMapDataType dt, cuuint32_t rank, void *base,
+                               const cuuint64_t *dims, const cuuint64_t *strides,
+                               const cuuint32_t *box, const cuuint32_t *es,
+                               CUtensorMapInterleave il, CUtensorMapSwizzle sw,
+                               CUtensorMapL2promotion l2, CUtensorMapFloatOOBfill oob) {
+  if (rank < 1 || rank > 3) return driver_encode_fn()(m, dt, rank, base, dims, strides, box, es, il, sw, l2, oob);
+  TmapKey k;
+  memset(&k, 0, sizeof(k));
+  k.base = base;
+  for (cuuint32_t i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    k.es[i] = es[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  k.dtype = (uint32_t)dt; k.rank = rank; k.interleave = (uint32_t)il; k.swizzle = (uint32_t)sw;
+  k.l2 = (uint32_t)l2; k.oob = (uint32_t)oob;
+  uint64_t h = reinterpret_cast<uint64_t>(base) >> 4;
+  for (cuuint32_t i = 0; i < rank; ++i) h = h * 0x9E3779B97F4A7C15ull + dims[i] * 131 + box[i];
+  TmapEntry &e = t_tmap_cache[(h ^ (h >> 29)) & 63];
+  if (e.valid && memcmp(&e.key, &k, sizeof(k)) == 0) {
+    *m = e.map;
+    return CUDA_SUCCESS;
+  }
+  const CUresult r = driver_encode_fn()(m, dt, rank, base, dims, strides, box, es, il, sw, l2, oob);
+  if (r == CUDA_SUCCESS) {
+    e.map = *m;
+    e.key = k;
+    e.valid = true;
+  }
+  return r;
+}
+
+// The encoder the map builders below use: the driver's cuTensorMapEncodeTiled behind the cache.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return driver_encode_fn() ? cached_encode : nullptr; }
 
 }  // namespace
 
