@@ -346,6 +346,15 @@ class Problem:
         self.fws = [torch.empty(max(1, vlf.vlf_attn_varlen_fwd_split_workspace_size(
             w.total_q, w.h_q, w.d_v, self.n_split)), dtype=torch.uint8, device=dev)
             for _ in range(2)]
+        # a bias: its bands (which keys it leaves each row) are computed once per step, for the
+        # forward and the backward, into a buffer allocated here
+        self.bands = None
+        if x["bias"] is not None:
+            self.bands = torch.empty(max(16, vlf.vlf_bias_bands_size(w.total_q, w.bias_heads)),
+                                     dtype=torch.uint8, device=dev)
+        # per-step timing stages (consecutive events)
+        self.stages = ((["bands"] if self.bands is not None else []) + ["fwd"] +
+                       (list(vlf.BWD_STAGE_NAMES) if w.backward else []))
 
     def run(self, d=None, r=None, fw=None, st=None, ev=None, stream=None):
         """One step on inputs d into results r (the problem's own when None) on stream st (the
@@ -357,6 +366,14 @@ class Problem:
         ops = [d[n] for n in self.in_names]
         cu = (d["cu_seqlens_q"], d["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv)
         kw = dict(self.kw, bias=d["bias"] if "bias" in d else self.kw["bias"], flags=self.flags)
+        e = 1  # the next timing event to record after a stage
+        if self.bands is not None:
+            vlf.vlf_bias_bands(kw["bias"], d["cu_seqlens_q"], d["cu_seqlens_kv"], out=self.bands,
+                               stream=st)
+            kw["bias_bands"] = self.bands
+            if ev is not None:
+                ev[e].record(stream)
+            e += 1
         if self.latent_api:
             vlf.vlf_attn_varlen_fwd_latent(*ops, *cu, out=r["out"], lse=r["lse"], stream=st, **kw)
         else:
@@ -364,9 +381,9 @@ class Problem:
                                     workspace=fw, num_splits=self.n_split, **kw)
         if not w.backward:
             if ev is not None:
-                ev[1].record(stream)
+                ev[e].record(stream)
             return
-        sev = None if ev is None else ev[1:]
+        sev = None if ev is None else ev[e:]
         if self.latent_api:
             vlf.vlf_attn_varlen_bwd_latent(d["dout"], *ops, r["out"], r["lse"], *cu,
                                            grads=tuple(r[g] for g in self.grad_of),
@@ -390,7 +407,8 @@ class Problem:
         o_b, row_b = nq * w.d_v * eb, 4 * nq                    # O (or dO), one fp32 per row
         bias_b = 0 if x["bias"] is None else x["bias"].numel() * 4
         flops = {"fwd": pairs * fpp["fwd"], "dkdv": pairs * fpp["dkdv"], "dq": pairs * fpp["dq"]}
-        bytes_ = {"fwd": q_b + k_b + v_b + o_b + row_b + bias_b,
+        bytes_ = {"bands": bias_b,  # (at most: the pass stops scanning a row at its ends)
+                  "fwd": q_b + k_b + v_b + o_b + row_b + bias_b,
                   "rowdot": 2 * o_b + row_b,
                   "dkdv": q_b + k_b + v_b + o_b + 2 * row_b + k_b + v_b + bias_b,
                   "dq": q_b + k_b + v_b + o_b + 2 * row_b + q_b + bias_b}
@@ -436,7 +454,7 @@ def time_steps(prob, steps, stream, dev, world, flush_l2):
     """Time exactly ``steps`` steps (barrier + synchronize on both sides).  Returns the step
     time in ms (max over ranks), the per-stage mean times and the library launches counted."""
     vlf = prob.vlf
-    n_ev = 2 if not prob.w.backward else 2 + vlf.VLF_BWD_STAGES
+    n_ev = len(prob.stages) + 1
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
     for row in evs:  # torch creates the CUDA event at its first record()
         for e in row:
@@ -463,9 +481,8 @@ def time_steps(prob, steps, stream, dev, world, flush_l2):
         ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[-1]) for e in evs), world)
     else:
         ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / steps
-    names = ["fwd"] + ([] if not prob.w.backward else list(vlf.BWD_STAGE_NAMES))
     stage_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
-                for i, n in enumerate(names)}
+                for i, n in enumerate(prob.stages)}
     return ms_step, stage_ms, launches
 
 
@@ -537,13 +554,23 @@ def latency(vlf, w, dev, calls=300, warmup=30):
     ends); us_per_call: back-to-back calls, wall clock (host and device overlap)."""
     stream = torch.cuda.current_stream()
     prob = Problem(vlf, w, dev, seed=0)
+    x, r = prob.x, prob.res
+    args = (x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_kv"], w.max_seqlen_q,
+            w.max_seqlen_kv)
+    kw = dict(scale=w.scale, causal=w.causal, window=w.window, out=r["out"], lse=r["lse"],
+              num_splits=prob.n_split, workspace=prob.fws[0])
+    fwd = vlf.vlf_attn_varlen_fwd
+
+    def call():  # the public call as a user makes it
+        fwd(*args, **kw)
+
     for _ in range(warmup):
-        prob.run()
+        call()
     torch.cuda.synchronize()
     # back-to-back calls, inputs L2-resident
     t0 = time.perf_counter()
     for _ in range(calls):
-        prob.run()
+        call()
     t1 = time.perf_counter()
     torch.cuda.synchronize()
     t2 = time.perf_counter()
@@ -557,7 +584,7 @@ def latency(vlf, w, dev, calls=300, warmup=30):
     for a, b in ev:
         flush_buf.zero_()
         a.record(stream)
-        prob.run()
+        call()
         b.record(stream)
     torch.cuda.synchronize()
     launches = (vlf.vlf_launch_count() - n0) / calls

@@ -93,7 +93,8 @@ typedef enum {
  *                -inf for a row that sees no key (its out row is 0).  Required by the backward.
  * Supported: dtype F16/BF16 with any 1 <= d_qk, d_v <= 256 (tensor-core kernels for
  * (d_qk, d_v) in {(64,64), (96,96), (128,128), (192,128), (256,256)}); dtype F32 with d_qk,
- * d_v <= 256 (fp32 FMA).
+ * d_v <= 256 (tensor-core kernels for (32,32) and (64,64), products in three tf32 passes with
+ * fp32 accumulation; fp32 FMA otherwise).
  */
 int vlf_attn_varlen_fwd(const void *q, const void *k, const void *v,
                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
@@ -103,13 +104,19 @@ int vlf_attn_varlen_fwd(const void *q, const void *k, const void *v,
                         const float *bias, int bias_heads,
                         void *out, float *lse, vlf_stream_t stream);
 
+/*
+ * As vlf_attn_varlen_fwd, plus `flags` (VLF_FLAG_*) and `bias_bands`: NULL, or the result of
+ * vlf_bias_bands for this bias (below), which lets the kernels skip the KV tiles the bias masks
+ * for every row of a query tile.
+ */
 int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
                            int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
                            int h_q, int h_kv, int d_qk, int d_v, int dtype,
                            float scale, int causal, int window,
                            const float *bias, int bias_heads,
-                           void *out, float *lse, vlf_stream_t stream, unsigned flags);
+                           void *out, float *lse, vlf_stream_t stream, unsigned flags,
+                           const void *bias_bands);
 
 /*
  * Split-KV forward, for problems whose (query tile, head) CTAs are too few to fill the GPU --
@@ -139,7 +146,7 @@ int vlf_attn_varlen_fwd_split(const void *q, const void *k, const void *v,
                               const float *bias, int bias_heads,
                               void *out, float *lse, int num_splits,
                               void *workspace, size_t workspace_bytes, vlf_stream_t stream,
-                              unsigned flags);
+                              unsigned flags, const void *bias_bands);
 
 /*
  * The number of parts vlf_attn_varlen_fwd_split uses for num_splits = 0 (1: no split).  Pure
@@ -192,7 +199,8 @@ int vlf_attn_varlen_bwd(const void *q, const void *k, const void *v, const void 
                         void *workspace, size_t workspace_bytes, vlf_stream_t stream);
 
 /*
- * As vlf_attn_varlen_bwd, plus `flags` and optional per-stage timing events.  When
+ * As vlf_attn_varlen_bwd, plus `flags`, optional per-stage timing events and the bias bands
+ * (NULL, or vlf_bias_bands's result for this bias, as in vlf_attn_varlen_fwd_ex).  When
  * stage_events is not NULL it holds n_stage_events >= VLF_BWD_STAGES + 1 cudaEvent_t handles
  * (created by the caller); event 0 is recorded on `stream` before the first kernel and event
  * s+1 after stage s, stages being, in order: 0 the dO.O row-dot pre-pass, 1 the dK/dV kernel,
@@ -208,7 +216,32 @@ int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
                            const float *bias, int bias_heads,
                            void *dq, void *dk, void *dv,
                            void *workspace, size_t workspace_bytes, vlf_stream_t stream,
-                           unsigned flags, void *const *stage_events, int n_stage_events);
+                           unsigned flags, void *const *stage_events, int n_stage_events,
+                           const void *bias_bands);
+
+/*
+ * Bias bands.  An additive bias often masks whole stretches of each row (mtlattn 0.3.0, "Use":
+ * -inf masks a pair and a boolean mask becomes a 0 / -inf bias; a prefix-LM mask hides every key
+ * past the prefix and the diagonal).  This pass records, for each bias head and query row, the
+ * keys from the first to the last finite value among the row's first kv_len columns, and whether
+ * the bias is exactly 0 throughout them; and the same, combined, for each block of 64 rows of
+ * each sequence.  Given to the _ex calls, it lets the tensor-core kernels (16-bit data, widths
+ * up to 128, one query tile per CTA) skip the KV tiles and query items that hold only -inf bias
+ * values for their rows -- the skipped pairs contribute exact zeros -- and mask by interval
+ * without reading the bias where every row of a tile is such a 0 / -inf interval.  The results
+ * equal those computed without the bands within the stated tolerances (the bias values of a pure
+ * interval are 0; the masked pairs are the same).  The bands must come from this bias (same
+ * tensor, unmodified since): stale bands give wrong results.
+ *   bias, bias_heads, cu_seqlens_q / _kv, num_seqs, total_q, max_seqlen_kv   as in the forward
+ *   bands        device buffer of at least vlf_bias_bands_size(total_q, bias_heads) bytes,
+ *                16-byte aligned, owned by the caller, written
+ * Enqueued on `stream`; no synchronisation.  Returns VLF_OK or a negative status (invalid
+ * arguments, VLF_ERR_WORKSPACE for a missing or short buffer).
+ */
+size_t vlf_bias_bands_size(int total_q, int bias_heads);
+int vlf_bias_bands(const float *bias, int bias_heads, const int32_t *cu_seqlens_q,
+                   const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int max_seqlen_kv,
+                   void *bands, size_t bands_bytes, vlf_stream_t stream);
 
 /*
  * Latent attention with split operands (triton-msl part 2, "Latent attention": the score is the

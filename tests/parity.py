@@ -16,20 +16,24 @@ def to_np(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def gpu_run(w, x, flags=0, backward=True, device="cuda"):
+def gpu_run(w, x, flags=0, backward=True, device="cuda", bias_bands=None):
+    """The CUDA path through the binding; bias_bands as the binding takes it (None: computed
+    for a bias, False: none)."""
     import variable_length_flash_gb300 as vlf
     g = {k: (t.to(device) if isinstance(t, torch.Tensor) else t) for k, t in x.items()}
+    if bias_bands is None and g["bias"] is not None:
+        bias_bands = vlf.vlf_bias_bands(g["bias"], g["cu_seqlens_q"], g["cu_seqlens_kv"])
     out, lse = vlf.vlf_attn_varlen_fwd(g["q"], g["k"], g["v"], g["cu_seqlens_q"],
                                        g["cu_seqlens_kv"], w.max_seqlen_q, w.max_seqlen_kv,
                                        scale=w.scale, causal=w.causal, window=w.window,
-                                       bias=g["bias"], flags=flags)
+                                       bias=g["bias"], flags=flags, bias_bands=bias_bands)
     res = {"out": out, "lse": lse}
     if backward:
         dq, dk, dv = vlf.vlf_attn_varlen_bwd(g["dout"], g["q"], g["k"], g["v"], out, lse,
                                              g["cu_seqlens_q"], g["cu_seqlens_kv"],
                                              w.max_seqlen_q, w.max_seqlen_kv, scale=w.scale,
                                              causal=w.causal, window=w.window, bias=g["bias"],
-                                             flags=flags)
+                                             flags=flags, bias_bands=bias_bands)
         res.update(dq=dq, dk=dk, dv=dv)
     status = vlf.vlf_check_error()
     assert status == 0, vlf.vlf_status_string(status)

@@ -44,7 +44,8 @@ EXPORTS = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_fwd_ex", "vlf_attn_varlen_bwd
            "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path", "vlf_attn_varlen_bwd_noalloc",
            "vlf_noalloc_scratch_bytes", "vlf_attn_varlen_fwd_split", "vlf_fwd_num_splits",
            "vlf_attn_varlen_fwd_split_workspace_size", "vlf_attn_varlen_fwd_latent",
-           "vlf_attn_varlen_bwd_latent", "vlf_attn_varlen_bwd_latent_workspace_size"]
+           "vlf_attn_varlen_bwd_latent", "vlf_attn_varlen_bwd_latent_workspace_size",
+           "vlf_bias_bands", "vlf_bias_bands_size"]
 VLF_BWD_STAGES = 3
 BWD_STAGE_NAMES = ["rowdot", "dkdv", "dq"]
 
@@ -63,10 +64,10 @@ def _load():
     P, I, F, Z, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint
     fwd = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, I, P, I, P, P, P]
     lib.vlf_attn_varlen_fwd.argtypes = fwd
-    lib.vlf_attn_varlen_fwd_ex.argtypes = fwd + [U]
+    lib.vlf_attn_varlen_fwd_ex.argtypes = fwd + [U, P]
     bwd = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, I, P, I, P, P, P, P, Z, P]
     lib.vlf_attn_varlen_bwd.argtypes = bwd
-    lib.vlf_attn_varlen_bwd_ex.argtypes = bwd + [U, P, I]
+    lib.vlf_attn_varlen_bwd_ex.argtypes = bwd + [U, P, I, P]
     for name in ("vlf_attn_varlen_fwd", "vlf_attn_varlen_fwd_ex", "vlf_attn_varlen_bwd",
                  "vlf_attn_varlen_bwd_ex"):
         getattr(lib, name).restype = I
@@ -85,7 +86,7 @@ def _load():
     lib.vlf_version.restype = I
     lib.vlf_attn_varlen_bwd_noalloc.argtypes = bwd[:23] + [P, P, P, P]  # ... bias_heads, dq, dk, dv, stream
     lib.vlf_attn_varlen_bwd_noalloc.restype = I
-    lib.vlf_attn_varlen_fwd_split.argtypes = fwd[:22] + [I, P, Z, P, U]  # ..., out, lse, splits, ws, bytes, stream, flags
+    lib.vlf_attn_varlen_fwd_split.argtypes = fwd[:22] + [I, P, Z, P, U, P]  # ..., out, lse, splits, ws, bytes, stream, flags, bands
     lib.vlf_attn_varlen_fwd_split.restype = I
     lib.vlf_fwd_num_splits.argtypes = [I, I, I, I, I, I, I, I, U, I]
     lib.vlf_fwd_num_splits.restype = I
@@ -98,6 +99,10 @@ def _load():
     lib.vlf_attn_varlen_bwd_latent.argtypes = ([P] * 10 + [I] * 12 + [F, I, I, P, I] + [P] * 6 +
                                                [Z, P, U, P, I])
     lib.vlf_attn_varlen_bwd_latent.restype = I
+    lib.vlf_bias_bands_size.argtypes = [I, I]
+    lib.vlf_bias_bands_size.restype = Z
+    lib.vlf_bias_bands.argtypes = [P, I, P, P, I, I, I, P, Z, P]
+    lib.vlf_bias_bands.restype = I
     lib.vlf_noalloc_scratch_bytes.argtypes = []
     lib.vlf_noalloc_scratch_bytes.restype = Z
     lib.vlf_launch_count.argtypes = []
@@ -246,16 +251,54 @@ def _fwd_checks(q, k, v, cu_seqlens_q, cu_seqlens_kv):
         raise VlfError(VLF_ERR_INVALID, "q, k, v must be [tokens, heads, head_dim]")
 
 
+def vlf_bias_bands_size(total_q, bias_heads) -> int:
+    return int(_lib.vlf_bias_bands_size(int(total_q), int(bias_heads)))
+
+
+def vlf_bias_bands(bias, cu_seqlens_q, cu_seqlens_kv, max_seqlen_kv=None, out=None, stream=None):
+    """The bias bands of ``bias`` [total_q, 1 or H_q, max_seqlen_kv] (fp32, CUDA): per bias head
+    and query row the keys from the first to the last finite value and whether the bias is 0
+    throughout them, plus the same per 64-row block of each sequence (include/vlf.h).  Returns
+    the uint8 CUDA buffer (``out`` when given) to pass as ``bias_bands`` to the forward and
+    backward; it stays valid while the bias is unchanged."""
+    _req(bias, "bias", torch.float32)
+    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32), _req(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
+    if bias.dim() != 3:
+        raise VlfError(VLF_ERR_INVALID, "bias must be [total_q, 1 or H_q, max_seqlen_kv]")
+    tq, bh, mk = bias.shape
+    if max_seqlen_kv is not None and int(max_seqlen_kv) != mk:
+        raise VlfError(VLF_ERR_INVALID, "bias last dim must be max_seqlen_kv")
+    need = vlf_bias_bands_size(tq, bh)
+    if out is None:
+        out = torch.empty(max(need, 16), dtype=torch.uint8, device=bias.device)
+    st = _lib.vlf_bias_bands(bias.data_ptr(), bh, cu_seqlens_q.data_ptr(), cu_seqlens_kv.data_ptr(),
+                             cu_seqlens_q.numel() - 1, tq, mk, out.data_ptr(), out.numel(),
+                             _stream(stream, bias))
+    _check(st, "vlf_bias_bands")
+    return out
+
+
+def _bands_arg(bias_bands, bias, cu_seqlens_q, cu_seqlens_kv, stream):
+    """The bands pointer for a call: computed here for a bias when not given (None); False
+    (or no bias) passes none."""
+    if bias is None or bias_bands is False:
+        return None
+    if bias_bands is None:
+        bias_bands = vlf_bias_bands(bias, cu_seqlens_q, cu_seqlens_kv, stream=stream)
+    return bias_bands.data_ptr()
+
+
 def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_seqlen_kv=None,
                         scale=None, causal=False, window=0, bias=None, out=None, lse=None,
-                        stream=None, flags=0, num_splits=None, workspace=None):
+                        stream=None, flags=0, num_splits=None, workspace=None, bias_bands=None):
     """Forward.  q [Tq,Hq,Dqk], k [Tkv,Hkv,Dqk], v [Tkv,Hkv,Dv] (fp16/bf16/fp32, CUDA,
     contiguous), cu_seqlens int32 [n+1].  Returns out [Tq,Hq,Dv] and lse fp32 [Hq,Tq].
     ``max_seqlen_kv=None`` reads it from cu_seqlens_kv (a host sync); the bias's last dim
     must equal max_seqlen_kv when a bias is given.  ``num_splits``: None lets the library
     decide whether to split each CTA's KV band (small-batch / decode shapes; the parts' fp32
     results go to ``workspace``, allocated here when not given), 1 never splits, k > 1 splits
-    into k parts."""
+    into k parts.  ``bias_bands``: for a bias, vlf_bias_bands's result for it (None: computed
+    here, one extra pass; False: none, every tile's bias is read)."""
     # the common case's conditions in one pass (each tensor attribute costs ~0.1 us of host
     # time, which small problems pay per call); any failure takes the detailed checks
     dtype = q.dtype
@@ -277,8 +320,9 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
             raise VlfError(VLF_ERR_INVALID, "bias last dim must be max_seqlen_kv")
         bias, bh = _bias_args(bias, tq, hq)
         bias_p = bias.data_ptr()
+        bands_p = _bands_arg(bias_bands, bias, cu_seqlens_q, cu_seqlens_kv, stream)
     else:
-        bias_p, bh = None, 0
+        bias_p, bh, bands_p = None, 0, None
     if out is None:
         out = torch.empty((tq, hq, dv), dtype=dtype, device=q.device)
     elif not (out.dtype is dtype and out.is_cuda and out.is_contiguous()):
@@ -303,7 +347,7 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
             cu_seqlens_kv.data_ptr(), nseq, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
             dqk, dv, dt, float(scale) if scale else 0.0, int(bool(causal)), int(window or 0), bias_p,
             bh, out.data_ptr(), lse.data_ptr(), int(num_splits), workspace.data_ptr(),
-            workspace.numel() * workspace.element_size(), st_h, int(flags))
+            workspace.numel() * workspace.element_size(), st_h, int(flags), bands_p)
         if st != VLF_OK:
             _check(st, "vlf_attn_varlen_fwd_split")
         return out, lse
@@ -311,7 +355,7 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
         q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_kv.data_ptr(),
         nseq, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv, dt,
         float(scale) if scale else 0.0, int(bool(causal)), int(window or 0), bias_p, bh,
-        out.data_ptr(), lse.data_ptr(), st_h, int(flags))
+        out.data_ptr(), lse.data_ptr(), st_h, int(flags), bands_p)
     if st != VLF_OK:
         _check(st, "vlf_attn_varlen_fwd")
     return out, lse
@@ -320,7 +364,7 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
 def vlf_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q,
                         max_seqlen_kv=None, scale=None, causal=False, window=0, bias=None,
                         dq=None, dk=None, dv=None, workspace=None, stream=None, flags=0,
-                        stage_events=None):
+                        stage_events=None, bias_bands=None):
     """Backward: gradients of sum(out * dout) w.r.t. q, k, v (bias constant).
     Returns dq, dk, dv in the input dtype.  ``workspace`` (uint8 CUDA tensor of at least
     vlf_attn_varlen_bwd_workspace_size bytes) is allocated with torch when not given.
@@ -346,7 +390,8 @@ def vlf_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, ma
         _ptr(cu_seqlens_kv), cu_seqlens_q.numel() - 1, tq, tk, int(max_seqlen_q),
         int(max_seqlen_kv), hq, hkv, dqk, dvv, _DTYPE[q.dtype], float(scale) if scale else 0.0,
         int(bool(causal)), int(window or 0), _ptr(bias), bh, _ptr(dq), _ptr(dk), _ptr(dv),
-        _ptr(workspace), workspace.numel(), _stream(stream, q), int(flags), *_events(stage_events))
+        _ptr(workspace), workspace.numel(), _stream(stream, q), int(flags), *_events(stage_events),
+        _bands_arg(bias_bands, bias, cu_seqlens_q, cu_seqlens_kv, stream))
     _check(st, "vlf_attn_varlen_bwd")
     return dq, dk, dv
 
@@ -463,6 +508,7 @@ def vlf_attn_varlen_bwd_noalloc(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlen
 
 
 __all__ = ["vlf_attn_varlen_fwd", "vlf_attn_varlen_bwd", "vlf_attn_varlen_bwd_workspace_size",
+           "vlf_bias_bands", "vlf_bias_bands_size",
            "vlf_check_error", "vlf_status_string", "vlf_sched_kv_band", "vlf_sched_q_band",
            "vlf_version", "vlf_launch_count", "vlf_fwd_path", "vlf_bwd_path",
            "vlf_attn_varlen_bwd_noalloc", "vlf_noalloc_scratch_bytes", "VlfError",

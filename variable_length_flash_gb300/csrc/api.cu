@@ -109,6 +109,13 @@ void fill_common(vlf::Params &p, const void *q, const void *k, const void *v, co
   p.flags = flags;
 }
 
+// The bias bands' two tables in the caller's buffer (vlf_bias_bands): rows, then blocks.
+void attach_bands(vlf::Params &p, const void *bands) {
+  if (!bands || !p.bias || p.total_q <= 0) return;
+  p.bias_rows = static_cast<const int4 *>(bands);
+  p.bias_blocks = p.bias_rows + (size_t)p.total_q * (size_t)p.bias_heads;
+}
+
 size_t workspace_bytes_for(int total_q, int h_q, int d_qk, int dtype) {
   if (total_q < 0 || h_q < 1 || d_qk < 1) return 0;
   size_t rowdot = (size_t)h_q * (size_t)total_q * sizeof(float);
@@ -221,7 +228,8 @@ int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
                            int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
                            int h_q, int h_kv, int d_qk, int d_v, int dtype, float scale,
                            int causal, int window, const float *bias, int bias_heads, void *out,
-                           float *lse, vlf_stream_t stream, unsigned flags) {
+                           float *lse, vlf_stream_t stream, unsigned flags,
+                           const void *bias_bands) {
   int st = check_common(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
                         max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, bias, bias_heads);
   if (st != VLF_OK) return st;
@@ -234,6 +242,8 @@ int vlf_attn_varlen_fwd_ex(const void *q, const void *k, const void *v,
               flags);
   p.out = out;
   p.lse = lse;
+  if (!aligned16(bias_bands)) return VLF_ERR_ALIGN;
+  attach_bands(p, bias_bands);
   p.err = error_word_ptr();
   if (!p.err) return VLF_ERR_LAUNCH;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -248,7 +258,7 @@ int vlf_attn_varlen_fwd(const void *q, const void *k, const void *v, const int32
                         int bias_heads, void *out, float *lse, vlf_stream_t stream) {
   return vlf_attn_varlen_fwd_ex(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
                                 max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, scale,
-                                causal, window, bias, bias_heads, out, lse, stream, 0u);
+                                causal, window, bias, bias_heads, out, lse, stream, 0u, nullptr);
 }
 
 int vlf_fwd_num_splits(int num_seqs, int max_seqlen_q, int max_seqlen_kv, int h_q, int h_kv,
@@ -277,13 +287,14 @@ int vlf_attn_varlen_fwd_split(const void *q, const void *k, const void *v,
                               float scale, int causal, int window, const float *bias,
                               int bias_heads, void *out, float *lse, int num_splits,
                               void *workspace, size_t workspace_bytes, vlf_stream_t stream,
-                              unsigned flags) {
+                              unsigned flags, const void *bias_bands) {
   int st = check_common(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
                         max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, bias, bias_heads);
   if (st != VLF_OK) return st;
   if (num_splits < 0) return VLF_ERR_INVALID;
   if (total_q > 0 && !out) return VLF_ERR_INVALID;
-  if (!aligned16(out) || !aligned16(lse) || !aligned16(workspace)) return VLF_ERR_ALIGN;
+  if (!aligned16(out) || !aligned16(lse) || !aligned16(workspace) || !aligned16(bias_bands))
+    return VLF_ERR_ALIGN;
   if (num_seqs == 0 || max_seqlen_q == 0) return VLF_OK;
   vlf::Params p;
   fill_common(p, q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, max_seqlen_q,
@@ -291,6 +302,7 @@ int vlf_attn_varlen_fwd_split(const void *q, const void *k, const void *v,
               flags);
   p.out = out;
   p.lse = lse;
+  attach_bands(p, bias_bands);
   p.err = error_word_ptr();
   if (!p.err) return VLF_ERR_LAUNCH;
   if (num_splits == 0)
@@ -327,7 +339,8 @@ int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
                            int d_v, int dtype, float scale, int causal, int window,
                            const float *bias, int bias_heads, void *dq, void *dk, void *dv,
                            void *workspace, size_t workspace_bytes, vlf_stream_t stream,
-                           unsigned flags, void *const *stage_events, int n_stage_events) {
+                           unsigned flags, void *const *stage_events, int n_stage_events,
+                           const void *bias_bands) {
   if (stage_events && n_stage_events < VLF_BWD_STAGES + 1) return VLF_ERR_INVALID;
   int st = check_common(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
                         max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk, d_v, dtype, bias, bias_heads);
@@ -335,7 +348,7 @@ int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   if (total_q > 0 && (!out || !lse || !dout || !dq)) return VLF_ERR_INVALID;
   if (total_kv > 0 && (!dk || !dv)) return VLF_ERR_INVALID;
   if (!aligned16(out) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
-      !aligned16(dv) || !aligned16(workspace))
+      !aligned16(dv) || !aligned16(workspace) || !aligned16(bias_bands))
     return VLF_ERR_ALIGN;
   const size_t need = workspace_bytes_for(total_q, h_q, d_qk, dtype);
   if (need > 0 && (!workspace || workspace_bytes < need)) return VLF_ERR_WORKSPACE;
@@ -351,6 +364,7 @@ int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.rowdot = static_cast<float *>(workspace);
   p.dq_acc = nullptr;
+  attach_bands(p, bias_bands);
   p.err = error_word_ptr();
   if (!p.err) return VLF_ERR_LAUNCH;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -372,7 +386,7 @@ int vlf_attn_varlen_bwd(const void *q, const void *k, const void *v, const void 
   return vlf_attn_varlen_bwd_ex(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, num_seqs,
                                 total_q, total_kv, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk,
                                 d_v, dtype, scale, causal, window, bias, bias_heads, dq, dk, dv,
-                                workspace, workspace_bytes, stream, 0u, nullptr, 0);
+                                workspace, workspace_bytes, stream, 0u, nullptr, 0, nullptr);
 }
 
 int vlf_attn_varlen_fwd_latent(const void *q_nope, const void *q_rope, const void *k_nope,
@@ -483,6 +497,32 @@ int vlf_attn_varlen_bwd_latent(const void *q_nope, const void *q_rope, const voi
   p.err = error_word_ptr();
   if (!p.err) return VLF_ERR_LAUNCH;
   cudaError_t e = vlf::tc_backward(p, cs, reinterpret_cast<const cudaEvent_t *>(stage_events));
+  return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
+}
+
+size_t vlf_bias_bands_size(int total_q, int bias_heads) {
+  return vlf::bias_bands_bytes(total_q, bias_heads);
+}
+
+int vlf_bias_bands(const float *bias, int bias_heads, const int32_t *cu_seqlens_q,
+                   const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int max_seqlen_kv,
+                   void *bands, size_t bands_bytes, vlf_stream_t stream) {
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_kv < 0 || bias_heads < 1) return VLF_ERR_INVALID;
+  if (num_seqs > 65535) return VLF_ERR_UNSUPPORTED;
+  if (total_q == 0) return VLF_OK;
+  if (!bias || num_seqs == 0 || !cu_seqlens_q || !cu_seqlens_kv) return VLF_ERR_INVALID;
+  if (!aligned16(bias) || !aligned16(bands) || !aligned16(cu_seqlens_q) || !aligned16(cu_seqlens_kv))
+    return VLF_ERR_ALIGN;
+  if (!bands || bands_bytes < vlf::bias_bands_bytes(total_q, bias_heads)) return VLF_ERR_WORKSPACE;
+  vlf::Params p{};
+  p.bias = bias;
+  p.bias_heads = bias_heads;
+  p.cu_q = cu_seqlens_q;
+  p.cu_kv = cu_seqlens_kv;
+  p.num_seqs = num_seqs;
+  p.total_q = total_q;
+  p.max_kv = max_seqlen_kv;
+  const cudaError_t e = vlf::bias_bands(p, bands, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;
 }
 

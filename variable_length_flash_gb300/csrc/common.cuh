@@ -51,6 +51,12 @@ struct Params {
   int rope_heads = 0;
   void *dq_rope = nullptr, *dk_rope = nullptr;
   float *dk_rope_part = nullptr;
+  // bias bands (bias_bands.cu), nullptr when not computed: bias_rows[hb * total_q + r] =
+  // {lo, hi, pure, 0}, the keys [lo, hi) from the first to the last finite bias value of global
+  // query row r and bias head hb, pure = the bias is exactly 0 throughout them (it is then that
+  // interval mask alone); bias_blocks[hb * total_q + q0 + 64 b] the same for the 64-row block b
+  // of the sequence starting at row q0 (union of the intervals, AND of the flags).
+  const int4 *bias_rows = nullptr, *bias_blocks = nullptr;
 };
 
 // ---------------------------------------------------------------- element access

@@ -33,6 +33,10 @@ bool tc_backward_supported(const Params &p);
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev);
 size_t tc_backward_workspace(int total_q, int h_q, int d_qk);
 
+// Bias bands (bias_bands.cu): the buffer size, and the pass that fills it from p.bias.
+size_t bias_bands_bytes(int total_q, int bias_heads);
+cudaError_t bias_bands(const Params &p, void *bands, cudaStream_t st);
+
 // Host-side count of successful kernel launches (api.cu).
 void count_launch(int n = 1);
 // cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes), made once per (kernel, device)

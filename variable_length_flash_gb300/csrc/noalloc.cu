@@ -76,7 +76,7 @@ int vlf_attn_varlen_bwd_noalloc(const void *q, const void *k, const void *v, con
   return vlf_attn_varlen_bwd_ex(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, num_seqs,
                                 total_q, total_kv, max_seqlen_q, max_seqlen_kv, h_q, h_kv, d_qk,
                                 d_v, dtype, scale, causal, window, bias, bias_heads, dq, dk, dv,
-                                scratch, kNoAllocScratchBytes, stream, 0u, nullptr, 0);
+                                scratch, kNoAllocScratchBytes, stream, 0u, nullptr, 0, nullptr);
 }
 
 }  // extern "C"

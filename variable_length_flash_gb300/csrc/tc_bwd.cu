@@ -91,6 +91,10 @@ struct BwdCfg {
   // (dK/dV only)
   static constexpr int PAIRS = KEYS ? IR / 2 : 0;
   static constexpr int OFF_LD = OFF_IN1 + NSTAGE1 * I1_BYTES;
+  // dK/dV with TMA-staged bias: per ring-0 slot the item's rows' finite-bias intervals as IR/2
+  // pairs {lo_c, hi_c, lo_c+1, hi_c+1} (bias bands; pure items are masked by them)
+  static constexpr int BD_BYTES = (KEYS && NBS > 0) ? NSTAGE * PAIRS * 16 : 0;
+  static constexpr int OFF_BD = OFF_LD + NSTAGE * PAIRS * 16;
   // bias ring: per item its 128 x IR fp32 tile as 32-column boxes.  dK/dV: 4 boxes {32 keys, IR
   // query rows}, unswizzled (the 32 keys of a warp read one 128-byte row at a time); dQ: IR / 32
   // boxes {32 keys, 128 query rows}, 128-byte swizzled (each thread reads along its own row).
@@ -99,7 +103,7 @@ struct BwdCfg {
   static constexpr int NBS_ = NBS > 0 ? NBS : 1;  // (a nonzero divisor where there is no ring)
   // (swizzled boxes start 1024-byte aligned, unswizzled ones 128-byte aligned)
   static constexpr int B_ALIGN = KEYS ? 128 : 1024;
-  static constexpr int OFF_B = (OFF_LD + NSTAGE * PAIRS * 16 + B_ALIGN - 1) & ~(B_ALIGN - 1);
+  static constexpr int OFF_B = (OFF_BD + BD_BYTES + B_ALIGN - 1) & ~(B_ALIGN - 1);
   static constexpr int OFF_BAR = OFF_B + NBS * BIAS_STAGE;
   // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE] (ring 0), in1_full[NSTAGE1],
   // in1_empty[NSTAGE1] (ring 1), s_full[NBUF] (S and dP issued:
@@ -113,7 +117,8 @@ struct BwdCfg {
   static constexpr int B_BF = B_QT + 1, B_BE = B_BF + NBS;  // bias full / empty
   static constexpr int NBAR = B_BE + NBS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  // (no alignment slack: the dynamic shared window starts 1024-byte aligned, checked in-kernel)
+  static constexpr int SMEM = OFF_MISC + 16;
   // TMEM: accumulators first, then NBUF x (S IR cols, dP IR cols); kDqS: NBUF S buffers, then
   // one dP buffer.  kDv / kDk: the one accumulator (dV / dK, up to 256 columns) at 0.
   static constexpr uint32_t ACC0 = 0;                       // dV (dK/dV, kDv) or dQ (dQ)
@@ -158,13 +163,14 @@ __global__ void __launch_bounds__(384, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS>;
   static_assert((BIAS == 2) == (NBS > 0), "the bias ring serves TMA-staged bias only");
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int s = blockIdx.z;
   Seq sq;
   if (!load_seq(p, s, sq)) return;
   const int off = sq.kv_len - sq.q_len;
   // the CTA's outer tile and its item range (items start at multiples of IR)
   int tile0, head_outer, hk, n_items, lo = 0, nq_tiles = 0;
+  bool cta_pure = false;  // dQ with bias bands: mask by the rows' intervals, bias not read
   // heads_fast (a head-broadcast bias): grid x enumerates heads, y the 128-row tiles, so that the
   // heads of one tile run together and share its bias tiles in L2
   const int bxr = p.heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
@@ -194,16 +200,63 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       kv_band(tile0, min(tile0 + 128, sq.q_len), sq.q_len, sq.kv_len, p.causal, p.window, klo, khi);
       if (p.flags & VLF_FLAG_NO_SKIP) { klo = 0; khi = sq.kv_len; }
     }
+    // bias bands: only the keys some row of the tile has a finite bias value for (the others
+    // hold masked pairs alone); cta_pure: every row's bias is 0 over its finite interval
+    if (BIAS != 0 && p.bias_blocks && khi > klo) {
+      const int hb = p.bias_heads == 1 ? 0 : head_outer;
+      const int4 *bb = p.bias_blocks + (size_t)hb * p.total_q + sq.q0 + tile0;
+      const int4 e0 = __ldg(bb);
+      int blo = e0.x, bhi = e0.y, pure = e0.z;
+      if (tile0 + 64 < sq.q_len) {
+        const int4 e1 = __ldg(bb + 64);
+        if (e1.y > e1.x) {
+          blo = bhi > blo ? min(blo, e1.x) : e1.x;
+          bhi = max(bhi, e1.y);
+        }
+        pure &= e1.z;
+      }
+      if (bhi > blo) {
+        klo = max(klo, blo);
+        khi = min(khi, bhi);
+      }
+      if (bhi <= blo || khi <= klo) khi = klo;
+      cta_pure = BIAS == 2 && pure != 0;
+    }
     lo = (klo / IR) * IR;
     n_items = khi > klo ? (khi - lo + IR - 1) / IR : 0;
   }
 
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t *gbase = smem_raw + (base - raw);
+  // dK/dV with bias bands: the items (query head, 64-row block) whose rows have a finite bias
+  // value among this tile's keys; the others hold masked pairs alone and are skipped (exact).
+  // Every role walks the candidates in order and counts the kept ones, which index the rings
+  // and buffers; n_kept replaces n_items as the length of the pipeline.
+  const int4 *item_bands = (C::KEYS && BIAS != 0) ? p.bias_blocks : nullptr;
+  auto item_band = [&](int n) -> int4 {
+    const int hb = p.bias_heads == 1 ? 0 : hk * p.group + n / nq_tiles;
+    return __ldg(item_bands + (size_t)hb * p.total_q + sq.q0 + lo + (n % nq_tiles) * IR);
+  };
+  auto item_kept = [&](const int4 &e) { return e.y > e.x && e.x < tile0 + 128 && e.y > tile0; };
+  int n_kept = n_items;
+  if (item_bands) {
+    n_kept = 0;
+    for (int b0 = 0; b0 < n_items; b0 += (int)blockDim.x) {
+      const int n = b0 + (int)threadIdx.x;
+      n_kept += __syncthreads_count(n < n_items && item_kept(item_band(n)));
+    }
+  }
+
+  // The kernel has no static shared memory, so the dynamic window starts 1024-byte aligned, as
+  // the 128-byte swizzle atoms of the TMA tiles and MMA descriptors require; refuse otherwise.
+  const uint32_t base = smem_u32(smem_raw);
+  if (base & 1023u) {
+    if (threadIdx.x == 0) set_error(p.err, VLF_ERR_ALIGN);
+    return;
+  }
+  uint8_t *gbase = smem_raw;
   const uint32_t sO0 = base + C::OFF_O0, sO1 = base + C::OFF_O1;
   const uint32_t sIn0 = base + C::OFF_IN0, sIn1 = base + C::OFF_IN1, sBias = base + C::OFF_B;
   float4 *ldbuf = reinterpret_cast<float4 *>(gbase + C::OFF_LD);  // [stage][IR/2 column pairs]
+  int4 *bdbuf = reinterpret_cast<int4 *>(gbase + C::OFF_BD);      // [stage][IR/2 column pairs]
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
@@ -249,7 +302,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     const bool lat = DQK == 192 && p.latent;
     const int qw = lat ? 128 : DQK;
     const int rh = lat && p.rope_heads == 1 ? 0 : hk;  // the kv head's rope key
-    if (n_items > 0) {
+    if (n_kept > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&maps.outer0);
         tma_prefetch_desc(&maps.outer1);
@@ -279,8 +332,12 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       // (the raw values are kept: no instruction uses them, so nothing waits, until the write)
       constexpr int PPL = C::PAIRS > 0 ? C::PAIRS / 32 : 1;
       float rl[PPL][2], rd[PPL][2];
+      // (dK/dV with bias bands and TMA-staged bias: the rows' finite-bias intervals as well)
+      const bool stage_bands = C::BD_BYTES > 0 && p.bias_rows != nullptr;
+      int rbl[PPL][2], rbh[PPL][2];
       auto load_pairs = [&](int n) {
         const int h = item_head(n), i0 = item_row(n);
+        const int hb = p.bias_heads == 1 ? 0 : h;
 #pragma unroll
         for (int pp = 0; pp < PPL; ++pp) {
 #pragma unroll
@@ -288,24 +345,44 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             const int qi = i0 + 2 * (lane + 32 * pp) + u;
             rl[pp][u] = -INFINITY;
             rd[pp][u] = 0.f;
+            rbl[pp][u] = rbh[pp][u] = 0;
             if (qi < sq.q_len) {
               const size_t gi = (size_t)h * p.total_q + sq.q0 + qi;
               rl[pp][u] = __ldg(p.lse + gi);
               rd[pp][u] = __ldg(p.rowdot + gi);
+              if (stage_bands) {
+                const int4 e = __ldg(p.bias_rows + (size_t)hb * p.total_q + sq.q0 + qi);
+                rbl[pp][u] = e.x;
+                rbh[pp][u] = e.y;
+              }
             }
           }
         }
       };
-      if (C::KEYS) load_pairs(0);
-      for (int n = 0; n < n_items; ++n) {
-        const int st = n % NSTAGE, st1 = n % NSTAGE1;
-        if (BIAS == 2) {
-          // the item's bias tile (needed last, by the compute warps; its slot frees earliest)
-          const int bs = n % C::NBS_;
+      // the next kept candidate item at or after n (every candidate without bias bands)
+      auto next_kept = [&](int n) {
+        if (item_bands)
+          while (n < n_items && !item_kept(item_band(n))) ++n;
+        return n;
+      };
+      int n = next_kept(0);
+      if (C::KEYS && n < n_items) load_pairs(n);
+      for (int k = 0; n < n_items; ++k) {
+        const int st = k % NSTAGE, st1 = k % NSTAGE1;
+        const int n_next = next_kept(n + 1);
+        if (BIAS == 2 && !cta_pure) {
+          // the item's bias tile (needed last, by the compute warps; its slot frees earliest);
+          // an item whose rows' bias is 0 over their intervals (pure) needs no tile: its slot
+          // is passed along without a copy
+          const bool pure_item = item_bands && p.bias_rows && item_band(n).z != 0;
+          const int bs = k % C::NBS_;
           bool wb = true;
           if (lane == 0) {
-            if (n >= C::NBS_) wb = mbar_wait(bar(C::B_BE + bs), ((n / C::NBS_) - 1) & 1, abort_flag, p.err);
-            if (wb) {
+            if (k >= C::NBS_) wb = mbar_wait(bar(C::B_BE + bs), ((k / C::NBS_) - 1) & 1, abort_flag, p.err);
+            if (wb && pure_item) {
+              mbar_arrive(bar(C::B_BF + bs));
+              ++issuedb[bs];
+            } else if (wb) {
               const uint32_t dst = sBias + bs * C::BIAS_STAGE;
               mbar_expect_tx(bar(C::B_BF + bs), C::BIAS_STAGE);
               // bias columns: bias head * max_seqlen_kv + sequence-local key; rows: global query
@@ -327,9 +404,9 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           }
           if (!__shfl_sync(0xffffffffu, (int)wb, 0)) break;
         }
-        if (n >= NSTAGE) {
+        if (k >= NSTAGE) {
           bool w = true;
-          if (lane == 0) w = mbar_wait(bar(C::B_IE + st), ((n / NSTAGE) - 1) & 1, abort_flag, p.err);
+          if (lane == 0) w = mbar_wait(bar(C::B_IE + st), ((k / NSTAGE) - 1) & 1, abort_flag, p.err);
           if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
         }
         if (C::KEYS) {
@@ -339,8 +416,10 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) nl[u] = rl[pp][u] == -INFINITY ? -INFINITY : -rl[pp][u] * kLog2e;
             ldbuf[st * C::PAIRS + lane + 32 * pp] = make_float4(nl[0], nl[1], -rd[pp][0], -rd[pp][1]);
+            if (stage_bands)
+              bdbuf[st * C::PAIRS + lane + 32 * pp] = make_int4(rbl[pp][0], rbh[pp][0], rbl[pp][1], rbh[pp][1]);
           }
-          if (n + 1 < n_items) load_pairs(n + 1);  // (consumed next iteration)
+          if (n_next < n_items) load_pairs(n_next);  // (consumed next iteration)
         }
         const int ih = C::KEYS ? item_head(n) : hk;  // head inside the inner tensors
         const int irow = (C::KEYS ? sq.q0 : sq.k0) + item_row(n);
@@ -359,7 +438,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         mbar_arrive(bar(C::B_IF + st));
         bool w1 = true;
         if (lane == 0) {
-          if (n >= NSTAGE1) w1 = mbar_wait(bar(C::B_IE1 + st1), ((n / NSTAGE1) - 1) & 1, abort_flag, p.err);
+          if (k >= NSTAGE1) w1 = mbar_wait(bar(C::B_IE1 + st1), ((k / NSTAGE1) - 1) & 1, abort_flag, p.err);
           if (w1) {
             mbar_expect_tx(bar(C::B_IF1 + st1), C::I1_BYTES);
             for (int c = 0; c < C::KB1; ++c)
@@ -369,6 +448,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           }
         }
         if (!__shfl_sync(0xffffffffu, (int)w1, 0)) break;
+        n = n_next;
       }
       if (lane == 0) {
         drain_wait(bar(C::B_OUT), 0);
@@ -388,7 +468,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     // the pipe idle; split, each waits only for what its own products need.  Each runs its
     // loop as a whole converged warp (uniform operands) and elect.sync picks the issuing lane.
     const int role = warp == 1 ? 0 : (warp == 11 ? 1 : 2);  // 0: S, 1: dP, 2: accumulations
-    if (n_items > 0 && (C::HAS_DP || role != 1)) {  // (kDv: no dP products)
+    if (n_kept > 0 && (C::HAS_DP || role != 1)) {  // (kDv: no dP products)
       // S / dP: M = 128 outer rows, N = IR inner rows, both operands K-major
       const uint32_t id_sp = idesc_f16(is_bf16, 128, IR, 0, 0);
       // accumulations: A from TMEM (K = IR inner rows), B = inner tile MN-major
@@ -446,7 +526,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         // products of item m, once its inner tile has landed and its TMEM columns are free
         // (QT: once the compute warps have copied the outer rows into TMEM)
         ok = wait_all(C::QT ? C::B_QT : C::B_OUT, 0);
-        for (int m = 0; m < n_items && ok; ++m) {
+        for (int m = 0; m < n_kept && ok; ++m) {
           const int b = m % NBUF;
           // S reads ring 0 (Q or K), dP reads ring 1 (dO or V)
           ok = role == 0 ? wait_all(C::B_IF + m % NSTAGE, (m / NSTAGE) & 1)
@@ -479,7 +559,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           if (!C::HAS_DV && role == 1) mma_commit_w(bar(C::B_IE1 + m % NSTAGE1));
         }
       } else {
-        for (int n = 0; n < n_items && ok; ++n) {
+        for (int n = 0; n < n_kept && ok; ++n) {
           const int b = n % NBUF;
           ok = wait_all(C::B_P + b, (n / NBUF) & 1);
           if (!ok) break;
@@ -517,7 +597,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     int vis_lo, vis_hi;
     if (C::KEYS) visible_rows(orow, off, sq.q_len, p.causal, p.window, vis_lo, vis_hi);
     else visible_range(orow, off, sq.kv_len, p.causal, p.window, vis_lo, vis_hi);
-    if (!orow_ok) vis_hi = vis_lo;
+    if (!C::KEYS && cta_pure && orow_ok) {
+      // dQ over rows whose bias is 0 on its finite interval: that interval masks the keys
+      const int hb = p.bias_heads == 1 ? 0 : head_outer;
+      const int4 e = __ldg(p.bias_rows + (size_t)hb * p.total_q + sq.q0 + orow);
+      vis_lo = max(vis_lo, e.x);
+      vis_hi = min(vis_hi, e.y);
+    }
+    if (!orow_ok || vis_hi < vis_lo) vis_hi = vis_lo;
     float row_nl = -INFINITY, row_nd = 0.f;  // dQ: this row's -LSE (base 2) and -D
     const float *brow_dq = nullptr;
     if (!C::KEYS && orow_ok) {
@@ -531,7 +618,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       }
     }
     bool ok = true;
-    if (C::QT && n_items > 0) {
+    if (C::QT && n_kept > 0) {
       // this thread's row of the outer Q (first half of the compute warps) or dO tile (second
       // half), 16 bytes at a time from its 128-byte-swizzled blocks, into the A-operand columns
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_OUT), 0, abort_flag, p.err));
@@ -553,14 +640,27 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       fence_before();
       mbar_arrive(bar(C::B_QT));
     }
-    for (int n = 0; n < n_items && ok; ++n) {
-      const int b = n % NBUF, st = n % NSTAGE;
+    for (int n = 0, kept = 0; n < n_items && ok; ++n) {
+      // n: the candidate item (which query head and rows, dK/dV; which keys, dQ); it: its place
+      // in the pipeline (rings, buffers, barrier phases)
+      bool ipure = false;
+      if (item_bands) {
+        const int4 e = item_band(n);
+        if (!item_kept(e)) continue;
+        ipure = BIAS == 2 && p.bias_rows != nullptr && e.z != 0;
+      }
+      const int it = kept++;
+      // bias values enter the logits (TMA-staged or read row by row), unless this item's or
+      // this CTA's rows are all pure intervals
+      const bool use_vals = BIAS == 1 || (BIAS == 2 && !ipure && !cta_pure);
+      const int b = it % NBUF, st = it % NSTAGE;
       const int h = item_head(n);
-      bool w = mbar_wait(bar(C::B_S + b), (n / NBUF) & 1, abort_flag, p.err);
+      bool w = mbar_wait(bar(C::B_S + b), (it / NBUF) & 1, abort_flag, p.err);
       // the LSE / D pairs were written by the producer lanes before their arrive on in_full:
       // acquire that barrier too before reading them
-      if (C::KEYS && w) w = mbar_wait(bar(C::B_IF + st), (n / NSTAGE) & 1, abort_flag, p.err);
-      if (BIAS == 2 && w) w = mbar_wait(bar(C::B_BF + n % C::NBS_), (n / C::NBS_) & 1, abort_flag, p.err);
+      if (C::KEYS && w) w = mbar_wait(bar(C::B_IF + st), (it / NSTAGE) & 1, abort_flag, p.err);
+      if (BIAS == 2 && !cta_pure && w)
+        w = mbar_wait(bar(C::B_BF + it % C::NBS_), (it / C::NBS_) & 1, abort_flag, p.err);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       fence_after();
@@ -595,12 +695,27 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
                   (p.window <= 0 || i0 >= i + off - p.window + 1);
         }
         plain = plain && BIAS != 1;
+        // dK/dV, a pure item: the columns (query rows) whose finite-bias interval holds this key
+        unsigned bmask = 0xffffffffu;
+        if (C::BD_BYTES > 0 && ipure) {
+          const int4 *bp = bdbuf + st * C::PAIRS + col0 / 2;
+          bmask = 0u;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int4 bb = bp[e];
+            bmask |= (unsigned)(bb.x <= orow && orow < bb.y) << (2 * e);
+            bmask |= (unsigned)(bb.z <= orow && orow < bb.w) << (2 * e + 1);
+          }
+          plain = plain && bmask == 0xffffffffu;
+        }
+        // dQ over pure rows: the chunk's keys must all lie in this row's interval
+        if (!C::KEYS && cta_pure) plain = plain && i0 >= vis_lo && i0 + 31 < vis_hi;
         const float4 *lp = ldbuf + st * C::PAIRS + col0 / 2;  // this chunk's 16 pairs (dK/dV)
         // TMA-staged bias: the chunk's 32 values of this thread -- dQ: along its row, from the
         // chunk's swizzled box; dK/dV: down its key's column, one 128-byte box row per query row
         float bq4[32];
-        if (BIAS == 2) {
-          const uint32_t bstage = sBias + (n % C::NBS_) * C::BIAS_STAGE;
+        if (BIAS == 2 && use_vals) {
+          const uint32_t bstage = sBias + (it % C::NBS_) * C::BIAS_STAGE;
           if (C::KEYS) {
             const uint32_t bcol = bstage + quarter * C::BIAS_BOX + lane * 4 + col0 * 128;
 #pragma unroll
@@ -633,7 +748,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
             uint64_t x2 = fma2(f2pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl22,
                                f2pack(q4.x, q4.y));
-            if (BIAS == 2) x2 = fma2(f2pack(bq4[c], bq4[c + 1]), lg22, x2);
+            if (BIAS == 2 && use_vals) x2 = fma2(f2pack(bq4[c], bq4[c + 1]), lg22, x2);
             const float2 x = f2unpack(x2);
             const float pa = ex2(x.x), pb = ex2(x.y);
             const uint64_t p2 = f2pack(pa, pb);
@@ -667,7 +782,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
               const int cc = i0 + c + u;  // sequence-local column: query row (dK/dV) or key (dQ)
               float x = __uint_as_float(sv[c + u]) * sl2;
               if (BIAS == 2) {
-                x = fmaf(bq4[c + u], kLog2e, x);
+                if (use_vals) x = fmaf(bq4[c + u], kLog2e, x);
               } else if (BIAS == 1 && brow) {
                 // element by element unless the chunk was loaded 16 bytes at a time (bq4),
                 // clamped into the sequence so that masked columns read a valid address
@@ -676,7 +791,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
                                      : (bvec ? bq4[c + u] : __ldg(brow + min(cc, sq.kv_len - 1)));
                 x = fmaf(bv, kLog2e, x);
               }
-              xs[u] = (cc >= vis_lo && cc < vis_hi) ? x : -INFINITY;
+              xs[u] = (cc >= vis_lo && cc < vis_hi && ((bmask >> (c + u)) & 1u)) ? x : -INFINITY;
             }
             // masked logits (-inf) and rows without keys (-LSE2 = -inf) give P = 0
             const float2 x = f2unpack(add2(f2pack(xs[0], xs[1]), f2pack(q4.x, q4.y)));
@@ -692,14 +807,14 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         if (C::KEYS && C::HAS_DV) tmem_st16(s_addr, pk);          // P^T for dV
         if (C::HAS_DP) tmem_st16(MODE == kDqS ? s_addr : dp_addr, dk);  // dS (dK/dV: dS^T)
       }
-      if (BIAS == 2) mbar_arrive(bar(C::B_BE + n % C::NBS_));  // the bias slot may be refilled
+      if (BIAS == 2 && !cta_pure) mbar_arrive(bar(C::B_BE + it % C::NBS_));  // the slot may be refilled
       tmem_st_wait();
       fence_before();
       mbar_arrive(bar(C::B_P + b));
     }
     // epilogue: the last item's last accumulation completes every MMA of the CTA
-    if (ok && n_items > 0)
-      ok = mbar_wait(bar(C::B_D + (n_items - 1) % NBUF), ((n_items - 1) / NBUF) & 1, abort_flag, p.err);
+    if (ok && n_kept > 0)
+      ok = mbar_wait(bar(C::B_D + (n_kept - 1) % NBUF), ((n_kept - 1) / NBUF) & 1, abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
     // Outputs of a full 128-row tile whose widths are whole 64-column blocks leave through TMA:
     // each thread writes its row into the idle outer-tile shared memory in the 128-byte-swizzled
@@ -717,7 +832,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 #pragma unroll 1
         for (int ch = 0; ch < ncols / 32; ++ch) {
           uint32_t v[32];
-          if (n_items > 0) {
+          if (n_kept > 0) {
             __syncwarp();
             tmem_ld32(lane_addr + tcol + ch * 32, v);
             tmem_ld_wait();
@@ -755,7 +870,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
 #pragma unroll 1
         for (int ch = 0; ch < ncols / 32; ++ch) {
           uint32_t v[32];
-          if (n_items > 0) {
+          if (n_kept > 0) {
             __syncwarp();
             tmem_ld32(lane_addr + tcol + ch * 32, v);
             tmem_ld_wait();

@@ -198,6 +198,35 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     ti.jlo[0] = ti.lo = a;
     ti.jhi[0] = ti.hi = b;
   }
+  // Bias bands: the KV tiles in which some row of the tile has a finite bias value (the others
+  // hold only masked pairs: skipping them is exact); cta_pure: every row's bias is 0 over its
+  // finite interval, so the tile is masked by those intervals and the bias is not read.
+  bool cta_pure = false;
+  if constexpr (BIAS != 0 && NT == 1 && !PACK && !SPLIT) {
+    if (p.bias_blocks && ti.hi > ti.lo) {
+      const int hb = p.bias_heads == 1 ? 0 : ti.head[0];
+      const int4 *bb = p.bias_blocks + (size_t)hb * p.total_q + sq.q0 + ti.row0[0];
+      const int4 e0 = __ldg(bb);
+      int blo = e0.x, bhi = e0.y, pure = e0.z;
+      if (ti.row0[0] + 64 < sq.q_len) {
+        const int4 e1 = __ldg(bb + 64);
+        if (e1.y > e1.x) {
+          blo = bhi > blo ? min(blo, e1.x) : e1.x;
+          bhi = max(bhi, e1.y);
+        }
+        pure &= e1.z;
+      }
+      int jl = ti.lo, jh = ti.hi;
+      if (bhi > blo) {
+        jl = max(jl, blo / kBN);
+        jh = min(jh, (bhi + kBN - 1) / kBN);
+      }
+      if (bhi <= blo || jh <= jl) jl = jh = 0;
+      ti.jlo[0] = ti.lo = jl;
+      ti.jhi[0] = ti.hi = jh;
+      cta_pure = pure != 0;
+    }
+  }
 
   // The kernel has no static shared memory, so the dynamic window starts 1024-byte aligned, as
   // the 128-byte swizzle atoms of the TMA tiles and MMA descriptors require; refuse otherwise.
@@ -283,7 +312,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       bool ok = true;
       for (int j = lo; j < hi + C::LEAD && ok; ++j) {
         const int kj = j, vj = j - C::LEAD;  // K tile issued ahead of V by LEAD
-        if (BIAS == 2 && kj < hi) {
+        if (BIAS == 2 && kj < hi && !cta_pure) {
           // the query tile's bias columns of KV tile kj: rows row0 .. row0 + 127
           const int it = kj - lo, bs = it % C::NBS_;
           if (it >= C::NBS_) ok = mbar_wait(bar(C::B_BE + bs), ((it / C::NBS_) - 1) & 1, abort_flag, p.err);
@@ -420,10 +449,19 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
     const uint32_t s_addr = lane_addr + 128 * t, o_addr = lane_addr + C::O_COL + 128 * t;
     const float sl2 = p.scale_log2;
     const float *brow = nullptr;
-    if (BIAS && row_ok) {
+    if (BIAS && row_ok && !cta_pure) {
       const int bh = p.bias_heads == 1 ? 0 : head;
       brow = p.bias + ((size_t)(sq.q0 + i) * (size_t)p.bias_heads + (size_t)bh) * (size_t)p.max_kv;
     }
+    // a pure CTA: this row's finite-bias interval, intersected with its causal / window range
+    int rlo = 0, rhi = sq.kv_len;
+    if (BIAS && cta_pure && row_ok) {
+      const int bh = p.bias_heads == 1 ? 0 : head;
+      const int4 e = __ldg(p.bias_rows + (size_t)bh * p.total_q + sq.q0 + i);
+      rlo = e.x;
+      rhi = e.y;
+    }
+    const bool bias_vals = BIAS && !cta_pure;  // bias values are added to the logits
     // l: sum of the rounded P the MMA multiplies (normalises O); lf: the fp32 sum (for LSE)
     float m_ref = -INFINITY, l = 0.f, lf = 0.f;
     const int jlo = ti.jlo[t], jhi = ti.jhi[t];
@@ -436,8 +474,8 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       const uint32_t sb = s_addr + 64 * b;
       const int kb = j * kBN;
       const bool full = row_ok && (kb + kBN - 1 < sq.kv_len) && (!p.causal || kb + kBN - 1 <= i + off) &&
-                        (p.window <= 0 || kb >= i + off - p.window + 1);
-      const bool plain = full && !BIAS;
+                        (p.window <= 0 || kb >= i + off - p.window + 1) && kb >= rlo && kb + kBN <= rhi;
+      const bool plain = full && !bias_vals;
       // the whole S row (64 fp32) in registers: two TMEM loads, one wait
       uint32_t v[kBN];
       __syncwarp();
@@ -514,12 +552,17 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           // the visible keys of this row are one interval: mask by two compares per element
           int vlo, vhi;
           visible_range(i, off, sq.kv_len, p.causal, p.window, vlo, vhi);
+          vlo = max(vlo, rlo);
+          vhi = min(vhi, rhi);
           if (!row_ok) vhi = vlo;
           const int elo = vlo - kb, ehi = vhi - kb;
           // logits in base 2; the bias row is read 16 bytes at a time when its address allows
           // and the tile lies inside it, else element by element (the column clamped into the
           // row: masked elements read a valid address)
-          if (BIAS == 2) {
+          if (!bias_vals) {
+#pragma unroll
+            for (int e = 0; e < kBN; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * sl2);
+          } else if (BIAS == 2) {
             // the tile's bias, staged by the producer: this row of the two 32-column boxes
             // (128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r mod 8))
             const int it = j - jlo, bs = it % C::NBS_;

@@ -19,7 +19,8 @@ from __future__ import annotations
 import torch
 
 from . import (VLF_ERR_INVALID, VLF_ERR_UNSUPPORTED, VlfError, vlf_attn_varlen_bwd,
-               vlf_attn_varlen_bwd_latent, vlf_attn_varlen_fwd, vlf_attn_varlen_fwd_latent)
+               vlf_attn_varlen_bwd_latent, vlf_attn_varlen_fwd, vlf_attn_varlen_fwd_latent,
+               vlf_bias_bands)
 
 
 def mask_to_bias(mask: torch.Tensor) -> torch.Tensor:
@@ -48,11 +49,13 @@ class _VarlenAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_seqlen_kv, scale,
                 causal, window, bias):
+        # the bias bands (which keys the bias leaves each row) serve the forward and backward
+        bands = None if bias is None else vlf_bias_bands(bias, cu_seqlens_q, cu_seqlens_kv)
         out, lse = vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q,
                                        max_seqlen_kv, scale=scale, causal=causal, window=window,
-                                       bias=bias)
+                                       bias=bias, bias_bands=bands)
         ctx.save_for_backward(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv)
-        ctx.bias = bias
+        ctx.bias, ctx.bands = bias, bands
         ctx.args = (max_seqlen_q, max_seqlen_kv, scale, causal, window)
         return out
 
@@ -62,7 +65,7 @@ class _VarlenAttention(torch.autograd.Function):
         max_q, max_kv, scale, causal, window = ctx.args
         dq, dk, dv = vlf_attn_varlen_bwd(dout.contiguous(), q, k, v, out, lse, cu_q, cu_kv,
                                          max_q, max_kv, scale=scale, causal=causal,
-                                         window=window, bias=ctx.bias)
+                                         window=window, bias=ctx.bias, bias_bands=ctx.bands)
         return dq, dk, dv, None, None, None, None, None, None, None, None
 
 
