@@ -234,7 +234,12 @@ int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
  * tensor, unmodified since): stale bands give wrong results.
  *   bias, bias_heads, cu_seqlens_q / _kv, num_seqs, total_q, max_seqlen_kv   as in the forward
  *   bands        device buffer of at least vlf_bias_bands_size(total_q, bias_heads) bytes,
- *                16-byte aligned, owned by the caller, written
+ *                16-byte aligned, owned by the caller, written: two int32x4 tables of
+ *                [bias_heads][total_q] entries -- per row {lo, hi, pure, 0} (keys [lo, hi) from
+ *                the first to the last finite value, lo = hi = 0 if none; pure 1 when the bias
+ *                is 0 throughout them), then per 64-row block of each sequence, at the block's
+ *                first row, {lo, hi, ilo, ihi}: the union of its rows' intervals and, when all
+ *                its rows are pure, their intersection (-1, -1 otherwise)
  * Enqueued on `stream`; no synchronisation.  Returns VLF_OK or a negative status (invalid
  * arguments, VLF_ERR_WORKSPACE for a missing or short buffer).
  */

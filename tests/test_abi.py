@@ -119,16 +119,18 @@ def test_noalloc_array_holds_a_problem_at_its_limit():
 
 def test_path_queries():
     """Which kernel family a shape gets (host-only): 16-bit widths 64/96/128/192-128/256 and
-    fp32 widths 32/64 on the tensor cores, everything else (and VLF_FLAG_FORCE_SIMT) on the
-    SIMT fp32-FMA kernels."""
+    fp32 widths 32/64 (forward and backward) on the tensor cores, everything else (and
+    VLF_FLAG_FORCE_SIMT) on the SIMT fp32-FMA kernels."""
     for d, dv in ((64, 64), (96, 96), (128, 128), (192, 128), (256, 256)):
         for dt in (vlf.VLF_F16, vlf.VLF_BF16):
             assert vlf.vlf_fwd_path(8, 2, d, dv, dt) == 1
             assert vlf.vlf_bwd_path(8, 2, d, dv, dt) == 1
     for d in (32, 64):
         assert vlf.vlf_fwd_path(8, 2, d, d, vlf.VLF_F32) == 1
+        assert vlf.vlf_bwd_path(8, 2, d, d, vlf.VLF_F32) == 1
     for d, dv in ((128, 128), (40, 24), (96, 96)):
         assert vlf.vlf_fwd_path(8, 2, d, dv, vlf.VLF_F32) == 0
+        assert vlf.vlf_bwd_path(8, 2, d, dv, vlf.VLF_F32) == 0
     assert vlf.vlf_fwd_path(8, 2, 64, 64, vlf.VLF_F32, flags=vlf.VLF_FLAG_FORCE_SIMT) == 0
     assert vlf.vlf_fwd_path(8, 2, 80, 48, vlf.VLF_BF16) == 0
     assert vlf.vlf_fwd_path(3, 2, 64, 64, vlf.VLF_BF16) == vlf.VLF_ERR_INVALID

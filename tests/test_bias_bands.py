@@ -33,10 +33,15 @@ def band_definition(bias, cu_q, cu_kv):
                     lo, hi = int(fin[0]), int(fin[-1]) + 1
                     rows[h, r] = (lo, hi, int(np.all(vals[lo:hi] == 0.0)))
             for r0 in range(q0, q1, 64):
+                # union of the rows' intervals; their intersection when all are pure, else -1s
                 ent = rows[h, r0:min(r0 + 64, q1)]
                 live = ent[ent[:, 1] > ent[:, 0]]
                 lo, hi = (int(live[:, 0].min()), int(live[:, 1].max())) if live.size else (0, 0)
-                blocks[(h, r0)] = (lo, hi, int(ent[:, 2].all()))
+                if ent[:, 2].all():
+                    ilo, ihi = int(ent[:, 0].max()), int(ent[:, 1].min())
+                    blocks[(h, r0)] = (lo, hi, ilo, max(ihi, ilo))
+                else:
+                    blocks[(h, r0)] = (lo, hi, -1, -1)
     return rows, blocks
 
 
@@ -86,7 +91,7 @@ def test_bands_match_definition(kind):
     rows, blocks = band_definition(bias, cu_q.tolist(), cu_kv.tolist())
     np.testing.assert_array_equal(got[0, :, :, :3], rows)
     for (h, r0), e in blocks.items():
-        assert tuple(got[1, h, r0, :3]) == e, (h, r0, got[1, h, r0], e)
+        assert tuple(got[1, h, r0]) == e, (h, r0, got[1, h, r0], e)
 
 
 CASES = [

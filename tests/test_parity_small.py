@@ -193,19 +193,20 @@ def test_tile_skipping_is_exact(name, simt):
         assert torch.equal(a[k], b[k]), k
 
 
-def test_fp32_tensor_core_forward_is_taken_and_matches_simt():
-    """fp32 at widths 32 / 64 runs the three-pass tf32 forward; it and the SIMT fp32-FMA forward
-    both meet the fp32 gate against the oracle."""
+def test_fp32_tensor_core_path_is_taken_and_matches_simt():
+    """fp32 at widths 32 / 64 runs the three-pass tf32 forward and backward; they and the SIMT
+    fp32-FMA kernels all meet the fp32 gates against the oracle."""
     import variable_length_flash_gb300 as vlf
     for d in (32, 64):
         assert vlf.vlf_fwd_path(4, 2, d, d, vlf.VLF_F32) == 1
+        assert vlf.vlf_bwd_path(4, 2, d, d, vlf.VLF_F32) == 1
         assert vlf.vlf_fwd_path(4, 2, d, d, vlf.VLF_F32, flags=vlf.VLF_FLAG_FORCE_SIMT) == 0
     w = CASES["fp32_d64_odd_gqa"]
-    x = W.make_inputs(w, seed=31, with_dout=False)
-    ref = oracle_run(w, x, backward=False)
+    x = W.make_inputs(w, seed=31, with_dout=True)
+    ref = oracle_run(w, x)
     for flags in (0, vlf.VLF_FLAG_FORCE_SIMT):
-        gpu = gpu_run(w, x, flags=flags, backward=False)
-        assert_within(compare(w, gpu, ref), f"fp32 forward flags={flags}")
+        gpu = gpu_run(w, x, flags=flags)
+        assert_within(compare(w, gpu, ref), f"fp32 flags={flags}")
 
 
 @pytest.mark.parametrize("name", ["bf16_d128_gqa_causal_odd", "bf16_latent_192_128",

@@ -192,7 +192,8 @@ int vlf_bwd_path(int h_q, int h_kv, int d_qk, int d_v, int dtype, int bias_heads
     return VLF_ERR_INVALID;
   if (d_qk > 256 || d_v > 256) return VLF_ERR_UNSUPPORTED;
   vlf::Params p = shape_params(h_q, h_kv, d_qk, d_v, dtype, bias_heads, flags);
-  return (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_backward_supported(p)) ? 1 : 0;
+  return (!(flags & VLF_FLAG_FORCE_SIMT) &&
+          (vlf::tc_backward_supported(p) || vlf::tc_backward32_supported(p))) ? 1 : 0;
 }
 
 const char *vlf_status_string(int status) {
@@ -371,6 +372,8 @@ int vlf_attn_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   cudaError_t e;
   if (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_backward_supported(p))
     e = vlf::tc_backward(p, cs, ev);
+  else if (!(flags & VLF_FLAG_FORCE_SIMT) && vlf::tc_backward32_supported(p))
+    e = vlf::tc_backward32(p, cs, ev);
   else
     e = vlf::simt_backward(p, cs, ev);
   return e == cudaSuccess ? VLF_OK : VLF_ERR_LAUNCH;

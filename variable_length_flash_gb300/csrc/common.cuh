@@ -54,8 +54,9 @@ struct Params {
   // bias bands (bias_bands.cu), nullptr when not computed: bias_rows[hb * total_q + r] =
   // {lo, hi, pure, 0}, the keys [lo, hi) from the first to the last finite bias value of global
   // query row r and bias head hb, pure = the bias is exactly 0 throughout them (it is then that
-  // interval mask alone); bias_blocks[hb * total_q + q0 + 64 b] the same for the 64-row block b
-  // of the sequence starting at row q0 (union of the intervals, AND of the flags).
+  // interval mask alone); bias_blocks[hb * total_q + q0 + 64 b] = {lo, hi, ilo, ihi} for the
+  // 64-row block b of the sequence starting at row q0: the union of the rows' intervals and, when
+  // all are pure, their intersection (else ilo = ihi = -1).
   const int4 *bias_rows = nullptr, *bias_blocks = nullptr;
 };
 

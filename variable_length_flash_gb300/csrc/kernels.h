@@ -30,6 +30,9 @@ int fwd_num_splits(int num_seqs, int max_q, int max_kv, int h_q, int h_kv, int d
 bool tc_forward32_supported(const Params &p);
 cudaError_t tc_forward32(const Params &p, cudaStream_t st);
 bool tc_backward_supported(const Params &p);
+// fp32 backward on the tensor cores, three tf32 passes (tc_bwd32.cu): head widths 32 and 64.
+bool tc_backward32_supported(const Params &p);
+cudaError_t tc_backward32(const Params &p, cudaStream_t st, const cudaEvent_t *ev);
 cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev);
 size_t tc_backward_workspace(int total_q, int h_q, int d_qk);
 

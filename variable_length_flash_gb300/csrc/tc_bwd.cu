@@ -93,8 +93,12 @@ struct BwdCfg {
   static constexpr int OFF_LD = OFF_IN1 + NSTAGE1 * I1_BYTES;
   // dK/dV with TMA-staged bias: per ring-0 slot the item's rows' finite-bias intervals as IR/2
   // pairs {lo_c, hi_c, lo_c+1, hi_c+1} (bias bands; pure items are masked by them)
-  static constexpr int BD_BYTES = (KEYS && NBS > 0) ? NSTAGE * PAIRS * 16 : 0;
+  static constexpr int BD_BYTES = KEYS ? NSTAGE * PAIRS * 16 : 0;
   static constexpr int OFF_BD = OFF_LD + NSTAGE * PAIRS * 16;
+  // dK/dV: per ring-0 slot the kept item's candidate index and flags (1: its rows are pure
+  // 0 / -inf intervals, 2: every row sees every key of the tile) for the compute warps
+  static constexpr int IS_BYTES = KEYS ? NSTAGE * 8 : 0;
+  static constexpr int OFF_IS = OFF_BD + BD_BYTES;
   // bias ring: per item its 128 x IR fp32 tile as 32-column boxes.  dK/dV: 4 boxes {32 keys, IR
   // query rows}, unswizzled (the 32 keys of a warp read one 128-byte row at a time); dQ: IR / 32
   // boxes {32 keys, 128 query rows}, 128-byte swizzled (each thread reads along its own row).
@@ -103,7 +107,7 @@ struct BwdCfg {
   static constexpr int NBS_ = NBS > 0 ? NBS : 1;  // (a nonzero divisor where there is no ring)
   // (swizzled boxes start 1024-byte aligned, unswizzled ones 128-byte aligned)
   static constexpr int B_ALIGN = KEYS ? 128 : 1024;
-  static constexpr int OFF_B = (OFF_BD + BD_BYTES + B_ALIGN - 1) & ~(B_ALIGN - 1);
+  static constexpr int OFF_B = (OFF_IS + IS_BYTES + B_ALIGN - 1) & ~(B_ALIGN - 1);
   static constexpr int OFF_BAR = OFF_B + NBS * BIAS_STAGE;
   // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE] (ring 0), in1_full[NSTAGE1],
   // in1_empty[NSTAGE1] (ring 1), s_full[NBUF] (S and dP issued:
@@ -155,12 +159,12 @@ struct BwdCfg {
 // BF16: element type of the 16-bit tensors (bf16, else fp16), fixed at compile time so the
 // per-element conversions carry no runtime branch.
 // BIAS: 0 none; 1 the compute threads load their bias values from global memory; 2 the producer
-// stages each item's bias tile through the NBS-stage ring (a separate instantiation each, so that
-// kernels without a bias carry none of its code or registers).
+// stages each item's bias tile through the NBS-stage ring; 3 a bias whose rows (those this CTA
+// works on) are all 0 / -inf intervals: masked by the bias bands, no bias value read (a separate
+// instantiation each, so that kernels without a bias carry none of its code or registers).
 template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS, bool BF16,
           int BIAS>
-__global__ void __launch_bounds__(384, 1)
-tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
+__device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p) {
   using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS>;
   static_assert((BIAS == 2) == (NBS > 0), "the bias ring serves TMA-staged bias only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -206,21 +210,21 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       const int hb = p.bias_heads == 1 ? 0 : head_outer;
       const int4 *bb = p.bias_blocks + (size_t)hb * p.total_q + sq.q0 + tile0;
       const int4 e0 = __ldg(bb);
-      int blo = e0.x, bhi = e0.y, pure = e0.z;
+      int blo = e0.x, bhi = e0.y, pure = e0.z >= 0;
       if (tile0 + 64 < sq.q_len) {
         const int4 e1 = __ldg(bb + 64);
         if (e1.y > e1.x) {
           blo = bhi > blo ? min(blo, e1.x) : e1.x;
           bhi = max(bhi, e1.y);
         }
-        pure &= e1.z;
+        pure &= e1.z >= 0;
       }
       if (bhi > blo) {
         klo = max(klo, blo);
         khi = min(khi, bhi);
       }
       if (bhi <= blo || khi <= klo) khi = klo;
-      cta_pure = BIAS == 2 && pure != 0;
+      cta_pure = (BIAS == 2 || BIAS == 3) && pure != 0;
     }
     lo = (klo / IR) * IR;
     n_items = khi > klo ? (khi - lo + IR - 1) / IR : 0;
@@ -236,6 +240,12 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
     return __ldg(item_bands + (size_t)hb * p.total_q + sq.q0 + lo + (n % nq_tiles) * IR);
   };
   auto item_kept = [&](const int4 &e) { return e.y > e.x && e.x < tile0 + 128 && e.y > tile0; };
+  // a kept item's flags: 1 its rows are pure 0 / -inf intervals (masked by them, no bias value
+  // read), 2 besides, every one of its rows sees every key of this tile (no mask from the bias)
+  auto item_flags = [&](const int4 &e) {
+    if ((BIAS != 2 && BIAS != 3) || !p.bias_rows || e.z < 0) return 0;
+    return 1 | ((e.z <= tile0 && e.w >= min(tile0 + 128, sq.kv_len)) ? 2 : 0);
+  };
   int n_kept = n_items;
   if (item_bands) {
     n_kept = 0;
@@ -257,6 +267,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   const uint32_t sIn0 = base + C::OFF_IN0, sIn1 = base + C::OFF_IN1, sBias = base + C::OFF_B;
   float4 *ldbuf = reinterpret_cast<float4 *>(gbase + C::OFF_LD);  // [stage][IR/2 column pairs]
   int4 *bdbuf = reinterpret_cast<int4 *>(gbase + C::OFF_BD);      // [stage][IR/2 column pairs]
+  int2 *islot = reinterpret_cast<int2 *>(gbase + C::OFF_IS);      // [stage] {candidate, flags}
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
@@ -333,7 +344,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       constexpr int PPL = C::PAIRS > 0 ? C::PAIRS / 32 : 1;
       float rl[PPL][2], rd[PPL][2];
       // (dK/dV with bias bands and TMA-staged bias: the rows' finite-bias intervals as well)
-      const bool stage_bands = C::BD_BYTES > 0 && p.bias_rows != nullptr;
+      const bool stage_bands = (BIAS == 2 || BIAS == 3) && C::BD_BYTES > 0 && p.bias_rows != nullptr;
       int rbl[PPL][2], rbh[PPL][2];
       auto load_pairs = [&](int n) {
         const int h = item_head(n), i0 = item_row(n);
@@ -374,7 +385,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
           // the item's bias tile (needed last, by the compute warps; its slot frees earliest);
           // an item whose rows' bias is 0 over their intervals (pure) needs no tile: its slot
           // is passed along without a copy
-          const bool pure_item = item_bands && p.bias_rows && item_band(n).z != 0;
+          const bool pure_item = item_bands && (item_flags(item_band(n)) & 1);
           const int bs = k % C::NBS_;
           bool wb = true;
           if (lane == 0) {
@@ -419,6 +430,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
             if (stage_bands)
               bdbuf[st * C::PAIRS + lane + 32 * pp] = make_int4(rbl[pp][0], rbh[pp][0], rbl[pp][1], rbh[pp][1]);
           }
+          if (lane == 0) islot[st] = make_int2(n, item_bands ? item_flags(item_band(n)) : 0);
           if (n_next < n_items) load_pairs(n_next);  // (consumed next iteration)
         }
         const int ih = C::KEYS ? item_head(n) : hk;  // head inside the inner tensors
@@ -640,21 +652,10 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
       fence_before();
       mbar_arrive(bar(C::B_QT));
     }
-    for (int n = 0, kept = 0; n < n_items && ok; ++n) {
-      // n: the candidate item (which query head and rows, dK/dV; which keys, dQ); it: its place
-      // in the pipeline (rings, buffers, barrier phases)
-      bool ipure = false;
-      if (item_bands) {
-        const int4 e = item_band(n);
-        if (!item_kept(e)) continue;
-        ipure = BIAS == 2 && p.bias_rows != nullptr && e.z != 0;
-      }
-      const int it = kept++;
-      // bias values enter the logits (TMA-staged or read row by row), unless this item's or
-      // this CTA's rows are all pure intervals
-      const bool use_vals = BIAS == 1 || (BIAS == 2 && !ipure && !cta_pure);
+    for (int it = 0; it < n_kept && ok; ++it) {
+      // it: the item's place in the pipeline (rings, buffers, barrier phases); n: which item it
+      // is (query head and rows, dK/dV, from the producer's slot record; keys, dQ)
       const int b = it % NBUF, st = it % NSTAGE;
-      const int h = item_head(n);
       bool w = mbar_wait(bar(C::B_S + b), (it / NBUF) & 1, abort_flag, p.err);
       // the LSE / D pairs were written by the producer lanes before their arrive on in_full:
       // acquire that barrier too before reading them
@@ -663,6 +664,17 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         w = mbar_wait(bar(C::B_BF + it % C::NBS_), (it / C::NBS_) & 1, abort_flag, p.err);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
+      int n = it, iflags = 0;
+      if (C::KEYS) {
+        const int2 rec = islot[st];
+        n = rec.x;
+        iflags = rec.y;
+      }
+      const bool ipure = (iflags & 1) != 0, iinterior = (iflags & 2) != 0;
+      // bias values enter the logits (TMA-staged or read row by row), unless this item's or
+      // this CTA's rows are all pure intervals
+      const bool use_vals = BIAS == 1 || (BIAS == 2 && !ipure && !cta_pure);
+      const int h = item_head(n);
       fence_after();
       const float *brow = brow_dq;
       if (C::KEYS && BIAS == 1 && orow_ok) {
@@ -697,7 +709,7 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
         plain = plain && BIAS != 1;
         // dK/dV, a pure item: the columns (query rows) whose finite-bias interval holds this key
         unsigned bmask = 0xffffffffu;
-        if (C::BD_BYTES > 0 && ipure) {
+        if (C::BD_BYTES > 0 && ipure && !iinterior) {
           const int4 *bp = bdbuf + st * C::PAIRS + col0 / 2;
           bmask = 0u;
 #pragma unroll
@@ -970,8 +982,70 @@ tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
   }
 }
 
-// NBS > 0: the problem's bias is staged through TMA (the caller checked that it can be).
-template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS>
+// Whether every row this CTA works on has a bias that is 0 over its finite interval (bias
+// bands): dQ -- the CTA's 128 query rows; dK/dV -- the rows of every query item it keeps.  The
+// tile and item walk are those of tc_bwd_body.  Every thread of the CTA calls it.
+template <bool KEYS, int IR>
+__device__ __forceinline__ bool bwd_cta_all_pure(const Params &p) {
+  if (!p.bias_blocks) return false;
+  Seq sq;
+  if (!load_seq(p, (int)blockIdx.z, sq)) return false;
+  const int bxr = p.heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  const int gx = p.heads_fast ? (int)gridDim.y : (int)gridDim.x;
+  const int byh = p.heads_fast ? (int)blockIdx.x : (int)blockIdx.y;
+  if (KEYS) {
+    const int tile0 = bxr * 128, hk = byh;
+    if (tile0 >= sq.kv_len) return false;
+    int qlo = 0, qhi = 0;
+    if (sq.q_len > 0) {
+      q_band(tile0, min(tile0 + 128, sq.kv_len), sq.q_len, sq.kv_len, p.causal, p.window, qlo, qhi);
+      if (p.flags & VLF_FLAG_NO_SKIP) { qlo = 0; qhi = sq.q_len; }
+    }
+    const int lo = (qlo / IR) * IR;
+    const int nq_tiles = qhi > qlo ? (qhi - lo + IR - 1) / IR : 0;
+    const int n_items = nq_tiles * p.group;
+    bool all = true;
+    for (int b0 = 0; b0 < n_items; b0 += (int)blockDim.x) {
+      const int n = b0 + (int)threadIdx.x;
+      bool pure = true;
+      if (n < n_items) {
+        const int hb = p.bias_heads == 1 ? 0 : hk * p.group + n / nq_tiles;
+        const int4 e = __ldg(p.bias_blocks + (size_t)hb * p.total_q + sq.q0 + lo + (n % nq_tiles) * IR);
+        if (e.y > e.x && e.x < tile0 + 128 && e.y > tile0) pure = e.z >= 0;
+      }
+      all = __syncthreads_and(pure) && all;
+    }
+    return all;
+  }
+  const int bx = p.causal ? gx - 1 - bxr : bxr;
+  const int tile0 = bx * 128, hb = p.bias_heads == 1 ? 0 : byh;
+  if (tile0 >= sq.q_len) return false;
+  const int4 *bb = p.bias_blocks + (size_t)hb * p.total_q + sq.q0 + tile0;
+  int pure = __ldg(bb).z >= 0;
+  if (tile0 + 64 < sq.q_len) pure &= __ldg(bb + 64).z >= 0;
+  return pure != 0;
+}
+
+// The backward kernel.  With a TMA-staged bias (BIAS 2) and PST > 0, a CTA whose rows are all
+// 0 / -inf intervals runs the body without a bias ring instead (BIAS 3): its rings take the
+// shared memory of the bias tiles (PST / PST1 slots), as deep as the kernel without a bias.
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS, bool BF16,
+          int BIAS, int PST = 0, int PST1 = 0>
+__global__ void __launch_bounds__(384, 1)
+tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
+  if constexpr (BIAS == 2 && PST > 0) {
+    if (bwd_cta_all_pure<BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS>::KEYS, IR>(p)) {
+      tc_bwd_body<MODE, DQK, DV, IR, NBUF, PST, PST1, 0, BF16, 3>(maps, p);
+      return;
+    }
+  }
+  tc_bwd_body<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, BF16, BIAS>(maps, p);
+}
+
+// NBS > 0: the problem's bias is staged through TMA (the caller checked that it can be); PST /
+// PST1: the ring depths of its CTAs over pure 0 / -inf interval rows (0: none).
+template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS, int PST = 0,
+          int PST1 = 0>
 cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   using C = BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS>;
   const int bf = p.dtype == VLF_BF16;
@@ -1028,18 +1102,20 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   pl.heads_fast = p.bias != nullptr && p.bias_heads == 1;
   const dim3 grid = pl.heads_fast ? dim3(heads, tiles, p.num_seqs) : dim3(tiles, heads, p.num_seqs);
   void (*kern)(const BwdMaps, const Params);
+  int smem = C::SMEM;
   if constexpr (NBS > 0) {
-    kern = bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, true, 2>
-              : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, false, 2>;
+    kern = bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, true, 2, PST, PST1>
+              : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, false, 2, PST, PST1>;
+    if constexpr (PST > 0) smem = max(smem, BwdCfg<MODE, DQK, DV, IR, NBUF, PST, PST1, 0>::SMEM);
   } else {
     kern = p.bias ? (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, 0, true, 1>
                         : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, 0, false, 1>)
                   : (bf ? tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, 0, true, 0>
                         : tc_bwd_kernel<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, 0, false, 0>);
   }
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 384, C::SMEM, st>>>(m, pl);
+  kern<<<grid, 384, smem, st>>>(m, pl);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
@@ -1074,18 +1150,22 @@ cudaError_t rope_grad_sum(const Params &p, cudaStream_t st) {
 // (IR_KV, NBUF_KV, NST_KV, NST1_KV, NBS_KV) and the mode, item rows, buffers, ring stages and
 // bias stages of the dQ kernel (MODE_Q, IR_Q, NBUF_Q, NST_Q, NST1_Q, NBS_Q).  A ring slot is
 // refilled only after its item's last product has read it, so the rings are as deep as shared
-// memory allows.
+// memory allows.  With a TMA-staged bias, PST* are the ring depths of the CTAs whose rows are
+// all 0 / -inf intervals (the bias tiles' shared memory goes to the rings).
 template <int DQK, int DV, int IR_KV, int NBUF_KV, int NST_KV, int NST1_KV, int NBS_KV, int MODE_Q,
-          int IR_Q, int NBUF_Q, int NST_Q, int NST1_Q, int NBS_Q>
+          int IR_Q, int NBUF_Q, int NST_Q, int NST1_Q, int NBS_Q, int PST_KV = 0, int PST1_KV = 0,
+          int PST_Q = 0, int PST1_Q = 0>
 cudaError_t bwd_shape(const Params &p, cudaStream_t st, const cudaEvent_t *ev) {
   cudaError_t e;
   if ((e = mark(ev, 0, st)) != cudaSuccess) return e;
   if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV, NST1_KV, NBS_KV>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDkdv, DQK, DV, IR_KV, NBUF_KV, NST_KV, NST1_KV, NBS_KV, PST_KV, PST1_KV>(p, st)) != cudaSuccess)
+    return e;
   if (DQK == 192 && p.latent && p.dk_rope_part && (e = rope_grad_sum(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<MODE_Q, DQK, DV, IR_Q, NBUF_Q, NST_Q, NST1_Q, NBS_Q>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<MODE_Q, DQK, DV, IR_Q, NBUF_Q, NST_Q, NST1_Q, NBS_Q, PST_Q, PST1_Q>(p, st)) != cudaSuccess)
+    return e;
   return mark(ev, 3, st);
 }
 
@@ -1120,9 +1200,9 @@ cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev)
   const bool bias_tma = p.bias != nullptr && p.max_kv % 4 == 0 &&
                         (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0 && p.d_qk <= 128;
   if (bias_tma) {
-    if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 4, 4, 3, kDq, 64, 2, 4, 4, 3>(p, st, ev);
-    if (p.d_qk == 96) return bwd_shape<96, 96, 64, 2, 2, 2, 3, kDq, 64, 2, 2, 2, 3>(p, st, ev);
-    return bwd_shape<128, 128, 64, 2, 2, 2, 3, kDq, 64, 2, 2, 2, 3>(p, st, ev);
+    if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 4, 4, 3, kDq, 64, 2, 4, 4, 3, 6, 6, 6, 6>(p, st, ev);
+    if (p.d_qk == 96) return bwd_shape<96, 96, 64, 2, 2, 2, 3, kDq, 64, 2, 2, 2, 3, 5, 4, 5, 4>(p, st, ev);
+    return bwd_shape<128, 128, 64, 2, 2, 2, 3, kDq, 64, 2, 2, 2, 3, 5, 4, 5, 4>(p, st, ev);
   }
   if (p.d_qk == 64) return bwd_shape<64, 64, 64, 2, 6, 6, 0, kDqS, 128, 2, 3, 3, 0>(p, st, ev);
   if (p.d_qk == 96) return bwd_shape<96, 96, 64, 2, 5, 4, 0, kDqS, 128, 2, 3, 2, 0>(p, st, ev);

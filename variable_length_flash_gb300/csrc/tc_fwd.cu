@@ -207,14 +207,14 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       const int hb = p.bias_heads == 1 ? 0 : ti.head[0];
       const int4 *bb = p.bias_blocks + (size_t)hb * p.total_q + sq.q0 + ti.row0[0];
       const int4 e0 = __ldg(bb);
-      int blo = e0.x, bhi = e0.y, pure = e0.z;
+      int blo = e0.x, bhi = e0.y, pure = e0.z >= 0;
       if (ti.row0[0] + 64 < sq.q_len) {
         const int4 e1 = __ldg(bb + 64);
         if (e1.y > e1.x) {
           blo = bhi > blo ? min(blo, e1.x) : e1.x;
           bhi = max(bhi, e1.y);
         }
-        pure &= e1.z;
+        pure &= e1.z >= 0;
       }
       int jl = ti.lo, jh = ti.hi;
       if (bhi > blo) {
