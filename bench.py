@@ -426,13 +426,18 @@ def roofline(prob, stage_ms, peaks, tensor_peak, dev):
     tc = (fwd_path if dom == "fwd" else bwd_path) == 1
     sec = stage_ms[dom] * 1e-3
     hbm_frac = bytes_of[dom] / sec / 1e9 / peaks["hbm_gbs"]
-    ten_frac = flops_of.get(dom, 0) / sec / 1e12 / tensor_peak
+    ten_roof = tensor_peak * (1.1 / 2.25) / 3.0 if w.dtype == "fp32" else tensor_peak
+    ten_frac = flops_of.get(dom, 0) / sec / 1e12 / ten_roof
     if dom == "rowdot" or (tc and hbm_frac > ten_frac):
         roof = {"bound": "hbm", "achieved": bytes_of[dom] / sec / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "algorithmic_bytes": bytes_of[dom]}
     elif tc:
         roof = {"bound": "tensor", "achieved": flops_of[dom] / sec / 1e12, "peak": tensor_peak,
                 "unit": "TFLOP/s", "algorithmic_flops": flops_of[dom]}
+        if w.dtype == "fp32":
+            # fp32 on the tensor cores: tf32 products (the bf16 roof x the nominal dense ratio
+            # 1.1 / 2.25), three passes per product -- the roof of the algorithmic FLOPs
+            roof["peak"] = tensor_peak * (1.1 / 2.25) / 3.0
     else:
         props = torch.cuda.get_device_properties(dev)
         alu_peak = props.multi_processor_count * 128 * 2 * 2070.0 * 1e6 / 1e12
@@ -444,8 +449,10 @@ def roofline(prob, stage_ms, peaks, tensor_peak, dev):
     tr = ncu_traffic(dom, w.name) if tc or roof["bound"] == "hbm" else None
     roof["traffic"] = tr
     roof["kernel"] = dom
-    roof["peak_source"] = peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz)"
-                                             if roof["bound"] == "alu" else "")
+    roof["peak_source"] = peaks["source"] + (
+        " (fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz)" if roof["bound"] == "alu" else
+        (" (tf32 = bf16 x 1.1/2.25 nominal ratio, / 3 passes per product)"
+         if roof["bound"] == "tensor" and w.dtype == "fp32" else ""))
     return roof, {"fwd": "tcgen05" if fwd_path == 1 else "simt",
                   "bwd": "tcgen05" if bwd_path == 1 else "simt"}
 
@@ -677,6 +684,8 @@ def main():
                     help="headline workload only (skip the other configurations)")
     ap.add_argument("--configs", default=None,
                     help="comma-separated subset of the other configurations to time")
+    ap.add_argument("--sustain", type=float, default=SUSTAIN_S,
+                    help="seconds of the sustained run before the timed steps (clock evidence)")
     ap.add_argument("--cpu-units", type=int, default=20,
                     help="(sequence, head) units of the workload for the CPU oracle baseline")
     args = ap.parse_args()
@@ -696,7 +705,7 @@ def main():
     time.sleep(0.3)
 
     head, prob = measure(vlf, w, dev, world, args.steps, args.warmup, sampler, peaks,
-                         sustain_s=SUSTAIN_S)
+                         sustain_s=args.sustain)
     pairs = F.workload_pairs(w)
     fpp = F.flops_per_pair(w.d_qk, w.d_v)
     step_flops = fpp["fwd_bwd"] if w.backward else fpp["fwd"]

@@ -376,16 +376,22 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           while (n < n_items && !item_kept(item_band(n))) ++n;
         return n;
       };
+      const int4 none = make_int4(0, 0, -1, -1);
       int n = next_kept(0);
+      int4 e_n = item_bands && n < n_items ? item_band(n) : none;  // its block band
       if (C::KEYS && n < n_items) load_pairs(n);
       for (int k = 0; n < n_items; ++k) {
         const int st = k % NSTAGE, st1 = k % NSTAGE1;
-        const int n_next = next_kept(n + 1);
+        // the next candidate's band, loaded here so that its latency passes during this item's
+        // waits; the walk to the next kept candidate follows below
+        int n_next = n + 1;
+        int4 e_next = item_bands && n_next < n_items ? item_band(n_next) : none;
+        const int flags_n = item_bands ? item_flags(e_n) : 0;
         if (BIAS == 2 && !cta_pure) {
           // the item's bias tile (needed last, by the compute warps; its slot frees earliest);
           // an item whose rows' bias is 0 over their intervals (pure) needs no tile: its slot
           // is passed along without a copy
-          const bool pure_item = item_bands && (item_flags(item_band(n)) & 1);
+          const bool pure_item = (flags_n & 1) != 0;
           const int bs = k % C::NBS_;
           bool wb = true;
           if (lane == 0) {
@@ -421,6 +427,11 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
         }
         if (C::KEYS) {
+          if (item_bands)
+            while (n_next < n_items && !item_kept(e_next)) {
+              ++n_next;
+              if (n_next < n_items) e_next = item_band(n_next);
+            }
 #pragma unroll
           for (int pp = 0; pp < PPL; ++pp) {
             float nl[2];
@@ -430,7 +441,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
             if (stage_bands)
               bdbuf[st * C::PAIRS + lane + 32 * pp] = make_int4(rbl[pp][0], rbh[pp][0], rbl[pp][1], rbh[pp][1]);
           }
-          if (lane == 0) islot[st] = make_int2(n, item_bands ? item_flags(item_band(n)) : 0);
+          if (lane == 0) islot[st] = make_int2(n, flags_n);
           if (n_next < n_items) load_pairs(n_next);  // (consumed next iteration)
         }
         const int ih = C::KEYS ? item_head(n) : hk;  // head inside the inner tensors
@@ -461,6 +472,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
         }
         if (!__shfl_sync(0xffffffffu, (int)w1, 0)) break;
         n = n_next;
+        e_n = e_next;
       }
       if (lane == 0) {
         drain_wait(bar(C::B_OUT), 0);

@@ -24,10 +24,10 @@ def visible_pairs(q_len: int, kv_len: int, causal: bool, window: int) -> int:
     return int(np.clip(hi - lo + 1, 0, None).sum())
 
 
-def prefix_lm_pairs(q_len: int, kv_len: int) -> int:
-    """Pairs with a finite prefix-LM bias (key <= 8191 or key <= query), single sequence."""
+def prefix_lm_pairs(q_len: int, kv_len: int, prefix: int = PREFIX_LEN) -> int:
+    """Pairs with a finite prefix-LM bias (key <= prefix - 1 or key <= query), single sequence."""
     i = np.arange(q_len, dtype=np.int64)
-    return int(np.minimum(kv_len, np.maximum(PREFIX_LEN, i + 1)).sum())
+    return int(np.minimum(kv_len, np.maximum(prefix, i + 1)).sum())
 
 
 def workload_pairs(w) -> int:
@@ -36,7 +36,7 @@ def workload_pairs(w) -> int:
     for lq, lk in zip(w.lengths_q, w.lengths_kv):
         if w.bias is not None:
             assert not w.causal and w.window <= 0
-            total += prefix_lm_pairs(lq, lk)
+            total += prefix_lm_pairs(lq, lk, w.meta.get("prefix", PREFIX_LEN))
         else:
             total += visible_pairs(lq, lk, w.causal, w.window)
     return total * w.h_q

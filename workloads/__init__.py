@@ -150,6 +150,13 @@ def workload(name: str, seed: int = 0) -> Workload:
         lens = [49152]
         return Workload(name, "fp16", lens, lens, 16, 16, 128, 128, causal=False, sigma=0.5,
                         bias="alibi_prefix" if name.endswith("alibi") else "prefix")
+    if name in ("long12288_fp16_bias_alibi", "long12288_fp16_bias_prefix"):
+        # the long-context workload at a quarter of the length (prefix 2048, the same share of
+        # the sequence), small enough for profiler captures of its kernels
+        lens = [12288]
+        return Workload(name, "fp16", lens, lens, 16, 16, 128, 128, causal=False, sigma=0.5,
+                        bias="alibi_prefix" if name.endswith("alibi") else "prefix",
+                        meta={"prefix": 2048})
     raise KeyError(name)
 
 
@@ -157,7 +164,8 @@ WORKLOADS = ["varlen64_fp16_full", "varlen64_fp16_causal", "dense4x4096_bf16_cau
              "ragged64_gqa_window_bf16", "latent2x8192_bf16_causal",
              "long49152_fp16_bias_alibi", "long49152_fp16_bias_prefix", "decode64x8192_bf16_gqa",
              "dense4x4096_bf16_causal_d96", "decode4x32768_bf16_gqa", "dense4x4096_bf16_causal_d256",
-             "latent2x8192_bf16_causal_shared_rope", "dense4x4096_fp32_causal_d64"]
+             "latent2x8192_bf16_causal_shared_rope", "dense4x4096_fp32_causal_d64",
+             "long12288_fp16_bias_alibi", "long12288_fp16_bias_prefix"]
 
 
 def custom(lengths_q, lengths_kv=None, *, dtype="bf16", h_q=4, h_kv=None, d_qk=64, d_v=None,
@@ -204,7 +212,7 @@ def bias_block(w: Workload, rows: torch.Tensor, heads, device="cpu") -> torch.Te
     n_kv = w.max_seqlen_kv
     i = rows.to(device=device, dtype=torch.int64)[:, None]
     j = torch.arange(n_kv, device=device, dtype=torch.int64)[None, :]
-    allowed = (j <= PREFIX_LEN - 1) | (j <= i)
+    allowed = (j <= w.meta.get("prefix", PREFIX_LEN) - 1) | (j <= i)
     out = torch.empty((rows.numel(), len(heads), n_kv), dtype=torch.float32, device=device)
     dist = (i - j).abs().to(torch.float64)
     slopes = alibi_slopes(w.h_q).to(device)
