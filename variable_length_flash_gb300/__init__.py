@@ -114,6 +114,7 @@ def _load():
 
 
 _lib = _load()
+_fwd_ex = _lib.vlf_attn_varlen_fwd_ex  # (looked up once: the attribute lookup costs per call)
 
 
 def _ptr(t):
@@ -333,7 +334,8 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
         _req(lse, "lse", torch.float32)
     nseq = cu_seqlens_q.numel() - 1
     dt = _DTYPE[dtype]
-    st_h = stream.cuda_stream if stream is not None else _stream(None, q)
+    st_h = (stream.cuda_stream if stream is not None else
+            _raw_stream(q.get_device()) if _raw_stream is not None else _stream(None, q))
     if num_splits is None:
         num_splits = _lib.vlf_fwd_num_splits(nseq, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
                                              dqk, dv, dt, int(flags), 0)
@@ -351,11 +353,11 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
         if st != VLF_OK:
             _check(st, "vlf_attn_varlen_fwd_split")
         return out, lse
-    st = _lib.vlf_attn_varlen_fwd_ex(
+    st = _fwd_ex(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_kv.data_ptr(),
         nseq, tq, tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv, dt,
-        float(scale) if scale else 0.0, int(bool(causal)), int(window or 0), bias_p, bh,
-        out.data_ptr(), lse.data_ptr(), st_h, int(flags), bands_p)
+        float(scale) if scale else 0.0, 1 if causal else 0, int(window) if window else 0, bias_p,
+        bh, out.data_ptr(), lse.data_ptr(), st_h, int(flags), bands_p)
     if st != VLF_OK:
         _check(st, "vlf_attn_varlen_fwd")
     return out, lse

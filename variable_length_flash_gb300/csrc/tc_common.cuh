@@ -28,6 +28,16 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialization may start before the kernel ahead of
+// it in the stream has finished: it must wait (griddepcontrol.wait) for that kernel's completion
+// and memory before reading anything global.  pdl_trigger lets the kernel after this one be
+// launched as soon as every CTA of this one has issued it.  (No-ops for a normal launch.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -58,6 +58,23 @@ struct FwdMaps {
   CUtensorMap bias;  // bias through TMA: [total_q][bias_heads x max_kv] fp32, box {32, 128}
   CUtensorMap q_rope, k_rope;  // latent head with split operands: the rope tensors (64 columns)
 };
+// The kernels that need none of the extra maps take only Q, K, V: a smaller parameter block to
+// copy per launch (host time a small problem pays on every call).
+struct FwdMapsPlain {
+  CUtensorMap q, k, v;
+};
+template <int DQK, bool PACK, int BIAS>
+struct FwdMapsFor {
+  using type = typename std::conditional<(PACK || BIAS == 2 || DQK == 192), FwdMaps, FwdMapsPlain>::type;
+};
+__device__ __forceinline__ const CUtensorMap *q3_of(const FwdMaps &m) { return &m.q3; }
+__device__ __forceinline__ const CUtensorMap *q3_of(const FwdMapsPlain &m) { return &m.q; }
+__device__ __forceinline__ const CUtensorMap *bias_of(const FwdMaps &m) { return &m.bias; }
+__device__ __forceinline__ const CUtensorMap *bias_of(const FwdMapsPlain &m) { return &m.q; }
+__device__ __forceinline__ const CUtensorMap *qrope_of(const FwdMaps &m) { return &m.q_rope; }
+__device__ __forceinline__ const CUtensorMap *qrope_of(const FwdMapsPlain &m) { return &m.q; }
+__device__ __forceinline__ const CUtensorMap *krope_of(const FwdMaps &m) { return &m.k_rope; }
+__device__ __forceinline__ const CUtensorMap *krope_of(const FwdMapsPlain &m) { return &m.k; }
 
 // NT: query tiles per CTA.  NT = 2: 416 threads and all 512 TMEM columns, one CTA per SM.
 // NT = 1: 256 threads, 256 TMEM columns and at most half the SM's shared memory, so two CTAs
@@ -164,12 +181,16 @@ __device__ __forceinline__ void tile_info(const Params &p, const Seq &sq, int bx
 // the unsplit kernels carry none of its code or registers).
 template <int DQK, int DV, int NK, int NV, int NT, bool BF16, int BIAS, bool PACK, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<DQK, DV, NK, NV, NT>::THREADS, FwdCfg<DQK, DV, NK, NV, NT>::MIN_BLOCKS)
-tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
+tc_fwd_kernel(const __grid_constant__ typename FwdMapsFor<DQK, PACK, BIAS>::type maps, const Params p) {
   constexpr int NBS = BIAS == 2 ? 2 : 0;
   static_assert(BIAS != 2 || (NT == 1 && !PACK), "bias tiles through TMA: one unpacked tile");
   static_assert(!SPLIT || (NT == 1 && BIAS != 2), "split-KV parts: one tile, no bias ring");
   using C = FwdCfg<DQK, DV, NK, NV, NT, NBS>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // launched with programmatic stream serialization (small problems, launch_kernel below): let
+  // the next kernel be launched now, and read nothing global before the previous one is done
+  pdl_trigger();
+  pdl_wait();
   const bool pair_heads = NT == 2 && (p.group % 2 == 0);
   // (split-KV: the part index is recomputed where it is needed, so that it is not held in a
   // register through the main loop)
@@ -284,8 +305,8 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
       const int qw = lat ? 128 : DQK;
       const int rh = lat && p.rope_heads == 1 ? 0 : hk;  // the kv head's rope key
       if (lat) {
-        tma_prefetch_desc(&maps.q_rope);
-        tma_prefetch_desc(&maps.k_rope);
+        tma_prefetch_desc(qrope_of(maps));
+        tma_prefetch_desc(krope_of(maps));
       }
       int nq = 0;
       for (int t = 0; t < 2; ++t) nq += ti.row0[t] < sq.q_len ? 1 : 0;
@@ -296,10 +317,10 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         if (ti.row0[t] >= sq.q_len) continue;
         for (int c = 0; c < C::KBQ; ++c) {
           if (PACK)  // rows (token, head of the group): one 3-D box
-            tma_load_3d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q3, 64 * c, hk * p.group,
+            tma_load_3d(sQ + t * C::Q_BYTES + c * C::QBLK, q3_of(maps), 64 * c, hk * p.group,
                         sq.q0 + ti.row0[t], bar(C::B_Q));
           else if (lat && c == 2)
-            tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q_rope, ti.head[t] * 64,
+            tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, qrope_of(maps), ti.head[t] * 64,
                         sq.q0 + ti.row0[t], bar(C::B_Q));
           else
             tma_load_2d(sQ + t * C::Q_BYTES + c * C::QBLK, &maps.q, ti.head[t] * qw + 64 * c,
@@ -307,7 +328,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
         }
       }
       int k_issued[NK] = {0}, v_issued[NV] = {0}, b_issued[NBS > 0 ? NBS : 1] = {0};
-      if (BIAS == 2) tma_prefetch_desc(&maps.bias);
+      if (BIAS == 2) tma_prefetch_desc(bias_of(maps));
       const int bcol = BIAS == 2 ? (p.bias_heads == 1 ? 0 : ti.head[0]) * p.max_kv : 0;
       bool ok = true;
       for (int j = lo; j < hi + C::LEAD && ok; ++j) {
@@ -319,7 +340,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           if (!ok) break;
           mbar_expect_tx(bar(C::B_BF + bs), C::BIAS_STAGE);
           for (int c = 0; c < 2; ++c)
-            tma_load_2d(sB + bs * C::BIAS_STAGE + c * C::BIAS_BOX, &maps.bias, bcol + kj * kBN + 32 * c,
+            tma_load_2d(sB + bs * C::BIAS_STAGE + c * C::BIAS_BOX, bias_of(maps), bcol + kj * kBN + 32 * c,
                         sq.q0 + ti.row0[0], bar(C::B_BF + bs));
           ++b_issued[bs];
         }
@@ -330,7 +351,7 @@ tc_fwd_kernel(const __grid_constant__ FwdMaps maps, const Params p) {
           mbar_expect_tx(bar(C::B_KF + ks), C::K_BYTES);
           for (int c = 0; c < C::KBQ; ++c) {
             if (lat && c == 2)
-              tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, &maps.k_rope, rh * 64,
+              tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, krope_of(maps), rh * 64,
                           sq.k0 + kj * kBN, bar(C::B_KF + ks));
             else
               tma_load_2d(sK + ks * C::K_BYTES + c * C::KVBLK, &maps.k, hk * qw + 64 * c,
@@ -776,6 +797,38 @@ cudaError_t launch_combine(const Params &p, cudaStream_t st) {
   return e;
 }
 
+// Launches kern with programmatic stream serialization when the grid is small (fewer CTAs than
+// SMs): its CTAs may then be made resident while the kernel ahead of them in the stream runs and
+// start the moment it finishes (the kernels wait for it before any global read), instead of
+// paying the launch latency after it -- microseconds that a small problem's whole kernel is made
+// of.  Larger grids launch normally (their first wave could only wait on busy SMs).
+cudaError_t launch_kernel(const void *kern, dim3 grid, int threads, int smem, cudaStream_t st,
+                          void **args) {
+  static int num_sms = [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 0;
+    return n;
+  }();
+  const long long ctas = (long long)grid.x * grid.y * grid.z;
+  if (num_sms <= 0 || ctas >= num_sms) {
+    const cudaError_t e = cudaLaunchKernel(kern, grid, dim3(threads), args, (size_t)smem, st);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 driver_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void *ptr = nullptr;
@@ -923,18 +976,28 @@ bool make_tmap_q3(CUtensorMap *m, const void *base, uint64_t tokens, uint64_t he
 
 // The kernel instantiation for a dtype and bias kind (0 none, 1 rows from global memory, 2 TMA
 // tiles: unpacked, unsplit, one tile per CTA only).
+// The chosen kernel and whether it takes the full map set (FwdMaps) or Q, K, V alone.
+struct FwdPick {
+  const void *kern;
+  bool full;
+};
+template <int DQK, int DV, int NK, int NV, int NT, bool BF16, int BIAS, bool PACK, bool SPLIT>
+FwdPick fwd_pick_one() {
+  return {reinterpret_cast<const void *>(tc_fwd_kernel<DQK, DV, NK, NV, NT, BF16, BIAS, PACK, SPLIT>),
+          std::is_same<typename FwdMapsFor<DQK, PACK, BIAS>::type, FwdMaps>::value};
+}
 template <int DQK, int DV, int NK, int NV, int NT, bool PACK, bool SPLIT>
-void (*pick_fwd(bool bf, int bias_kind))(const FwdMaps, const Params) {
+FwdPick pick_fwd(bool bf, int bias_kind) {
   if constexpr (NT == 1 && !PACK && !SPLIT && DV <= 128) {
     if (bias_kind == 2)
-      return bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 2, false, false>
-                : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 2, false, false>;
+      return bf ? fwd_pick_one<DQK, DV, NK, NV, NT, true, 2, false, false>()
+                : fwd_pick_one<DQK, DV, NK, NV, NT, false, 2, false, false>();
   }
   if (bias_kind != 0)
-    return bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 1, PACK, SPLIT>
-              : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 1, PACK, SPLIT>;
-  return bf ? tc_fwd_kernel<DQK, DV, NK, NV, NT, true, 0, PACK, SPLIT>
-            : tc_fwd_kernel<DQK, DV, NK, NV, NT, false, 0, PACK, SPLIT>;
+    return bf ? fwd_pick_one<DQK, DV, NK, NV, NT, true, 1, PACK, SPLIT>()
+              : fwd_pick_one<DQK, DV, NK, NV, NT, false, 1, PACK, SPLIT>();
+  return bf ? fwd_pick_one<DQK, DV, NK, NV, NT, true, 0, PACK, SPLIT>()
+            : fwd_pick_one<DQK, DV, NK, NV, NT, false, 0, PACK, SPLIT>();
 }
 
 template <int DQK, int DV, int NK, int NV, int NT>
@@ -983,8 +1046,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   const unsigned zdim = (unsigned)p.num_seqs * (split ? (unsigned)p.kv_splits : 1u);
   if (zdim > 65535u) return cudaErrorInvalidValue;
   const dim3 grid = pl.heads_fast ? dim3(heads, blocks, zdim) : dim3(blocks, heads, zdim);
-  using K = void (*)(const FwdMaps, const Params);
-  K kern;
+  FwdPick kern;
   int smem = C::SMEM;
   const int bias_kind = p.bias ? (bias_tma ? 2 : 1) : 0;
   if constexpr (NT == 1) {
@@ -1000,10 +1062,11 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
     if (pack || split || bias_tma) return cudaErrorInvalidValue;
     kern = pick_fwd<DQK, DV, NK, NV, NT, false, false>(bf, bias_kind);
   }
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem);
+  cudaError_t e = set_smem_once(kern.kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::THREADS, smem, st>>>(maps, pl);
-  e = cudaGetLastError();
+  FwdMapsPlain plain{maps.q, maps.k, maps.v};
+  void *args[2] = {kern.full ? static_cast<void *>(&maps) : static_cast<void *>(&plain), &pl};
+  e = launch_kernel(kern.kern, grid, C::THREADS, smem, st, args);
   if (e == cudaSuccess) count_launch();
   return e;
 }
