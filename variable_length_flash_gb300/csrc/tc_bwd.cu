@@ -26,7 +26,9 @@
 // MMA order: after item n's P / dS are ready its accumulations are issued; the products of the
 // item that next uses n's columns (n + NBUF) follow as soon as those columns are released: S
 // once accumulation 0 (dK/dV: dV += P^T dO) has read P^T (dQ: once the compute warps have read
-// S), dP once the last accumulation has read dS.
+// S), dP once the last accumulation has read dS.  S and dP complete on separate barriers: the
+// compute warps form P from S while dP still runs, then wait for dP to form dS; in the dK/dV
+// kernel P^T goes to the dV accumulation before dS^T is formed.
 // Tiles outside the causal / window band are skipped (they contribute exact zeros).  Every wait
 // is bounded.
 #include <cudaTypedefs.h>
@@ -110,8 +112,8 @@ struct BwdCfg {
   static constexpr int OFF_B = (OFF_IS + IS_BYTES + B_ALIGN - 1) & ~(B_ALIGN - 1);
   static constexpr int OFF_BAR = OFF_B + NBS * BIAS_STAGE;
   // barriers: outer_full, in_full[NSTAGE], in_empty[NSTAGE] (ring 0), in1_full[NSTAGE1],
-  // in1_empty[NSTAGE1] (ring 1), s_full[NBUF] (S and dP issued:
-  // two arrivals), p_ready[NBUF], acc0_done[NBUF] (dV), acc_done[NBUF] (dK or dQ: the item's last
+  // in1_empty[NSTAGE1] (ring 1), s_full[NBUF] (S done; and dP unless SPLIT: two arrivals),
+  // p_ready[NBUF], acc0_done[NBUF] (dV), acc_done[NBUF] (dK or dQ: the item's last
   // accumulation), drain[3] (one per MMA-issuing warp), dp_free (kDqS)
   static constexpr int B_OUT = 0, B_IF = 1, B_IE = B_IF + NSTAGE, B_IF1 = B_IE + NSTAGE;
   static constexpr int B_IE1 = B_IF1 + NSTAGE1, B_S = B_IE1 + NSTAGE1;
@@ -119,7 +121,9 @@ struct BwdCfg {
   static constexpr int B_PF = B_DRAIN + 3;  // kDqS: the compute warps have loaded dP
   static constexpr int B_QT = B_PF + 1;     // QT: the outer Q / dO rows are in TMEM (kDq)
   static constexpr int B_BF = B_QT + 1, B_BE = B_BF + NBS;  // bias full / empty
-  static constexpr int NBAR = B_BE + NBS;
+  // dp_full[NBUF] (SPLIT: dP done), ds_ready[NBUF] (P_EARLY: dS^T written; p_ready then means P^T)
+  static constexpr int B_DP = B_BE + NBS, B_DS = B_DP + NBUF;
+  static constexpr int NBAR = B_DS + NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // (no alignment slack: the dynamic shared window starts 1024-byte aligned, checked in-kernel)
   static constexpr int SMEM = OFF_MISC + 16;
@@ -147,6 +151,13 @@ struct BwdCfg {
   static_assert(!QT_DO || (DOA >= NQ_PAD && DOA + NV_PAD / 2 <= BUF), "TMEM columns of the dO operand");
   static constexpr int HALF = IR / 2;      // columns per compute warpgroup
   static constexpr int CHUNKS = HALF / 32;  // 32-column chunks per compute thread
+  // SPLIT (one 32-column chunk per compute thread): S and dP complete on separate barriers, and
+  // an item whose dP has not landed with S has its P formed first, its dP loaded after.  With two
+  // chunks (128-column dQ items) S and dP are awaited and loaded together, chunk by chunk.
+  // P_EARLY (dK/dV): P^T goes to the dV accumulation before dS^T is formed.
+  static constexpr bool SPLIT = HAS_DP && CHUNKS == 1;
+  static constexpr bool P_EARLY = HAS_DV && HAS_DP;
+  static_assert(!P_EARLY || SPLIT, "P^T released early needs the split form");
   static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * 2 * IR) <= 512, "TMEM columns");
   static_assert(SMEM <= 232448, "shared memory");
   static_assert((MODE != kDkdv || NV_PAD <= 128) && NV_PAD <= 256 && NQ_PAD <= 256 && DQK % 32 == 0 &&
@@ -280,7 +291,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
     for (int i = 0; i < NSTAGE; ++i) { mbar_init(bar(C::B_IF + i), 33); mbar_init(bar(C::B_IE + i), 1); }
     for (int i = 0; i < NSTAGE1; ++i) { mbar_init(bar(C::B_IF1 + i), 1); mbar_init(bar(C::B_IE1 + i), 1); }
     for (int b = 0; b < NBUF; ++b) {
-      mbar_init(bar(C::B_S + b), C::HAS_DP ? 2 : 1);  // S and dP issued
+      mbar_init(bar(C::B_S + b), C::HAS_DP && !C::SPLIT ? 2 : 1);  // S (and dP) done
       mbar_init(bar(C::B_P + b), 256);
       mbar_init(bar(C::B_D + b), 1);
       mbar_init(bar(C::B_D0 + b), 1);
@@ -289,6 +300,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
     mbar_init(bar(C::B_PF), 256);
     mbar_init(bar(C::B_QT), 256);
     for (int i = 0; i < NBS; ++i) { mbar_init(bar(C::B_BF + i), 1); mbar_init(bar(C::B_BE + i), 256); }
+    for (int b = 0; b < NBUF; ++b) { mbar_init(bar(C::B_DP + b), 1); mbar_init(bar(C::B_DS + b), 256); }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -578,7 +590,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           fence_after();
           if (role == 0) issue_s(m);
           else issue_dp(m);
-          mma_commit_w(bar(C::B_S + b));
+          mma_commit_w(bar((C::SPLIT && role == 1 ? C::B_DP : C::B_S) + b));
           // dQ, kDk: V / dO (ring 1) has no reader after dP
           if (!C::HAS_DV && role == 1) mma_commit_w(bar(C::B_IE1 + m % NSTAGE1));
         }
@@ -597,9 +609,17 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
             }
             issue_acc0(n);
             mma_commit_w(bar(C::B_D0 + b));
-            mma_commit_w(bar(C::B_IE1 + n % NSTAGE1));  // dO (ring 1) has no reader after dV
+            if (!C::P_EARLY) mma_commit_w(bar(C::B_IE1 + n % NSTAGE1));  // dO (ring 1): no reader after dV
+          }
+          if (C::P_EARLY) {
+            // dK once dS^T is written; dO's other reader, dP(n), completed before the compute
+            // warps loaded it, so the dO slot frees with this item's accumulations
+            ok = wait_all(C::B_DS + b, (n / NBUF) & 1);
+            if (!ok) break;
+            fence_after();
           }
           if (C::HAS_LAST) issue_acc1(n);
+          if (C::P_EARLY) mma_commit_w(bar(C::B_IE1 + n % NSTAGE1));
           mma_commit_w(bar(C::B_D + b));  // (the item's last accumulation)
           mma_commit_w(bar(C::B_IE + n % NSTAGE));
         }
@@ -693,6 +713,9 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
         const int bh = p.bias_heads == 1 ? 0 : h;
         brow = p.bias + (size_t)bh * p.max_kv + orow;  // + (q0 + i) * bias_heads * max_kv per column
       }
+      // SPLIT: has dP landed too (then it is loaded with S)?
+      const bool dp_now = C::SPLIT && __all_sync(0xffffffffu, mbar_test(bar(C::B_DP + b), (it / NBUF) & 1));
+      const bool with_dp = C::HAS_DP && (!C::SPLIT || dp_now);
 #pragma unroll 1
       for (int ch = 0; ch < C::CHUNKS; ++ch) {
         const int col0 = C::HALF * half + 32 * ch;  // this chunk's first column in the item
@@ -701,12 +724,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
         uint32_t sv[32], dv[32];
         __syncwarp();
         tmem_ld32(s_addr, sv);
-        if (C::HAS_DP) {
-          tmem_ld32(dp_addr, dv);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) dv[e] = 0u;  // (kDv: no dP; dS is not formed)
-        }
+        if (with_dp) tmem_ld32(dp_addr, dv);
         // is every element of this thread's 32 columns visible (no per-element mask)?
         bool plain;
         if (C::KEYS) {
@@ -754,33 +772,28 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           }
         }
         tmem_ld_wait();
-        if (MODE == kDqS && ch == C::CHUNKS - 1) {
+        if (MODE == kDqS && with_dp && ch == C::CHUNKS - 1) {
           // every dP column of the item is in registers: the next dP may overwrite them
           fence_before();
           mbar_arrive(bar(C::B_PF));
         }
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
+        float pf[32];  // P
         if (plain) {
-          // every pair visible: P = 2^(S log2e scale - LSE2 [+ bias log2e]), dS = P (dP - D)
+          // every pair visible: P = 2^(S log2e scale - LSE2 [+ bias log2e])
           // (packed f32x2 arithmetic: the same per-lane rounding as the scalar forms)
           const uint64_t sl22 = f2pack(sl2, sl2), lg22 = f2pack(kLog2e, kLog2e);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = 2 * e;
-            float4 q4;
-            if (C::KEYS) q4 = lp[e];
-            else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
+            const float2 nl = C::KEYS ? make_float2(lp[e].x, lp[e].y) : make_float2(row_nl, row_nl);
             uint64_t x2 = fma2(f2pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl22,
-                               f2pack(q4.x, q4.y));
+                               f2pack(nl.x, nl.y));
             if (BIAS == 2 && use_vals) x2 = fma2(f2pack(bq4[c], bq4[c + 1]), lg22, x2);
             const float2 x = f2unpack(x2);
-            const float pa = ex2(x.x), pb = ex2(x.y);
-            const uint64_t p2 = f2pack(pa, pb);
-            const uint64_t t2 = add2(f2pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
-                                     f2pack(q4.z, q4.w));
-            const float2 d = f2unpack(mul2(p2, t2));
-            pk[e] = pack2(pa, pb, is_bf16);
-            dk[e] = pack2(d.x, d.y, is_bf16);
+            pf[c] = ex2(x.x);
+            pf[c + 1] = ex2(x.y);
+            pk[e] = pack2(pf[c], pf[c + 1], is_bf16);
           }
         } else {
           // dQ with a bias from global memory: the chunk's 32 bias values of this row, 16 bytes
@@ -797,9 +810,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = 2 * e;
-            float4 q4;
-            if (C::KEYS) q4 = lp[e];
-            else q4 = make_float4(row_nl, row_nl, row_nd, row_nd);
+            const float2 nl = C::KEYS ? make_float2(lp[e].x, lp[e].y) : make_float2(row_nl, row_nl);
             float xs[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -818,23 +829,56 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
               xs[u] = (cc >= vis_lo && cc < vis_hi && ((bmask >> (c + u)) & 1u)) ? x : -INFINITY;
             }
             // masked logits (-inf) and rows without keys (-LSE2 = -inf) give P = 0
-            const float2 x = f2unpack(add2(f2pack(xs[0], xs[1]), f2pack(q4.x, q4.y)));
-            const float pa = ex2(x.x), pb = ex2(x.y);
-            const uint64_t t2 = add2(f2pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
-                                     f2pack(q4.z, q4.w));
-            const float2 d = f2unpack(mul2(f2pack(pa, pb), t2));
-            pk[e] = pack2(pa, pb, is_bf16);
-            dk[e] = pack2(d.x, d.y, is_bf16);
+            const float2 x = f2unpack(add2(f2pack(xs[0], xs[1]), f2pack(nl.x, nl.y)));
+            pf[c] = ex2(x.x);
+            pf[c + 1] = ex2(x.y);
+            pk[e] = pack2(pf[c], pf[c + 1], is_bf16);
           }
         }
-        __syncwarp();
-        if (C::KEYS && C::HAS_DV) tmem_st16(s_addr, pk);          // P^T for dV
-        if (C::HAS_DP) tmem_st16(MODE == kDqS ? s_addr : dp_addr, dk);  // dS (dK/dV: dS^T)
+        if (C::HAS_DV) {
+          __syncwarp();
+          tmem_st16(s_addr, pk);  // P^T for dV
+        }
+        if (C::P_EARLY) {
+          // P^T to the dV accumulation now, before dS^T
+          tmem_st_wait();
+          fence_before();
+          mbar_arrive(bar(C::B_P + b));
+        }
+        if (C::SPLIT && !dp_now) {
+          // dP ran while P was formed
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DP + b), (it / NBUF) & 1, abort_flag, p.err));
+          if (!ok) break;
+          fence_after();
+          __syncwarp();
+          tmem_ld32(dp_addr, dv);
+          tmem_ld_wait();
+          if (MODE == kDqS) {
+            fence_before();
+            mbar_arrive(bar(C::B_PF));
+          }
+        }
+        if (C::HAS_DP) {
+          // dS = P (dP - D)
+          uint32_t dk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = 2 * e;
+            const float2 nd = C::KEYS ? make_float2(lp[e].z, lp[e].w) : make_float2(row_nd, row_nd);
+            const uint64_t t2 = add2(f2pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                                     f2pack(nd.x, nd.y));
+            const float2 d = f2unpack(mul2(f2pack(pf[c], pf[c + 1]), t2));
+            dk[e] = pack2(d.x, d.y, is_bf16);
+          }
+          __syncwarp();
+          tmem_st16(MODE == kDqS ? s_addr : dp_addr, dk);  // dS (dK/dV: dS^T)
+        }
       }
+      if (!ok) break;
       if (BIAS == 2 && !cta_pure) mbar_arrive(bar(C::B_BE + it % C::NBS_));  // the slot may be refilled
       tmem_st_wait();
       fence_before();
-      mbar_arrive(bar(C::B_P + b));
+      mbar_arrive(bar((C::P_EARLY ? C::B_DS : C::B_P) + b));
     }
     // epilogue: the last item's last accumulation completes every MMA of the CTA
     if (ok && n_kept > 0)
