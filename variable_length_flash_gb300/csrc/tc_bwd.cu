@@ -94,8 +94,9 @@ struct BwdCfg {
   static constexpr int PAIRS = KEYS ? IR / 2 : 0;
   static constexpr int OFF_LD = OFF_IN1 + NSTAGE1 * I1_BYTES;
   // dK/dV with TMA-staged bias: per ring-0 slot the item's rows' finite-bias intervals as IR/2
-  // pairs {lo_c, hi_c, lo_c+1, hi_c+1} (bias bands; pure items are masked by them)
-  static constexpr int BD_BYTES = KEYS ? NSTAGE * PAIRS * 16 : 0;
+  // pairs {lo_c, hi_c, lo_c+1, hi_c+1} (bias bands; pure items are masked by them).  The bias
+  // is staged through TMA at QK widths up to 128 only.
+  static constexpr int BD_BYTES = KEYS && NQ_PAD <= 128 ? NSTAGE * PAIRS * 16 : 0;
   static constexpr int OFF_BD = OFF_LD + NSTAGE * PAIRS * 16;
   // dK/dV: per ring-0 slot the kept item's candidate index and flags (1: its rows are pure
   // 0 / -inf intervals, 2: every row sees every key of the tile) for the compute warps
@@ -1232,7 +1233,7 @@ cudaError_t bwd_shape256(const Params &p, cudaStream_t st, const cudaEvent_t *ev
   if ((e = mark(ev, 0, st)) != cudaSuccess) return e;
   if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDv, 256, 256, 64, 2, 2, 2, 0>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDv, 256, 256, 64, 2, 3, 2, 0>(p, st)) != cudaSuccess) return e;
   if ((e = launch_bwd<kDk, 256, 256, 64, 2, 2, 1, 0>(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
   if ((e = launch_bwd<kDqS, 256, 256, 64, 2, 2, 1, 0>(p, st)) != cudaSuccess) return e;
