@@ -193,6 +193,22 @@ def test_tile_skipping_is_exact(name, simt):
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("w", [
+    W.custom([2048, 1000], dtype="bf16", h_q=8, h_kv=2, d_qk=128, causal=True),
+    W.custom([2048, 700], dtype="bf16", h_q=4, d_qk=192, d_v=128, causal=True, scale=1 / 192 ** 0.5),
+    W.custom([1024, 300], dtype="bf16", h_q=4, d_qk=256, causal=True),
+    W.custom([1500], dtype="fp16", h_q=4, d_qk=64),
+], ids=["d128_gqa", "qk192", "d256", "d64_full"])
+def test_backward_is_deterministic(w):
+    """The kernels hand tiles and TMEM columns between warps through barriers only: repeated
+    calls on the same inputs give identical bits (a missing wait shows up as a difference)."""
+    x = W.make_inputs(w, seed=17, with_dout=True)
+    runs = [gpu_run(w, x) for _ in range(4)]
+    for r in runs[1:]:
+        for k in runs[0]:
+            assert torch.equal(runs[0][k], r[k]), k
+
+
 def test_fp32_tensor_core_path_is_taken_and_matches_simt():
     """fp32 at widths 32 / 64 runs the three-pass tf32 forward and backward; they and the SIMT
     fp32-FMA kernels all meet the fp32 gates against the oracle."""

@@ -255,7 +255,8 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
   // a kept item's flags: 1 its rows are pure 0 / -inf intervals (masked by them, no bias value
   // read), 2 besides, every one of its rows sees every key of this tile (no mask from the bias)
   auto item_flags = [&](const int4 &e) {
-    if ((BIAS != 2 && BIAS != 3) || !p.bias_rows || e.z < 0) return 0;
+    // (pure items are masked by their rows' intervals, staged per ring slot: BD_BYTES > 0)
+    if ((BIAS != 2 && BIAS != 3) || C::BD_BYTES == 0 || !p.bias_rows || e.z < 0) return 0;
     return 1 | ((e.z <= tile0 && e.w >= min(tile0 + 128, sq.kv_len)) ? 2 : 0);
   };
   int n_kept = n_items;
@@ -568,6 +569,9 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           // S reads ring 0 (Q or K), dP reads ring 1 (dO or V)
           ok = role == 0 ? wait_all(C::B_IF + m % NSTAGE, (m / NSTAGE) & 1)
                          : wait_all(C::B_IF1 + m % NSTAGE1, (m / NSTAGE1) & 1);
+          // P_EARLY: P^T(m) may go to the dV accumulation before dP(m) has been issued, so S(m)
+          // waits for the item's dO tile too (dV reads it)
+          if (C::P_EARLY && role == 0 && ok) ok = wait_all(C::B_IF1 + m % NSTAGE1, (m / NSTAGE1) & 1);
           if (!ok) break;
           if (MODE == kDqS && role == 1) {
             // the single dP buffer is free once the compute warps have loaded item m-1's dP
@@ -602,7 +606,8 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           if (!ok) break;
           fence_after();
           if (C::HAS_DV) {
-            // kDv: no dP product has waited for this item's dO tile; wait for it here
+            // kDv: no dP product has waited for this item's dO tile; wait for it here (dK/dV:
+            // the S issuer has, before S)
             if (MODE == kDv) {
               ok = wait_all(C::B_IF1 + n % NSTAGE1, (n / NSTAGE1) & 1);
               if (!ok) break;
@@ -708,14 +713,15 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
       // this CTA's rows are all pure intervals
       const bool use_vals = BIAS == 1 || (BIAS == 2 && !ipure && !cta_pure);
       const int h = item_head(n);
+      // SPLIT: has dP landed too (then it is loaded with S)?  (Observed before the fence that
+      // orders this thread's TMEM loads after it.)
+      const bool dp_now = C::SPLIT && __all_sync(0xffffffffu, mbar_test(bar(C::B_DP + b), (it / NBUF) & 1));
       fence_after();
       const float *brow = brow_dq;
       if (C::KEYS && BIAS == 1 && orow_ok) {
         const int bh = p.bias_heads == 1 ? 0 : h;
         brow = p.bias + (size_t)bh * p.max_kv + orow;  // + (q0 + i) * bias_heads * max_kv per column
       }
-      // SPLIT: has dP landed too (then it is loaded with S)?
-      const bool dp_now = C::SPLIT && __all_sync(0xffffffffu, mbar_test(bar(C::B_DP + b), (it / NBUF) & 1));
       const bool with_dp = C::HAS_DP && (!C::SPLIT || dp_now);
 #pragma unroll 1
       for (int ch = 0; ch < C::CHUNKS; ++ch) {
@@ -1253,7 +1259,8 @@ cudaError_t tc_backward(const Params &p, cudaStream_t st, const cudaEvent_t *ev)
   if (p.total_q == 0 || p.total_kv == 0) return simt_backward(p, st, ev);
   // A bias whose rows start 16-byte aligned streams through TMA in 64-row items (bias tiles take
   // a third of shared memory: the Q / dO and K / V rings are shallower); other bias shapes load
-  // their values from global memory in the compute threads.
+  // their values from global memory in the compute threads.  (Read into registers one item ahead
+  // instead, the dK/dV kernel's bias was slower: 40.2 against 35.8 ms on the per-head bias.)
   const bool bias_tma = p.bias != nullptr && p.max_kv % 4 == 0 &&
                         (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0 && p.d_qk <= 128;
   if (bias_tma) {
