@@ -83,7 +83,19 @@ struct BwdCfg {
   static constexpr int KB0 = (DQK + 63) / 64, KB1 = (DV + 63) / 64;
   static constexpr int NQ_PAD = KB0 * 64, NV_PAD = KB1 * 64;
   static constexpr int OBLK = 128 * 128, IBLK = IR * 128;  // bytes per 64-col block
-  static constexpr int O0_BYTES = KB0 * OBLK, O1_BYTES = MODE == kDv ? 0 : KB1 * OBLK;  // kDv: no V
+  // OT (the width-256 passes): the outer tile that is a product's A operand goes to TMEM (columns
+  // OTA on) -- K for the dV pass's S^T (OT_K), V for the dK pass's dP^T (OT_V) -- so that product
+  // reads only its inner tile from shared memory.  In the dK pass an item's S^T and dP^T share
+  // one 64-column region (SR): dP^T overwrites S^T once the compute warps have loaded it, dS^T
+  // overwrites dP^T, and the next item of the region waits for dK to have read dS^T; two regions
+  // fit beside the 256-column dK accumulator and V.  The tile lands in
+  // ring-0 slots 1 .. (its 64 KB), the compute warps copy their rows into TMEM, and those slots
+  // then take Q items: the rings get the tile's shared memory.
+  static constexpr bool OT_K = MODE == kDv && DQK == 256, OT_V = MODE == kDk;
+  static constexpr bool OT = OT_K || OT_V;
+  static constexpr int OT_KB = OT_K ? KB0 : KB1;  // 64-column blocks of the tile
+  static constexpr int O0_BYTES = OT_K ? 0 : KB0 * OBLK;
+  static constexpr int O1_BYTES = MODE == kDv || OT_V ? 0 : KB1 * OBLK;  // kDv: no V
   static constexpr int I0_BYTES = KB0 * IBLK, I1_BYTES = KB1 * IBLK;
   // two rings of inner tiles: ring 0 (Q for dK/dV, K for dQ; NSTAGE slots) and ring 1 (dO for
   // dK/dV, V for dQ; NSTAGE1 slots), each slot released as soon as its last reader is done
@@ -120,11 +132,13 @@ struct BwdCfg {
   static constexpr int B_IE1 = B_IF1 + NSTAGE1, B_S = B_IE1 + NSTAGE1;
   static constexpr int B_P = B_S + NBUF, B_D0 = B_P + NBUF, B_D = B_D0 + NBUF, B_DRAIN = B_D + NBUF;
   static constexpr int B_PF = B_DRAIN + 3;  // kDqS: the compute warps have loaded dP
-  static constexpr int B_QT = B_PF + 1;     // QT: the outer Q / dO rows are in TMEM (kDq)
+  static constexpr int B_QT = B_PF + 1;     // QT, OT: the outer tiles' rows are in TMEM
   static constexpr int B_BF = B_QT + 1, B_BE = B_BF + NBS;  // bias full / empty
   // dp_full[NBUF] (SPLIT: dP done), ds_ready[NBUF] (P_EARLY: dS^T written; p_ready then means P^T)
   static constexpr int B_DP = B_BE + NBS, B_DS = B_DP + NBUF;
-  static constexpr int NBAR = B_DS + NBUF;
+  // s_loaded[NBUF] (SR): the compute warps have loaded S from the region
+  static constexpr int B_SL = B_DS + NBUF;
+  static constexpr int NBAR = B_SL + NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // (no alignment slack: the dynamic shared window starts 1024-byte aligned, checked in-kernel)
   static constexpr int SMEM = OFF_MISC + 16;
@@ -134,8 +148,13 @@ struct BwdCfg {
   static constexpr uint32_t ACC1 = MODE == kDk ? 0 : 128;   // dK (dK/dV, kDk)
   static constexpr uint32_t BUF = MODE == kDkdv ? 128 + NQ_PAD
                                   : (MODE == kDv ? NV_PAD : (MODE == kDk || MODE == kDqS ? NQ_PAD : 256));
-  __host__ __device__ static constexpr uint32_t s_col(int b) { return MODE == kDqS ? BUF + IR * b : BUF + 2 * IR * b; }
-  __host__ __device__ static constexpr uint32_t dp_col(int b) { return MODE == kDqS ? BUF + NBUF * IR : BUF + 2 * IR * b + IR; }
+  static constexpr bool SR = MODE == kDk;
+  __host__ __device__ static constexpr uint32_t s_col(int b) {
+    return MODE == kDqS || MODE == kDv || SR ? BUF + IR * b : BUF + 2 * IR * b;  // (kDv: no dP columns)
+  }
+  __host__ __device__ static constexpr uint32_t dp_col(int b) {
+    return MODE == kDqS ? BUF + NBUF * IR : (SR ? BUF + IR * b : BUF + 2 * IR * b + IR);
+  }
   // kDq: the outer Q (QT_Q, widths up to 128) and dO (QT_DO) tiles are copied once into the
   // TMEM columns between the accumulator and the S / dP buffers, 16-bit pairs along the row, and
   // are the A operands of S and dP from there: those products then read only their inner K / V
@@ -159,7 +178,11 @@ struct BwdCfg {
   static constexpr bool SPLIT = HAS_DP && CHUNKS == 1;
   static constexpr bool P_EARLY = HAS_DV && HAS_DP;
   static_assert(!P_EARLY || SPLIT, "P^T released early needs the split form");
-  static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * 2 * IR) <= 512, "TMEM columns");
+  static_assert((MODE == kDqS ? BUF + (NBUF + 1) * IR : BUF + NBUF * (MODE == kDv || SR ? 1 : 2) * IR) <= 512,
+                "TMEM columns");
+  static constexpr uint32_t OTA = BUF + NBUF * (MODE == kDv || SR ? 1 : 2) * IR;  // OT: the tile's rows
+  static_assert(!OT || (OTA + OT_KB * 32 <= 512 && (NSTAGE - 1) * I0_BYTES >= OT_KB * OBLK),
+                "OT: TMEM columns of the tile, ring-0 slots that stage it");
   static_assert(SMEM <= 232448, "shared memory");
   static_assert((MODE != kDkdv || NV_PAD <= 128) && NV_PAD <= 256 && NQ_PAD <= 256 && DQK % 32 == 0 &&
                 DV % 32 == 0, "head widths");
@@ -301,6 +324,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
     for (int i = 0; i < 3; ++i) mbar_init(bar(C::B_DRAIN + i), 1);
     mbar_init(bar(C::B_PF), 256);
     mbar_init(bar(C::B_QT), 256);
+    for (int b = 0; b < NBUF; ++b) mbar_init(bar(C::B_SL + b), 256);
     for (int i = 0; i < NBS; ++i) { mbar_init(bar(C::B_BF + i), 1); mbar_init(bar(C::B_BE + i), 256); }
     for (int b = 0; b < NBUF; ++b) { mbar_init(bar(C::B_DP + b), 1); mbar_init(bar(C::B_DS + b), 256); }
     *abort_flag = 0;
@@ -340,15 +364,17 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
         }
         const int orow = (C::KEYS ? sq.k0 : sq.q0) + tile0;
         const int oh = C::KEYS ? hk : head_outer;  // head index inside the outer tensors
-        mbar_expect_tx(bar(C::B_OUT), C::O0_BYTES + C::O1_BYTES);
+        mbar_expect_tx(bar(C::B_OUT), C::O0_BYTES + C::O1_BYTES + (C::OT ? C::OT_KB * C::OBLK : 0));
+        const uint32_t sOT = sIn0 + C::I0_BYTES;  // OT: ring-0 slots 1 ..
         for (int c = 0; c < C::KB0; ++c) {
+          const uint32_t dst = (C::OT_K ? sOT : sO0) + c * C::OBLK;
           if (lat && c == 2)  // the rope block: K's from the (possibly shared) rope key, or Q's
-            tma_load_2d(sO0 + c * C::OBLK, &maps.outer0_rope, (C::KEYS ? rh : oh) * 64, orow, bar(C::B_OUT));
+            tma_load_2d(dst, &maps.outer0_rope, (C::KEYS ? rh : oh) * 64, orow, bar(C::B_OUT));
           else
-            tma_load_2d(sO0 + c * C::OBLK, &maps.outer0, oh * qw + 64 * c, orow, bar(C::B_OUT));
+            tma_load_2d(dst, &maps.outer0, oh * qw + 64 * c, orow, bar(C::B_OUT));
         }
-        for (int c = 0; c < (C::O1_BYTES > 0 ? C::KB1 : 0); ++c)  // (kDv reads no V)
-          tma_load_2d(sO1 + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
+        for (int c = 0; c < (C::O1_BYTES > 0 || C::OT_V ? C::KB1 : 0); ++c)  // (kDv reads no V)
+          tma_load_2d((C::OT_V ? sOT : sO1) + c * C::OBLK, &maps.outer1, oh * DV + 64 * c, orow, bar(C::B_OUT));
       }
       int issued0[NSTAGE] = {0}, issued1[NSTAGE1] = {0}, issuedb[C::NBS_] = {0};
       // dK/dV: -LSE (base 2; -inf for rows that see nothing or lie past the sequence, so P = 0)
@@ -435,9 +461,12 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           }
           if (!__shfl_sync(0xffffffffu, (int)wb, 0)) break;
         }
-        if (k >= NSTAGE) {
+        if (k >= NSTAGE || (C::OT && k == 1)) {
+          // (OT: slots 1 .. held the outer tile until the compute warps copied it into TMEM)
           bool w = true;
-          if (lane == 0) w = mbar_wait(bar(C::B_IE + st), ((k / NSTAGE) - 1) & 1, abort_flag, p.err);
+          if (lane == 0)
+            w = k >= NSTAGE ? mbar_wait(bar(C::B_IE + st), ((k / NSTAGE) - 1) & 1, abort_flag, p.err)
+                            : mbar_wait(bar(C::B_QT), 0, abort_flag, p.err);
           if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
         }
         if (C::KEYS) {
@@ -522,7 +551,8 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          if (C::QT_Q) mma_ts_w(s_cols(n), tmem + C::QA + 8 * kk, d_i0 + (ia >> 4), id_sp, kk > 0);
+          if (C::QT_Q || C::OT_K)
+            mma_ts_w(s_cols(n), tmem + (C::OT_K ? C::OTA : C::QA) + 8 * kk, d_i0 + (ia >> 4), id_sp, kk > 0);
           else mma_ss_w(s_cols(n), d_o0 + (oa >> 4), d_i0 + (ia >> 4), id_sp, kk > 0);
         }
       };
@@ -531,7 +561,8 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::OBLK + (kk & 3) * 32, ia = (kk >> 2) * C::IBLK + (kk & 3) * 32;
-          if (C::QT_DO) mma_ts_w(dp_cols(n), tmem + C::DOA + 8 * kk, d_i1 + (ia >> 4), id_sp, kk > 0);
+          if (C::QT_DO || C::OT_V)
+            mma_ts_w(dp_cols(n), tmem + (C::OT_V ? C::OTA : C::DOA) + 8 * kk, d_i1 + (ia >> 4), id_sp, kk > 0);
           else mma_ss_w(dp_cols(n), d_o1 + (oa >> 4), d_i1 + (ia >> 4), id_sp, kk > 0);
         }
       };
@@ -563,7 +594,7 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
       if (role < 2) {
         // products of item m, once its inner tile has landed and its TMEM columns are free
         // (QT: once the compute warps have copied the outer rows into TMEM)
-        ok = wait_all(C::QT ? C::B_QT : C::B_OUT, 0);
+        ok = wait_all(C::QT || (role == 0 ? C::OT_K : C::OT_V) ? C::B_QT : C::B_OUT, 0);
         for (int m = 0; m < n_kept && ok; ++m) {
           const int b = m % NBUF;
           // S reads ring 0 (Q or K), dP reads ring 1 (dO or V)
@@ -576,6 +607,9 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           if (MODE == kDqS && role == 1) {
             // the single dP buffer is free once the compute warps have loaded item m-1's dP
             if (m >= 1) ok = wait_all(C::B_PF, (m - 1) & 1);
+          } else if (C::SR && role == 1) {
+            // dP(m) overwrites S(m) in the item's region once the compute warps have loaded it
+            ok = wait_all(C::B_SL + b, (m / NBUF) & 1);
           } else if (m >= NBUF) {
             const int n = m - NBUF;  // the item that used these columns before
             const uint32_t par = (n / NBUF) & 1;
@@ -583,7 +617,9 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
               // S(m) overwrites the columns accumulation 0 (dK/dV, kDv) read P^T from; kDq, kDk:
               // they are free as soon as the compute warps have loaded them; kDqS: once the dQ
               // accumulation has read the dS written there
+              // (SR: the region is free once dK has read the dS written there)
               ok = C::HAS_DV ? wait_all(C::B_D0 + b, par)
+                             : C::SR ? wait_all(C::B_D + b, par)
                              : (MODE == kDq || MODE == kDk ? wait_all(C::B_P + b, par)
                                                            : wait_all(C::B_D + b, par));
             } else {
@@ -690,6 +726,29 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
       fence_before();
       mbar_arrive(bar(C::B_QT));
     }
+    if (C::OT && n_kept > 0) {
+      // this thread's row of the outer tile (the two halves take half of its 64-column blocks
+      // each) from ring-0 slots 1 .. into TMEM columns OTA on; the slots then take Q items
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_OUT), 0, abort_flag, p.err));
+      if (ok) {
+        const uint32_t src = sIn0 + C::I0_BYTES + r * 128;
+        constexpr int nbh = (C::OT_KB + 1) / 2;
+#pragma unroll 1
+        for (int c = half * nbh; c < min(C::OT_KB, (half + 1) * nbh); ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            lds_v4(src + c * C::OBLK + ((q ^ (r & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          __syncwarp();
+          tmem_st32(lane_addr + C::OTA + 32 * c, v);
+        }
+        tmem_st_wait();
+      }
+      // (these reads precede the TMA writes of Q items into the slots)
+      fence_proxy_async_smem();
+      fence_before();
+      mbar_arrive(bar(C::B_QT));
+    }
     for (int it = 0; it < n_kept && ok; ++it) {
       // it: the item's place in the pipeline (rings, buffers, barrier phases); n: which item it
       // is (query head and rows, dK/dV, from the producer's slot record; keys, dQ)
@@ -779,6 +838,11 @@ __device__ __forceinline__ void tc_bwd_body(const BwdMaps &maps, const Params &p
           }
         }
         tmem_ld_wait();
+        if (C::SR) {
+          // S is in registers: dP may overwrite its columns
+          fence_before();
+          mbar_arrive(bar(C::B_SL + b));
+        }
         if (MODE == kDqS && with_dp && ch == C::CHUNKS - 1) {
           // every dP column of the item is in registers: the next dP may overwrite them
           fence_before();
@@ -1239,8 +1303,8 @@ cudaError_t bwd_shape256(const Params &p, cudaStream_t st, const cudaEvent_t *ev
   if ((e = mark(ev, 0, st)) != cudaSuccess) return e;
   if ((e = rowdot_forward(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 1, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDv, 256, 256, 64, 2, 3, 2, 0>(p, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd<kDk, 256, 256, 64, 2, 2, 1, 0>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDv, 256, 256, 64, 2, 5, 2, 0>(p, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd<kDk, 256, 256, 64, 2, 3, 2, 0>(p, st)) != cudaSuccess) return e;
   if ((e = mark(ev, 2, st)) != cudaSuccess) return e;
   if ((e = launch_bwd<kDqS, 256, 256, 64, 2, 2, 1, 0>(p, st)) != cudaSuccess) return e;
   return mark(ev, 3, st);
