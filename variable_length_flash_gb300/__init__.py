@@ -289,6 +289,9 @@ def _bands_arg(bias_bands, bias, cu_seqlens_q, cu_seqlens_kv, stream):
     return bias_bands.data_ptr()
 
 
+_SPLITS = {}  # (shape, device) -> the library's split-KV part count
+
+
 def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_seqlen_kv=None,
                         scale=None, causal=False, window=0, bias=None, out=None, lse=None,
                         stream=None, flags=0, num_splits=None, workspace=None, bias_bands=None):
@@ -334,11 +337,19 @@ def vlf_attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_
         _req(lse, "lse", torch.float32)
     nseq = cu_seqlens_q.numel() - 1
     dt = _DTYPE[dtype]
+    dev = q.get_device()
     st_h = (stream.cuda_stream if stream is not None else
-            _raw_stream(q.get_device()) if _raw_stream is not None else _stream(None, q))
+            _raw_stream(dev) if _raw_stream is not None else _stream(None, q))
     if num_splits is None:
-        num_splits = _lib.vlf_fwd_num_splits(nseq, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
-                                             dqk, dv, dt, int(flags), 0)
+        # the library's part count depends on the shape and the device alone: remembered per
+        # (shape, device) so that a repeated call makes one foreign call, not two
+        key = (nseq, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, dqk, dv, dt, int(flags), dev)
+        num_splits = _SPLITS.get(key)
+        if num_splits is None:
+            num_splits = _lib.vlf_fwd_num_splits(nseq, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
+                                                 dqk, dv, dt, int(flags), 0)
+            if len(_SPLITS) < 4096:
+                _SPLITS[key] = num_splits
     if num_splits >= 2:
         need = vlf_attn_varlen_fwd_split_workspace_size(tq, hq, dv, int(num_splits))
         if workspace is None:
