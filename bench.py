@@ -472,12 +472,16 @@ def time_steps(prob, steps, stream, dev, world, flush_l2):
     n0 = vlf.vlf_launch_count()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    # the step time: events at the step boundaries only, so that a step's kernels follow one
+    # another directly as in a user's call (an event recorded between two kernels keeps the
+    # second from starting on the SMs the first one's last CTAs leave)
     t_start.record(stream)
     for i in range(steps):
         if flush_l2:
             flush_buf.zero_()  # (outside the step's own events)
         evs[i][0].record(stream)
-        prob.run(ev=evs[i], stream=stream)
+        prob.run(stream=stream)
+        evs[i][-1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     launches = vlf.vlf_launch_count() - n0
@@ -488,6 +492,15 @@ def time_steps(prob, steps, stream, dev, world, flush_l2):
         ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[-1]) for e in evs), world)
     else:
         ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / steps
+    # the stage times: as many steps again, with an event between stages
+    for i in range(steps):
+        if flush_l2:
+            flush_buf.zero_()
+        evs[i][0].record(stream)
+        prob.run(ev=evs[i], stream=stream)
+    torch.cuda.synchronize()
+    st = vlf.vlf_check_error()
+    assert st == 0, vlf.vlf_status_string(st)
     stage_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
                 for i, n in enumerate(prob.stages)}
     return ms_step, stage_ms, launches

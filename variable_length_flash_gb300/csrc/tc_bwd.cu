@@ -1156,17 +1156,30 @@ __device__ __forceinline__ bool bwd_cta_all_pure(const Params &p) {
 // The backward kernel.  With a TMA-staged bias (BIAS 2) and PST > 0, a CTA whose rows are all
 // 0 / -inf intervals runs the body without a bias ring instead (BIAS 3): its rings take the
 // shared memory of the bias tiles (PST / PST1 slots), as deep as the kernel without a bias.
+//
+// The backward kernels are launched with programmatic stream serialization (launch_bwd).  The
+// first key-tile kernel after the row-dot pass (dK/dV, or the width-256 dV pass) reads D, so it
+// waits for the kernel ahead before reading anything global; every backward kernel then lets the
+// next one be launched.  The kernels after it (the dK pass, dQ) read only the inputs and D -- no
+// output of the kernel just ahead -- so their CTAs start on the SMs the previous kernel's last
+// CTAs leave (D was complete before any CTA of that kernel allowed them to launch), and they wait
+// for it only at their end, so that their completion still implies its completion.
 template <int MODE, int DQK, int DV, int IR, int NBUF, int NSTAGE, int NSTAGE1, int NBS, bool BF16,
           int BIAS, int PST = 0, int PST1 = 0>
 __global__ void __launch_bounds__(384, 1)
 tc_bwd_kernel(const __grid_constant__ BwdMaps maps, const Params p) {
+  constexpr bool first = MODE == kDkdv || MODE == kDv;
+  if (first) pdl_wait();
+  pdl_trigger();
+  bool done = false;
   if constexpr (BIAS == 2 && PST > 0) {
     if (bwd_cta_all_pure<BwdCfg<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS>::KEYS, IR>(p)) {
       tc_bwd_body<MODE, DQK, DV, IR, NBUF, PST, PST1, 0, BF16, 3>(maps, p);
-      return;
+      done = true;
     }
   }
-  tc_bwd_body<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, BF16, BIAS>(maps, p);
+  if (!done) tc_bwd_body<MODE, DQK, DV, IR, NBUF, NSTAGE, NSTAGE1, NBS, BF16, BIAS>(maps, p);
+  if (!first) pdl_wait();
 }
 
 // NBS > 0: the problem's bias is staged through TMA (the caller checked that it can be); PST /
@@ -1242,8 +1255,19 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   }
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 384, smem, st>>>(m, pl);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(384);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *args[] = {&m, &pl};
+  e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kern), args);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
 }
