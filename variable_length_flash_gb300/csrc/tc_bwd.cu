@@ -14,10 +14,12 @@
 //          IR-key K / V items of its band: S = Q K^T, dP = dO V^T, dS in TMEM, dQ += dS K.
 // Item width IR: an MMA of 128 x N x 16 with both operands in shared memory runs at full rate
 // only for N >= 128 (at N = 64 it is limited by shared-memory bandwidth), but 128-row items
-// leave TMEM room for one S/dP buffer only.  Measured, two buffers of 64-row items win in both
-// kernels (the next item's products overlap this item's elementwise pass); the single-buffer
-// form serves the dK/dV kernel of the latent head (QK width 192), whose dK accumulator leaves
-// room for one buffer only.
+// leave TMEM room for one S/dP buffer only.  Measured, the dK/dV kernel runs two buffers of
+// 64-row items (the next item's products overlap this item's elementwise pass; the latent head,
+// QK width 192, whose dK accumulator leaves room for one buffer, runs one); the plain dQ kernel
+// runs 128-key items with dS written over S (two S buffers, one dP buffer: mode kDqS), and
+// 64-key items where a bias or the latent head takes the TMEM columns (kDq).  Width 256 splits
+// the key-tile work into a dV pass and a dK pass (kDv, kDk).
 // Warp roles (384 threads): warp 0 stages tiles with TMA and, with all its lanes, the item's LSE
 // and D columns into the same shared-memory stage; warps 1, 11 and 10 issue the S, dP and
 // accumulation MMAs (warp 1 also owns the TMEM allocation); warps 2-9 are two compute
@@ -26,9 +28,10 @@
 // MMA order: after item n's P / dS are ready its accumulations are issued; the products of the
 // item that next uses n's columns (n + NBUF) follow as soon as those columns are released: S
 // once accumulation 0 (dK/dV: dV += P^T dO) has read P^T (dQ: once the compute warps have read
-// S), dP once the last accumulation has read dS.  S and dP complete on separate barriers: the
-// compute warps form P from S while dP still runs, then wait for dP to form dS; in the dK/dV
-// kernel P^T goes to the dV accumulation before dS^T is formed.
+// S), dP once the last accumulation has read dS.  With one 32-column chunk per compute thread
+// (all but the 128-key dQ items) S and dP complete on separate barriers: the compute warps form
+// P from S while dP still runs, then wait for dP to form dS; in the dK/dV kernel P^T goes to the
+// dV accumulation before dS^T is formed.
 // Tiles outside the causal / window band are skipped (they contribute exact zeros).  Every wait
 // is bounded.
 #include <cudaTypedefs.h>
